@@ -1,0 +1,813 @@
+// C ABI of the SPD engine (declared in include/spd.h): handle, memory, and the enqueueing of
+// prefill, SPD cycles, plain AR steps and the host-side rollback.
+//
+// A cycle is enqueued as (SPD summary, 方法步骤详情 steps 1-5):
+//   draft stream  : anchor FC over the staircase rows -> Ls x (QKV, RoPE/KV append, attention,
+//                   o-proj, gate/up, down) on the draft rows                      (steps 2-4)
+//   main stream   : for s in 0..S-1: the same six launches over the stage diagonal (step 1)
+//   join, then    : vocab head (exiting token + draft row) -> control (verify / rollback, step 5)
+// With graphs enabled the whole cycle is captured once and replayed; all per-cycle state lives in
+// the device control block, so replays run back to back without host synchronisation.
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <string>
+#include <vector>
+
+#include "spd_internal.cuh"
+
+using namespace spd;
+
+namespace {
+
+constexpr int kBigRing = 1 << 30;
+thread_local std::string g_create_error;
+
+struct EvRec {
+  int kind;
+  cudaEvent_t a, b;
+};
+
+}  // namespace
+
+struct spd_handle {
+  spd_config cfg;
+  Dims D;
+  Bufs B;
+  LaunchCfg LC;
+  int esz = 2;
+  cudaStream_t s_main = nullptr, s_pdm = nullptr;
+  bool own_main = false;
+  cudaEvent_t ev_fork = nullptr, ev_join = nullptr, ev_t0 = nullptr, ev_t1 = nullptr;
+  std::vector<void*> allocs;
+  Act act_t{}, act_p{}, act_head{}, act_pf{}, act_pfp{};
+  float* p_z = nullptr;
+  int opts = SPD_OPT_GRAPHS | SPD_OPT_PDM_STREAM;
+  bool prefilled = false;
+  int P = 0;
+  cudaGraphExec_t g_cycle = nullptr;
+  cudaGraphExec_t g_ar = nullptr;
+  std::string err;
+  bool timing = false;
+  std::vector<EvRec> recs;
+  std::vector<cudaEvent_t> pool;
+  size_t pool_used = 0;
+  int64_t n_launch = 0;         // kernels enqueued (eager) or captured
+  int64_t graph_nodes_cycle = 0, graph_nodes_ar = 0;
+  int64_t launches[SPD_NUM_KINDS] = {0};
+  double ms[SPD_NUM_KINDS] = {0};
+  DevState* host_state = nullptr;  // pinned mirror
+};
+
+namespace {
+
+int fail(spd_handle* h, int code, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  if (h) h->err = buf; else g_create_error = buf;
+  return code;
+}
+
+#define SPD_CUDA(h, call)                                                                   \
+  do {                                                                                      \
+    cudaError_t e_ = (call);                                                                \
+    if (e_ != cudaSuccess) return fail((h), SPD_ECUDA, "%s: %s", #call, cudaGetErrorString(e_)); \
+  } while (0)
+
+template <typename T>
+T* dalloc(spd_handle* h, size_t count, cudaError_t* e) {
+  void* p = nullptr;
+  const size_t bytes = count * sizeof(T) + 16;
+  *e = cudaMalloc(&p, bytes);
+  if (*e != cudaSuccess) return nullptr;
+  *e = cudaMemset(p, 0, bytes);
+  h->allocs.push_back(p);
+  return reinterpret_cast<T*>(p);
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// ---- launch wrappers with optional per-kind event timing (eager mode only) ----
+cudaEvent_t pool_event(spd_handle* h) {
+  if (h->pool_used == h->pool.size()) {
+    cudaEvent_t e;
+    if (cudaEventCreate(&e) != cudaSuccess) return nullptr;
+    h->pool.push_back(e);
+  }
+  return h->pool[h->pool_used++];
+}
+
+struct Timed {
+  spd_handle* h;
+  int kind;
+  cudaStream_t s;
+  cudaEvent_t a = nullptr, b = nullptr;
+  Timed(spd_handle* h_, int k, cudaStream_t s_) : h(h_), kind(k), s(s_) {
+    h->n_launch += 1;
+    if (h->timing && h->pool_used + 2 <= 65536) {
+      a = pool_event(h);
+      b = pool_event(h);
+      if (a && b) cudaEventRecord(a, s);
+    }
+  }
+  ~Timed() {
+    if (a && b) {
+      cudaEventRecord(b, s);
+      h->recs.push_back({kind, a, b});
+    }
+  }
+};
+
+constexpr int kDraftKinds = 9;  // kinds 9..17: the same operators on the draft-module stack
+
+int run_gemv(spd_handle* h, int op, const Launch& lc, cudaStream_t s) {
+  static const int kind_of[] = {KK_QKV, KK_O, KK_GATEUP, KK_DOWN, KK_FC, KK_HEAD};
+  Timed tm(h, kind_of[op] + (lc.stack == 1 ? kDraftKinds : 0), s);
+  SPD_CUDA(h, launch_gemv(op, h->D, h->B, lc, h->LC, s));
+  return SPD_OK;
+}
+
+// one decoder layer for the rows a launch descriptor selects (6 launches)
+int enqueue_layer(spd_handle* h, Launch lc, cudaStream_t s) {
+  int rc;
+  if ((rc = run_gemv(h, OP_QKV, lc, s))) return rc;
+  const int off = lc.stack == 1 ? kDraftKinds : 0;
+  {
+    Timed tm(h, KK_ROPE + off, s);
+    SPD_CUDA(h, launch_rope(h->D, h->B, lc, s));
+  }
+  {
+    Timed tm(h, KK_ATTN + off, s);
+    SPD_CUDA(h, launch_attn(h->D, h->B, lc, h->LC, s));
+  }
+  if ((rc = run_gemv(h, OP_O, lc, s))) return rc;
+  if ((rc = run_gemv(h, OP_GATEUP, lc, s))) return rc;
+  return run_gemv(h, OP_DOWN, lc, s);
+}
+
+Launch mk(int kind, int stack, int sub, const Act& act, int pos0 = 0, int cnt = 0) {
+  Launch lc;
+  memset(&lc, 0, sizeof(lc));
+  lc.kind = kind; lc.stack = stack; lc.sub = sub; lc.pos0 = pos0; lc.cnt = cnt; lc.act = act;
+  return lc;
+}
+
+int enqueue_pdm(spd_handle* h, cudaStream_t s) {
+  int rc;
+  if ((rc = run_gemv(h, OP_FC, mk(LK_PDMROWS, 1, 0, h->act_p), s))) return rc;
+  for (int lp = 0; lp < h->D.Ls; ++lp)
+    if ((rc = enqueue_layer(h, mk(LK_PDMROWS, 1, lp, h->act_p), s))) return rc;
+  return SPD_OK;
+}
+
+int enqueue_cycle(spd_handle* h) {
+  int rc;
+  const bool pdm = !(h->opts & SPD_OPT_TARGET_ONLY);
+  const bool fork = pdm && (h->opts & SPD_OPT_PDM_STREAM);
+  cudaStream_t sm = h->s_main;
+  if (fork) {
+    SPD_CUDA(h, cudaEventRecord(h->ev_fork, sm));
+    SPD_CUDA(h, cudaStreamWaitEvent(h->s_pdm, h->ev_fork, 0));
+    if ((rc = enqueue_pdm(h, h->s_pdm))) return rc;
+    SPD_CUDA(h, cudaEventRecord(h->ev_join, h->s_pdm));
+  } else if (pdm) {
+    if ((rc = enqueue_pdm(h, sm))) return rc;
+  }
+  for (int s = 0; s < h->D.S; ++s)
+    if ((rc = enqueue_layer(h, mk(LK_DIAG, 0, s, h->act_t), sm))) return rc;
+  if (fork) SPD_CUDA(h, cudaStreamWaitEvent(sm, h->ev_join, 0));
+  if ((rc = run_gemv(h, OP_HEAD, mk(LK_DIAG, 0, 0, h->act_head), sm))) return rc;
+  Timed tm(h, KK_CTRL, sm);
+  SPD_CUDA(h, launch_control_cycle(h->D, h->B, sm));
+  return SPD_OK;
+}
+
+int enqueue_ar_step(spd_handle* h) {
+  int rc;
+  cudaStream_t sm = h->s_main;
+  for (int l = 0; l < h->D.L; ++l)
+    if ((rc = enqueue_layer(h, mk(LK_AR, 0, l, h->act_t), sm))) return rc;
+  if ((rc = run_gemv(h, OP_HEAD, mk(LK_AR, 0, 0, h->act_head), sm))) return rc;
+  Timed tm(h, KK_CTRL, sm);
+  SPD_CUDA(h, launch_control_ar(h->D, h->B, sm));
+  return SPD_OK;
+}
+
+void drop_graphs(spd_handle* h) {
+  if (h->g_cycle) cudaGraphExecDestroy(h->g_cycle);
+  if (h->g_ar) cudaGraphExecDestroy(h->g_ar);
+  h->g_cycle = h->g_ar = nullptr;
+}
+
+int capture(spd_handle* h, int (*fn)(spd_handle*), cudaGraphExec_t* out, int64_t* nodes) {
+  SPD_CUDA(h, cudaStreamBeginCapture(h->s_main, cudaStreamCaptureModeThreadLocal));
+  const bool saved = h->timing;
+  h->timing = false;
+  const int64_t n0 = h->n_launch;
+  const int rc = fn(h);
+  *nodes = h->n_launch - n0;
+  h->n_launch = n0;
+  h->timing = saved;
+  cudaGraph_t g = nullptr;
+  const cudaError_t e = cudaStreamEndCapture(h->s_main, &g);
+  if (rc) { if (g) cudaGraphDestroy(g); return rc; }
+  if (e != cudaSuccess) return fail(h, SPD_ECUDA, "graph capture: %s", cudaGetErrorString(e));
+  const cudaError_t e2 = cudaGraphInstantiate(out, g, 0);
+  cudaGraphDestroy(g);
+  if (e2 != cudaSuccess) return fail(h, SPD_ECUDA, "graph instantiate: %s", cudaGetErrorString(e2));
+  return SPD_OK;
+}
+
+int run_cycle(spd_handle* h) {
+  if ((h->opts & SPD_OPT_GRAPHS) && !h->timing) {
+    if (!h->g_cycle) {
+      const int rc = capture(h, enqueue_cycle, &h->g_cycle, &h->graph_nodes_cycle);
+      if (rc) return rc;
+    }
+    SPD_CUDA(h, cudaGraphLaunch(h->g_cycle, h->s_main));
+    h->n_launch += h->graph_nodes_cycle;
+    return SPD_OK;
+  }
+  return enqueue_cycle(h);
+}
+
+int run_ar(spd_handle* h) {
+  if ((h->opts & SPD_OPT_GRAPHS) && !h->timing) {
+    if (!h->g_ar) {
+      const int rc = capture(h, enqueue_ar_step, &h->g_ar, &h->graph_nodes_ar);
+      if (rc) return rc;
+    }
+    SPD_CUDA(h, cudaGraphLaunch(h->g_ar, h->s_main));
+    h->n_launch += h->graph_nodes_ar;
+    return SPD_OK;
+  }
+  return enqueue_ar_step(h);
+}
+
+int read_state(spd_handle* h) {
+  SPD_CUDA(h, cudaMemcpyAsync(h->host_state, h->B.st, sizeof(DevState), cudaMemcpyDeviceToHost,
+                              h->s_main));
+  SPD_CUDA(h, cudaStreamSynchronize(h->s_main));
+  return SPD_OK;
+}
+
+int state_error(spd_handle* h) {
+  const DevState& s = *h->host_state;
+  if (s.err & ERR_TIMEOUT)
+    return fail(h, SPD_ETIMEOUT, "a bounded device wait gave up (site %d)", s.err_where);
+  if (s.err & ERR_PDM_ROWS)
+    return fail(h, SPD_ESTATE, "draft-module cache out of step (t=%d, cached=%d); call spd_rollback",
+                s.t, s.pdm_len);
+  if (s.err)
+    return fail(h, SPD_ESTATE, "device error flag %d (site %d)", s.err, s.err_where);
+  return SPD_OK;
+}
+
+int copy_out(spd_handle* h, int32_t* out, int count) {
+  if (!out || count <= 0) return SPD_OK;
+  SPD_CUDA(h, cudaMemcpyAsync(out, h->B.seq + h->P + 1, sizeof(int32_t) * count, cudaMemcpyDefault,
+                              h->s_main));
+  SPD_CUDA(h, cudaStreamSynchronize(h->s_main));
+  return SPD_OK;
+}
+
+int generate(spd_handle* h, int32_t max_new, int32_t* out, int32_t* n_out, spd_stats* stats,
+             bool ar) {
+  if (!h) return SPD_EINVAL;
+  if (!h->prefilled) return fail(h, SPD_ESTATE, "generate before prefill");
+  if (max_new < 1) return fail(h, SPD_EINVAL, "max_new must be >= 1");
+  if (h->P + max_new + h->D.n + 1 > h->D.max_seq)
+    return fail(h, SPD_EINVAL, "P + max_new + n + 1 = %d exceeds max_seq %d",
+                h->P + max_new + h->D.n + 1, h->D.max_seq);
+  int rc;
+  const int64_t launches0 = h->n_launch;
+  SPD_CUDA(h, launch_begin_generate(h->D, h->B, max_new, h->s_main));
+  h->n_launch += 1;
+  if ((rc = read_state(h))) return rc;
+  if ((rc = state_error(h))) return rc;
+  const DevState s0 = *h->host_state;
+  SPD_CUDA(h, cudaEventRecord(h->ev_t0, h->s_main));
+  int committed = s0.v + 1 - s0.P;
+  while (committed < max_new) {
+    const int batch = max_new - committed;  // each cycle commits at most one token
+    for (int i = 0; i < batch; ++i)
+      if ((rc = ar ? run_ar(h) : run_cycle(h))) return rc;
+    if ((rc = read_state(h))) return rc;
+    if ((rc = state_error(h))) return rc;
+    committed = h->host_state->v + 1 - h->host_state->P;
+  }
+  SPD_CUDA(h, cudaEventRecord(h->ev_t1, h->s_main));
+  SPD_CUDA(h, cudaEventSynchronize(h->ev_t1));
+  if ((rc = copy_out(h, out, max_new))) return rc;
+  if (n_out) *n_out = out ? max_new : 0;
+  if (stats) {
+    float ms = 0.f;
+    cudaEventElapsedTime(&ms, h->ev_t0, h->ev_t1);
+    stats->cycles = h->host_state->cycles - s0.cycles;
+    stats->exits = h->host_state->exits - s0.exits;
+    stats->rejects = h->host_state->rejects - s0.rejects;
+    stats->committed = committed;
+    stats->device_ms = ms;
+    stats->kernel_launches = h->n_launch - launches0;
+  }
+  return SPD_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* spd_last_error(const spd_handle* h) {
+  return h ? h->err.c_str() : g_create_error.c_str();
+}
+
+void spd_destroy(spd_handle* h) {
+  if (!h) return;
+  if (h->s_main) cudaStreamSynchronize(h->s_main);
+  if (h->s_pdm) cudaStreamSynchronize(h->s_pdm);
+  drop_graphs(h);
+  for (void* p : h->allocs) cudaFree(p);
+  for (cudaEvent_t e : h->pool) cudaEventDestroy(e);
+  if (h->ev_fork) cudaEventDestroy(h->ev_fork);
+  if (h->ev_join) cudaEventDestroy(h->ev_join);
+  if (h->ev_t0) cudaEventDestroy(h->ev_t0);
+  if (h->ev_t1) cudaEventDestroy(h->ev_t1);
+  if (h->s_pdm) cudaStreamDestroy(h->s_pdm);
+  if (h->own_main && h->s_main) cudaStreamDestroy(h->s_main);
+  if (h->host_state) cudaFreeHost(h->host_state);
+  delete h;
+}
+
+int spd_create(const spd_config* cfg, const spd_weights* w, void* cuda_stream, spd_handle** out) {
+  if (out) *out = nullptr;
+  if (!cfg || !w || !out) return fail(nullptr, SPD_EINVAL, "NULL argument");
+  const spd_config& c = *cfg;
+  if (c.n_layers < 1 || c.d_model < 8 || c.n_heads < 1 || c.n_kv_heads < 1 || c.head_dim < 16 ||
+      c.d_ffn < 8 || c.vocab < 2 || c.n_stages < 1 || c.n_stages > SPD_MAX_STAGES ||
+      c.n_anchors < 1 || c.n_anchors > SPD_MAX_ANCHORS || c.max_seq < 4)
+    return fail(nullptr, SPD_EINVAL, "config value out of range");
+  if (c.n_layers % c.n_stages != 0)
+    return fail(nullptr, SPD_EINVAL, "n_stages=%d must divide n_layers=%d", c.n_stages, c.n_layers);
+  const int S = c.n_layers / c.n_stages;
+  if (c.pdm_layers < 1 || c.pdm_layers > S)
+    return fail(nullptr, SPD_EINVAL, "pdm_layers=%d must satisfy 1 <= Ls <= L/n = %d", c.pdm_layers, S);
+  if (c.anchors[0] != 0) return fail(nullptr, SPD_EINVAL, "anchors[0] must be 0 (the embedding)");
+  for (int i = 1; i < c.n_anchors; ++i)
+    if (c.anchors[i] <= c.anchors[i - 1])
+      return fail(nullptr, SPD_EINVAL, "anchors must increase strictly");
+  if (c.anchors[c.n_anchors - 1] > c.n_layers)
+    return fail(nullptr, SPD_EINVAL, "anchors must be <= n_layers");
+  if (c.n_heads % c.n_kv_heads != 0) return fail(nullptr, SPD_EINVAL, "n_heads %% n_kv_heads != 0");
+  if (c.head_dim % 16 != 0 || c.head_dim > 256)
+    return fail(nullptr, SPD_EINVAL, "head_dim must be a multiple of 16, <= 256");
+  if (c.d_model % 8 || c.d_ffn % 8) return fail(nullptr, SPD_EINVAL, "d_model and d_ffn must be multiples of 8");
+  if (c.dtype != SPD_DTYPE_F32 && c.dtype != SPD_DTYPE_BF16) return fail(nullptr, SPD_EINVAL, "bad dtype");
+  const int gq = c.n_heads / c.n_kv_heads;
+  if (kAttnQT * gq > 64) return fail(nullptr, SPD_EINVAL, "query heads per kv head too large");
+
+  spd_handle* h = new spd_handle();
+  h->cfg = c;
+  h->esz = c.dtype == SPD_DTYPE_BF16 ? 2 : 4;
+  Dims& D = h->D;
+  memset(&D, 0, sizeof(D));
+  D.L = c.n_layers; D.d = c.d_model; D.hq = c.n_heads; D.hkv = c.n_kv_heads; D.hd = c.head_dim;
+  D.ffn = c.d_ffn; D.V = c.vocab; D.n = c.n_stages; D.S = S; D.Ls = c.pdm_layers; D.m = c.n_anchors;
+  D.max_seq = c.max_seq; D.dtype = c.dtype; D.qkv_rows = (c.n_heads + 2 * c.n_kv_heads) * c.head_dim;
+  D.gq = gq; D.eps = c.norm_eps;
+  for (int i = 0; i < c.n_anchors; ++i) D.anchors[i] = c.anchors[i];
+  // f(k) = max{i : b_i <= lmax(k)}, lmax(k) = min(L, k*L/n)   (SPD summary, 核心方法)
+  for (int k = 0; k <= c.n_stages; ++k) {
+    const int lm = k * S < c.n_layers ? k * S : c.n_layers;
+    int f = 0;
+    for (int i = 0; i < c.n_anchors; ++i)
+      if (c.anchors[i] <= lm) f = i;
+    D.ftab[k] = f;
+  }
+  // weights
+  auto bad = [&](const void* p) { return p == nullptr || !aligned16(p); };
+  if (bad(w->embed) || bad(w->final_norm) || bad(w->lm_head) || bad(w->pdm_norm) || bad(w->pdm_lm_head) ||
+      !w->layers || !w->pdm_layers || !w->pdm_fc) {
+    delete h;
+    return fail(nullptr, SPD_EINVAL, "a weight pointer is NULL or not 16-byte aligned");
+  }
+  std::vector<LayerW> tl(c.n_layers), pl(c.pdm_layers);
+  auto conv = [&](const spd_layer_weights& s, LayerW& o) {
+    o.attn_norm = s.attn_norm; o.wq = s.wq; o.wk = s.wk; o.wv = s.wv; o.wo = s.wo;
+    o.ffn_norm = s.ffn_norm; o.wg = s.w_gate; o.wu = s.w_up; o.wd = s.w_down;
+    return !(bad(o.attn_norm) || bad(o.wq) || bad(o.wk) || bad(o.wv) || bad(o.wo) || bad(o.ffn_norm) ||
+             bad(o.wg) || bad(o.wu) || bad(o.wd));
+  };
+  for (int l = 0; l < c.n_layers; ++l)
+    if (!conv(w->layers[l], tl[l])) { delete h; return fail(nullptr, SPD_EINVAL, "target layer %d: bad pointer", l); }
+  for (int l = 0; l < c.pdm_layers; ++l)
+    if (!conv(w->pdm_layers[l], pl[l])) { delete h; return fail(nullptr, SPD_EINVAL, "draft layer %d: bad pointer", l); }
+  Bufs& B = h->B;
+  memset(&B, 0, sizeof(B));
+  for (int j = 0; j < c.n_anchors; ++j) {
+    B.fc[j] = w->pdm_fc[j];
+    if (B.fc[j] && !aligned16(B.fc[j])) { delete h; return fail(nullptr, SPD_EINVAL, "pdm_fc[%d] not aligned", j); }
+  }
+  for (int k = 0; k <= c.n_stages; ++k)
+    if (!B.fc[D.ftab[k]]) {
+      delete h;
+      return fail(nullptr, SPD_EINVAL, "pdm_fc[%d] is needed (depth %d) but NULL", D.ftab[k], k);
+    }
+  B.embed = w->embed; B.lm_head = w->lm_head; B.pdm_head = w->pdm_lm_head;
+  B.final_norm = (const float*)w->final_norm; B.pdm_norm = (const float*)w->pdm_norm;
+
+  cudaError_t e = cudaSuccess;
+  const int n = c.n_stages, d = c.d_model, m = c.n_anchors;
+  const size_t ms = c.max_seq, hd = c.head_dim;
+  const int PB = kPrefillBlock;
+#define ALLOC(ptr, T, count)                                                       \
+  do {                                                                             \
+    ptr = dalloc<T>(h, (count), &e);                                               \
+    if (e != cudaSuccess) {                                                        \
+      std::string msg = std::string("cudaMalloc: ") + cudaGetErrorString(e);       \
+      spd_destroy(h);                                                              \
+      return fail(nullptr, e == cudaErrorMemoryAllocation ? SPD_ENOMEM : SPD_ECUDA, "%s", msg.c_str()); \
+    }                                                                              \
+  } while (0)
+  LayerW *dtl, *dpl;
+  ALLOC(dtl, LayerW, c.n_layers);
+  ALLOC(dpl, LayerW, c.pdm_layers);
+  e = cudaMemcpy(dtl, tl.data(), sizeof(LayerW) * c.n_layers, cudaMemcpyHostToDevice);
+  if (e == cudaSuccess) e = cudaMemcpy(dpl, pl.data(), sizeof(LayerW) * c.pdm_layers, cudaMemcpyHostToDevice);
+  if (e != cudaSuccess) { spd_destroy(h); return fail(nullptr, SPD_ECUDA, "cudaMemcpy: %s", cudaGetErrorString(e)); }
+  B.tl = dtl; B.pl = dpl;
+  unsigned char *kc, *vc, *pkc, *pvc;
+  const size_t kv_t = (size_t)c.n_layers * c.n_kv_heads * ms * hd * h->esz;
+  const size_t kv_p = (size_t)c.pdm_layers * c.n_kv_heads * ms * hd * h->esz;
+  ALLOC(kc, unsigned char, kv_t); ALLOC(vc, unsigned char, kv_t);
+  ALLOC(pkc, unsigned char, kv_p); ALLOC(pvc, unsigned char, kv_p);
+  B.kc = kc; B.vc = vc; B.pkc = pkc; B.pvc = pvc;
+  ALLOC(B.st, DevState, 1);
+  ALLOC(B.seq, int, ms + 2);
+  ALLOC(B.trace, int, 2 * ms);
+  ALLOC(B.kvlen, int, c.n_layers);
+  ALLOC(B.ovr_ref, int, ms + 2);
+  ALLOC(B.ovr_mode, unsigned char, ms + 2);
+  ALLOC(B.resid, float, (size_t)(n + 1) * d);
+  ALLOC(B.anch, float, (size_t)(n + 1) * m * d);
+  float *rc_, *rs_;
+  ALLOC(rc_, float, ms * hd / 2);
+  ALLOC(rs_, float, ms * hd / 2);
+  B.rope_cos = rc_; B.rope_sin = rs_;
+  B.head_grid = gemv_head_grid(c.dtype);
+  ALLOC(B.head_part, float, (size_t)B.head_grid * 8);
+  ALLOC(B.logits, float, (size_t)2 * c.vocab);
+  const int qkvr = D.qkv_rows, hqd = c.n_heads * c.head_dim, f = c.d_ffn;
+  // target decode scratch
+  Act& T = h->act_t;
+  T.resid = B.resid; T.resid_ring = n + 1; T.anch = B.anch; T.anch_ring = n + 1;
+  ALLOC(T.qkv, float, (size_t)n * qkvr);
+  ALLOC(T.attn, float, (size_t)n * hqd);
+  ALLOC(T.u, float, (size_t)n * f);
+  const int part_rows_t = n > PB ? n : PB;
+  ALLOC(T.part, float, attn_part_floats(part_rows_t, c.n_heads, c.head_dim, c.max_seq));
+  ALLOC(T.tick, int, (size_t)kMaxTiles * c.n_kv_heads);
+  // draft rows
+  Act& Pm = h->act_p;
+  ALLOC(h->p_z, float, (size_t)(n + 2) * d);
+  Pm.resid = h->p_z; Pm.resid_ring = kBigRing; Pm.anch = nullptr;
+  ALLOC(Pm.qkv, float, (size_t)(n + 2) * qkvr);
+  ALLOC(Pm.attn, float, (size_t)(n + 2) * hqd);
+  ALLOC(Pm.u, float, (size_t)(n + 2) * f);
+  ALLOC(Pm.part, float, attn_part_floats(n + 2, c.n_heads, c.head_dim, c.max_seq));
+  ALLOC(Pm.tick, int, (size_t)kMaxTiles * c.n_kv_heads);
+  // head: target rows in the ring, draft row z in act.qkv
+  h->act_head = T;
+  h->act_head.qkv = h->p_z;
+  // prefill blocks
+  Act& F = h->act_pf;
+  ALLOC(F.resid, float, (size_t)PB * d);
+  F.resid_ring = kBigRing;
+  ALLOC(F.anch, float, (size_t)PB * m * d);
+  F.anch_ring = kBigRing;
+  ALLOC(F.qkv, float, (size_t)PB * qkvr);
+  ALLOC(F.attn, float, (size_t)PB * hqd);
+  ALLOC(F.u, float, (size_t)PB * f);
+  F.part = T.part; F.tick = T.tick;
+  Act& FP = h->act_pfp;
+  FP = F;
+  ALLOC(FP.resid, float, (size_t)PB * d);
+  FP.anch = F.anch;  // anchor source of the prefix rows for the draft FC
+#undef ALLOC
+  e = cudaMallocHost(reinterpret_cast<void**>(&h->host_state), sizeof(DevState));
+  if (e != cudaSuccess) { spd_destroy(h); return fail(nullptr, SPD_ENOMEM, "cudaMallocHost failed"); }
+  memset(h->host_state, 0, sizeof(DevState));
+
+  if (cuda_stream) {
+    h->s_main = reinterpret_cast<cudaStream_t>(cuda_stream);
+  } else {
+    e = cudaStreamCreate(&h->s_main);  // blocking: orders with the legacy default stream
+    h->own_main = true;
+  }
+  if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&h->s_pdm, cudaStreamNonBlocking);
+  if (e == cudaSuccess) e = cudaEventCreateWithFlags(&h->ev_fork, cudaEventDisableTiming);
+  if (e == cudaSuccess) e = cudaEventCreateWithFlags(&h->ev_join, cudaEventDisableTiming);
+  if (e == cudaSuccess) e = cudaEventCreate(&h->ev_t0);
+  if (e == cudaSuccess) e = cudaEventCreate(&h->ev_t1);
+  if (e == cudaSuccess) e = gemv_setup_attributes();
+  const size_t asm_ = attn_smem_bytes(D, true) > attn_smem_bytes(D, false) ? attn_smem_bytes(D, true)
+                                                                           : attn_smem_bytes(D, false);
+  if (e == cudaSuccess) e = attn_setup_attributes(asm_);
+  if (e == cudaSuccess) {
+    h->LC.sms = num_sms();
+    h->LC.gemv_grid = 0;
+    h->LC.attn_grid_decode = attn_grid(D, false);
+    h->LC.attn_grid_multi = attn_grid(D, true);
+    h->LC.debug_logits = 0;
+    e = launch_rope_tables(rc_, rs_, c.max_seq, c.head_dim, c.rope_theta, h->s_main);
+  }
+  if (e == cudaSuccess) e = cudaStreamSynchronize(h->s_main);
+  if (e != cudaSuccess) {
+    std::string msg = cudaGetErrorString(e);
+    spd_destroy(h);
+    return fail(nullptr, SPD_ECUDA, "setup: %s", msg.c_str());
+  }
+  *out = h;
+  return SPD_OK;
+}
+
+int spd_prefill(spd_handle* h, const int32_t* tokens, int32_t P, int32_t* first_token) {
+  if (!h) return SPD_EINVAL;
+  if (!tokens || P < 1) return fail(h, SPD_EINVAL, "need a prompt of >= 1 token");
+  if (P + h->D.n + 2 > h->D.max_seq) return fail(h, SPD_EINVAL, "prompt too long for max_seq");
+  for (int i = 0; i < P; ++i)
+    if (tokens[i] < 0 || tokens[i] >= h->D.V) return fail(h, SPD_EINVAL, "token %d out of range", i);
+  cudaStream_t s = h->s_main;
+  const Dims& D = h->D;
+  h->prefilled = false;
+  SPD_CUDA(h, cudaMemcpyAsync(h->B.seq + 1, tokens, sizeof(int32_t) * P, cudaMemcpyHostToDevice, s));
+  SPD_CUDA(h, cudaMemsetAsync(h->B.ovr_mode, 0, D.max_seq + 2, s));
+  SPD_CUDA(h, cudaMemsetAsync(h->B.st, 0, sizeof(DevState), s));
+  const int flags = (h->opts & SPD_OPT_TARGET_ONLY) ? SF_TARGET_ONLY : 0;
+  h->host_state->flags = flags;
+  SPD_CUDA(h, cudaMemcpyAsync(&h->B.st->flags, &h->host_state->flags, sizeof(int),
+                              cudaMemcpyHostToDevice, s));
+  SPD_CUDA(h, cudaStreamSynchronize(s));  // host_state is reused below
+  int rc, cnt = 0;
+  for (int p0 = 1; p0 <= P; p0 += kPrefillBlock) {
+    cnt = P - p0 + 1 < kPrefillBlock ? P - p0 + 1 : kPrefillBlock;
+    SPD_CUDA(h, launch_prefill_embed(D, h->B, h->act_pf.resid, h->act_pf.anch, p0, cnt, s));
+    for (int l = 0; l < D.L; ++l)
+      if ((rc = enqueue_layer(h, mk(LK_ROWS, 0, l, h->act_pf, p0, cnt), s))) return rc;
+    // draft-module prefix rows at depth n (cached verified features, SPD v3 App. A.1)
+    if ((rc = run_gemv(h, OP_FC, mk(LK_ROWS, 1, 0, h->act_pfp, p0, cnt), s))) return rc;
+    for (int lp = 0; lp < D.Ls; ++lp)
+      if ((rc = enqueue_layer(h, mk(LK_ROWS, 1, lp, h->act_pfp, p0, cnt), s))) return rc;
+  }
+  if ((rc = run_gemv(h, OP_HEAD, mk(LK_ROWS, 0, 0, h->act_pf, P - cnt + 1, cnt), s))) return rc;
+  SPD_CUDA(h, launch_prefill_finish(D, h->B, P, s));
+  h->P = P;
+  h->prefilled = true;
+  if (first_token) {
+    if ((rc = read_state(h))) return rc;
+    if ((rc = state_error(h))) return rc;
+    *first_token = h->host_state->pushed;
+  }
+  return SPD_OK;
+}
+
+int spd_cycle(spd_handle* h, spd_cycle_info* info) {
+  if (!h) return SPD_EINVAL;
+  if (!h->prefilled) return fail(h, SPD_ESTATE, "cycle before prefill");
+  int rc;
+  SPD_CUDA(h, launch_begin_generate(h->D, h->B, 0x7fffffff, h->s_main));
+  if ((rc = run_cycle(h))) return rc;
+  if (info) {
+    if ((rc = read_state(h))) return rc;
+    if ((rc = state_error(h))) return rc;
+    const DevState& s = *h->host_state;
+    info->t = s.t; info->a = s.a; info->v = s.v;
+    info->exited = s.last_exited; info->exit_pos = s.last_exit_pos; info->accepted = s.last_accept;
+    info->target_top1 = s.target_top1; info->pdm_top1 = s.pdm_top1; info->pdm_top2 = s.pdm_top2;
+    info->draft_token = s.draft; info->pushed_token = s.pushed;
+  }
+  return SPD_OK;
+}
+
+int spd_generate(spd_handle* h, int32_t max_new, int32_t* out, int32_t* n_out, spd_stats* stats) {
+  return generate(h, max_new, out, n_out, stats, false);
+}
+
+int spd_generate_ar(spd_handle* h, int32_t max_new, int32_t* out, int32_t* n_out, spd_stats* stats) {
+  return generate(h, max_new, out, n_out, stats, true);
+}
+
+int spd_rollback(spd_handle* h, int32_t keep_len, int32_t reseed_token) {
+  if (!h) return SPD_EINVAL;
+  if (!h->prefilled) return fail(h, SPD_ESTATE, "rollback before prefill");
+  int rc;
+  if ((rc = read_state(h))) return rc;
+  const int v = h->host_state->v;
+  if (keep_len < 1 || keep_len > v)
+    return fail(h, SPD_EINVAL, "keep_len %d outside 1..verified length %d", keep_len, v);
+  if (reseed_token < 0 || reseed_token >= h->D.V) return fail(h, SPD_EINVAL, "reseed token out of range");
+  if (keep_len + h->D.n + 2 > h->D.max_seq) return fail(h, SPD_EINVAL, "keep_len too large");
+  SPD_CUDA(h, cudaMemsetAsync(&h->B.st->err, 0, sizeof(int), h->s_main));
+  SPD_CUDA(h, launch_rollback(h->D, h->B, keep_len, reseed_token, h->s_main));
+  return SPD_OK;
+}
+
+int spd_set_draft_override(spd_handle* h, int32_t first_pos, int32_t count, const int32_t* ref,
+                           const uint8_t* modes) {
+  if (!h) return SPD_EINVAL;
+  if (count < 0 || first_pos < 1 || first_pos + count > h->D.max_seq + 2 || (count && (!ref || !modes)))
+    return fail(h, SPD_EINVAL, "override range outside 1..max_seq");
+  for (int i = 0; i < count; ++i) {
+    if (modes[i] > 2) return fail(h, SPD_EINVAL, "mode %d at %d", modes[i], i);
+    if (ref[i] < 0 || ref[i] >= h->D.V) return fail(h, SPD_EINVAL, "ref token out of range at %d", i);
+  }
+  if (!count) return SPD_OK;
+  SPD_CUDA(h, cudaMemcpyAsync(h->B.ovr_ref + first_pos, ref, sizeof(int32_t) * count,
+                              cudaMemcpyHostToDevice, h->s_main));
+  SPD_CUDA(h, cudaMemcpyAsync(h->B.ovr_mode + first_pos, modes, count, cudaMemcpyHostToDevice,
+                              h->s_main));
+  SPD_CUDA(h, cudaStreamSynchronize(h->s_main));
+  return SPD_OK;
+}
+
+int spd_set_options(spd_handle* h, int32_t flags) {
+  if (!h) return SPD_EINVAL;
+  if (flags & ~(SPD_OPT_GRAPHS | SPD_OPT_PDM_STREAM | SPD_OPT_TARGET_ONLY | SPD_OPT_DEBUG_LOGITS))
+    return fail(h, SPD_EINVAL, "unknown option bits");
+  SPD_CUDA(h, cudaStreamSynchronize(h->s_main));
+  if ((flags ^ h->opts) & (SPD_OPT_PDM_STREAM | SPD_OPT_TARGET_ONLY | SPD_OPT_DEBUG_LOGITS))
+    drop_graphs(h);
+  h->opts = flags;
+  h->LC.debug_logits = (flags & SPD_OPT_DEBUG_LOGITS) ? 1 : 0;
+  h->host_state->flags = (flags & SPD_OPT_TARGET_ONLY) ? SF_TARGET_ONLY : 0;
+  SPD_CUDA(h, cudaMemcpyAsync(&h->B.st->flags, &h->host_state->flags, sizeof(int),
+                              cudaMemcpyHostToDevice, h->s_main));
+  SPD_CUDA(h, cudaStreamSynchronize(h->s_main));
+  return SPD_OK;
+}
+
+size_t spd_dump_size(const spd_handle* h, int32_t what) {
+  if (!h) return 0;
+  const Dims& D = h->D;
+  switch (what) {
+    case SPD_DUMP_STATE: return sizeof(DevState);
+    case SPD_DUMP_RESID: return sizeof(float) * (D.n + 1) * D.d;
+    case SPD_DUMP_ANCHORS: return sizeof(float) * (D.n + 1) * D.m * D.d;
+    case SPD_DUMP_PDM_Z: return sizeof(float) * (D.n + 2) * D.d;
+    case SPD_DUMP_LOGITS: return sizeof(float) * 2 * D.V;
+    case SPD_DUMP_SEQ: return sizeof(int32_t) * (D.max_seq + 2);
+    case SPD_DUMP_TRACE: return sizeof(int32_t) * 2 * D.max_seq;
+    case SPD_DUMP_KVLEN: return sizeof(int32_t) * D.L;
+    default: return 0;
+  }
+}
+
+int spd_debug_dump(spd_handle* h, int32_t what, void* dst, size_t bytes) {
+  if (!h) return SPD_EINVAL;
+  const size_t want = spd_dump_size(h, what);
+  if (!want || bytes != want || !dst) return fail(h, SPD_EINVAL, "dump %d wants %zu bytes", what, want);
+  const void* src = nullptr;
+  switch (what) {
+    case SPD_DUMP_STATE: src = h->B.st; break;
+    case SPD_DUMP_RESID: src = h->B.resid; break;
+    case SPD_DUMP_ANCHORS: src = h->B.anch; break;
+    case SPD_DUMP_PDM_Z: src = h->p_z; break;
+    case SPD_DUMP_LOGITS: src = h->B.logits; break;
+    case SPD_DUMP_SEQ: src = h->B.seq; break;
+    case SPD_DUMP_TRACE: src = h->B.trace; break;
+    default: src = h->B.kvlen; break;
+  }
+  SPD_CUDA(h, cudaStreamSynchronize(h->s_main));
+  SPD_CUDA(h, cudaMemcpy(dst, src, bytes, cudaMemcpyDeviceToHost));
+  return SPD_OK;
+}
+
+int spd_time_kernels(spd_handle* h, int32_t enable) {
+  if (!h) return SPD_EINVAL;
+  SPD_CUDA(h, cudaStreamSynchronize(h->s_main));
+  h->timing = enable != 0;
+  return SPD_OK;
+}
+
+int spd_kernel_times(spd_handle* h, int64_t* launches, double* ms, int32_t n_kinds) {
+  if (!h || n_kinds < 0) return SPD_EINVAL;
+  SPD_CUDA(h, cudaDeviceSynchronize());
+  for (const EvRec& r : h->recs) {
+    float t = 0.f;
+    if (cudaEventElapsedTime(&t, r.a, r.b) == cudaSuccess) {
+      h->launches[r.kind] += 1;
+      h->ms[r.kind] += t;
+    }
+  }
+  h->recs.clear();
+  h->pool_used = 0;
+  for (int k = 0; k < n_kinds && k < SPD_NUM_KINDS; ++k) {
+    if (launches) launches[k] = h->launches[k];
+    if (ms) ms[k] = h->ms[k];
+    h->launches[k] = 0;
+    h->ms[k] = 0;
+  }
+  return SPD_OK;
+}
+
+int spd_cycle_bytes(const spd_handle* h, int32_t t, int32_t fill, int32_t exited, int32_t with_pdm,
+                    double* out, int32_t n_kinds) {
+  if (!h || !out || n_kinds < SPD_NUM_KINDS) return SPD_EINVAL;
+  const Dims& D = h->D;
+  const double e = h->esz;
+  for (int k = 0; k < SPD_NUM_KINDS; ++k) out[k] = 0.0;
+  const double qkv = (double)D.qkv_rows * D.d * e, wo = (double)D.d * D.hq * D.hd * e;
+  const double gu = 2.0 * D.ffn * D.d * e, dn = (double)D.d * D.ffn * e;
+  const double kvrow = 2.0 * D.hkv * D.hd * e;  // K and V of one position at one layer
+  const int a = fill < 0 ? 0 : (fill > D.n ? D.n : fill);
+  double kv = 0.0;
+  for (int j = 0; j < a; ++j) kv += (double)(t - j) * D.S * kvrow;
+  out[KK_QKV] = a * D.S * qkv;
+  out[KK_ROPE] = a * D.S * kvrow;
+  out[KK_ATTN] = kv;
+  out[KK_O] = a * D.S * wo;
+  out[KK_GATEUP] = a * D.S * gu;
+  out[KK_DOWN] = a * D.S * dn;
+  out[KK_HEAD] = exited ? (double)D.V * D.d * e : 0.0;
+  if (with_pdm) {  // draft-module kinds 9..17
+    const int o = 9;
+    out[o + KK_QKV] = D.Ls * qkv;
+    out[o + KK_O] = D.Ls * wo;
+    out[o + KK_GATEUP] = D.Ls * gu;
+    out[o + KK_DOWN] = D.Ls * dn;
+    out[o + KK_ATTN] = (double)t * D.Ls * kvrow;
+    bool used[SPD_MAX_ANCHORS] = {false};
+    for (int k = 0; k <= D.n; ++k) used[D.ftab[k]] = true;
+    for (int j = 0; j < D.m; ++j)
+      if (used[j]) out[o + KK_FC] += (double)D.d * (j + 1) * D.d * e;
+    out[KK_HEAD] += (double)D.V * D.d * e;  // the draft head rides in the same head launch
+  }
+  return SPD_OK;
+}
+
+size_t spd_attention_workspace_bytes(int32_t R, int32_t n_heads, int32_t n_kv_heads, int32_t head_dim,
+                                     int32_t max_pos) {
+  if (R < 1 || n_heads < 1 || n_kv_heads < 1 || head_dim < 16 || max_pos < 1) return 0;
+  return 256 + (size_t)kMaxTiles * n_kv_heads * sizeof(int) +
+         attn_part_floats(R, n_heads, head_dim, max_pos) * sizeof(float);
+}
+
+int spd_attention(const float* q, const void* k_cache, const void* v_cache, int32_t dtype,
+                  const int32_t* pos, int32_t R, int32_t n_heads, int32_t n_kv_heads, int32_t head_dim,
+                  int32_t max_seq, float* out, void* workspace, size_t ws_bytes, void* stream) {
+  if (!q || !k_cache || !v_cache || !pos || !out || !workspace || R < 1 || R > kMaxGroups - 2 ||
+      n_kv_heads < 1 || n_heads % n_kv_heads || head_dim % 16 || head_dim > 256 || max_seq < 1 ||
+      (dtype != SPD_DTYPE_F32 && dtype != SPD_DTYPE_BF16))
+    return fail(nullptr, SPD_EINVAL, "spd_attention: bad arguments");
+  if (ws_bytes < spd_attention_workspace_bytes(R, n_heads, n_kv_heads, head_dim, max_seq))
+    return fail(nullptr, SPD_EINVAL, "spd_attention: workspace too small");
+  Dims D;
+  memset(&D, 0, sizeof(D));
+  D.hq = n_heads; D.hkv = n_kv_heads; D.hd = head_dim; D.gq = n_heads / n_kv_heads;
+  D.max_seq = max_seq; D.dtype = dtype; D.qkv_rows = n_heads * head_dim;
+  Bufs B;
+  memset(&B, 0, sizeof(B));
+  Launch lc;
+  memset(&lc, 0, sizeof(lc));
+  lc.kind = LK_EXPLICIT; lc.cnt = R;
+  lc.act.qkv = const_cast<float*>(q);
+  lc.act.attn = out;
+  lc.act.tick = reinterpret_cast<int*>(workspace);
+  lc.act.part = reinterpret_cast<float*>(reinterpret_cast<unsigned char*>(workspace) + 256 +
+                                         (size_t)kMaxTiles * n_kv_heads * sizeof(int));
+  lc.act.pos_arr = pos;
+  lc.act.kc = k_cache; lc.act.vc = v_cache;
+  cudaError_t e = attn_setup_attributes(attn_smem_bytes(D, false));
+  if (e != cudaSuccess) return fail(nullptr, SPD_ECUDA, "%s", cudaGetErrorString(e));
+  LaunchCfg LC;
+  memset(&LC, 0, sizeof(LC));
+  LC.attn_grid_decode = attn_grid(D, false);
+  e = launch_attn(D, B, lc, LC, reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return fail(nullptr, SPD_ECUDA, "%s", cudaGetErrorString(e));
+  return SPD_OK;
+}
+
+int spd_grouped_gemv(const void* const* W, const float* const* x, float* const* y, int32_t G,
+                     int32_t rows, int32_t cols, int32_t dtype, const float* nw, float eps,
+                     void* stream) {
+  if (!W || !x || !y || G < 1 || G > kMaxGroups || rows < 1 || cols < 8 || cols % 8 ||
+      (dtype != SPD_DTYPE_F32 && dtype != SPD_DTYPE_BF16))
+    return fail(nullptr, SPD_EINVAL, "spd_grouped_gemv: bad arguments");
+  GemvExplicit ge;
+  memset(&ge, 0, sizeof(ge));
+  for (int g = 0; g < G; ++g) {
+    if (!aligned16(W[g]) || !aligned16(x[g]) || !W[g] || !x[g] || !y[g])
+      return fail(nullptr, SPD_EINVAL, "spd_grouped_gemv: pointer %d NULL or unaligned", g);
+    ge.W[g] = W[g]; ge.x[g] = x[g]; ge.y[g] = y[g];
+  }
+  if (nw && !aligned16(nw)) return fail(nullptr, SPD_EINVAL, "spd_grouped_gemv: norm weight unaligned");
+  ge.G = G; ge.rows = rows; ge.cols = cols; ge.nw = nw;
+  cudaError_t e = gemv_setup_attributes();
+  if (e == cudaSuccess) e = launch_gemv_explicit(ge, dtype, eps, 0, reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return fail(nullptr, SPD_ECUDA, "%s", cudaGetErrorString(e));
+  return SPD_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,313 @@
+// Internal types and device helpers shared by the SPD kernels and the C-ABI layer.
+//
+// Memory layout in HBM (all device-resident for the lifetime of a handle):
+//   target KV   [L ][Hkv][max_seq][hd]  (K and V separate), storage dtype
+//   draft KV    [Ls][Hkv][max_seq][hd]
+//   resid ring  [n+1][d]    fp32: residual stream of the n+1 trailing positions, row = pos % (n+1)
+//   anchor ring [n+1][m][d] fp32: h^(b_i) of those positions; row i = anchor b_i (b_0 = embedding)
+//   decode scratch (target): qkv [n][(Hq+2Hkv)hd], attn [n][Hq hd], u [n][ffn]
+//   draft rows (<= n+1 per cycle): z [n+2][d], qkv, attn, u
+//   prefill block scratch (PB rows): h, anchors [PB][m][d], z, qkv, attn, u
+//   rope tables cos/sin [max_seq][hd/2] fp32 (angles formed in fp64)
+//   control block (DevState), token sequence, verification trace, draft override arrays.
+#pragma once
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+#include "../../include/spd.h"
+
+namespace spd {
+
+constexpr int kMaxGroups = 34;      // >= n_stages + 2
+constexpr int kMaxTiles = 64;       // attention query tiles per launch
+constexpr int kPrefillBlock = 32;   // prompt rows per prefill pass
+constexpr int kAttnChunk = 128;     // keys per attention split (fixed: split count depends on length only)
+constexpr int kAttnQT = 8;          // query rows per attention tile for multi-row launches
+constexpr int kGemvTR = 4;          // rows per GEMV tile
+constexpr int kGemvConsumerWarps = 8;
+constexpr int kGemvThreads = (kGemvConsumerWarps + 1) * 32;
+constexpr int kGemvRingBytes = 96 * 1024;
+constexpr int kGemvMaxStages = 8;
+constexpr int kGemvMaxNV = 64;      // vectors per group (prefill block rows)
+constexpr int kAttnThreads = 256;
+
+// ------------------------------------------------------------------------------------------
+// control block
+// ------------------------------------------------------------------------------------------
+struct DevState {
+  int t, a, v, pdm_len;        // newest position, fill, verified length, draft cache length
+  int P, cycles, exits, rejects;
+  int err, done, max_commit, flags;
+  int last_exited, last_exit_pos, last_accept, target_top1;
+  int pdm_top1, pdm_top2, draft, pushed;
+  int err_where, pad0, pad1, pad2;
+};
+
+enum ErrCode { ERR_TIMEOUT = 1, ERR_PDM_ROWS = 2, ERR_BOUNDS = 4 };
+enum StateFlags { SF_TARGET_ONLY = 1 };
+
+struct LayerW {
+  const void *attn_norm, *wq, *wk, *wv, *wo, *ffn_norm, *wg, *wu, *wd;
+};
+
+struct Dims {
+  int L, d, hq, hkv, hd, ffn, V, n, S, Ls, m;
+  int max_seq, dtype, qkv_rows, gq;
+  int anchors[SPD_MAX_ANCHORS];
+  int ftab[SPD_MAX_STAGES + 1];
+  float eps;
+};
+
+struct Bufs {
+  DevState* st;
+  int* seq;          // [max_seq + 2]
+  int* trace;        // [2][max_seq]
+  int* kvlen;        // [L]
+  int* ovr_ref;      // [max_seq + 2]
+  unsigned char* ovr_mode;
+  float* resid;      // [(n+1)][d]
+  float* anch;       // [(n+1)][m][d]
+  void *kc, *vc, *pkc, *pvc;
+  const float *rope_cos, *rope_sin;
+  float* head_part;  // [grid][2][4]
+  float* logits;     // [2][V] (debug)
+  int head_grid;
+  const LayerW* tl;
+  const LayerW* pl;
+  const void* embed;
+  const void* lm_head;
+  const void* pdm_head;
+  const float* final_norm;
+  const float* pdm_norm;
+  const void* fc[SPD_MAX_ANCHORS];
+};
+
+// How the rows of one launch are formed from the control block.
+enum LaunchKind {
+  LK_DIAG = 0,     // target stage-diagonal sub-step `sub`: token at depth j runs layer j*S+sub
+  LK_PDMROWS = 1,  // draft rows pdm_len+1..t through draft layer `sub`
+  LK_ROWS = 2,     // explicit consecutive rows pos0..pos0+cnt-1 through layer `sub` of `stack`
+  LK_AR = 3,       // one token at position t through target layer `sub`
+  LK_EXPLICIT = 4  // stand-alone operator: caller-given rows
+};
+
+// Activation buffers a launch reads and writes.
+struct Act {
+  float* resid; int resid_ring;   // residual rows; ring size (huge = linear)
+  float* qkv;                     // [rows][qkv_rows]
+  float* attn;                    // [rows][hq*hd]
+  float* u;                       // [rows][ffn]
+  float* anch; int anch_ring;     // anchor rows [row][m][d] (target stacks only; may be null)
+  float* part; int* tick;         // attention split partials and tickets
+  const int* pos_arr;             // LK_EXPLICIT: positions
+  const void* kc; const void* vc; // LK_EXPLICIT: cache bases
+};
+
+struct Launch {
+  int kind, stack, sub, pos0, cnt;
+  Act act;
+};
+
+// ------------------------------------------------------------------------------------------
+// small device helpers
+// ------------------------------------------------------------------------------------------
+__device__ __forceinline__ float bf16_lo(uint32_t u) { return __uint_as_float(u << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t u) { return __uint_as_float(u & 0xFFFF0000u); }
+
+template <typename WT> struct WTraits;
+template <> struct WTraits<float> {
+  static constexpr int kVec = 4;  // elements per 16 bytes
+  __device__ static __forceinline__ void unpack(const uint4& q, float* f) {
+    f[0] = __uint_as_float(q.x); f[1] = __uint_as_float(q.y);
+    f[2] = __uint_as_float(q.z); f[3] = __uint_as_float(q.w);
+  }
+  __device__ static __forceinline__ float to_f(float x) { return x; }
+  __device__ static __forceinline__ float from_f(float x) { return x; }
+};
+template <> struct WTraits<__nv_bfloat16> {
+  static constexpr int kVec = 8;
+  __device__ static __forceinline__ void unpack(const uint4& q, float* f) {
+    f[0] = bf16_lo(q.x); f[1] = bf16_hi(q.x); f[2] = bf16_lo(q.y); f[3] = bf16_hi(q.y);
+    f[4] = bf16_lo(q.z); f[5] = bf16_hi(q.z); f[6] = bf16_lo(q.w); f[7] = bf16_hi(q.w);
+  }
+  __device__ static __forceinline__ float to_f(__nv_bfloat16 x) { return __bfloat162float(x); }
+  __device__ static __forceinline__ __nv_bfloat16 from_f(float x) { return __float2bfloat16_rn(x); }
+};
+
+__device__ __forceinline__ uint64_t globaltimer_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+// ---- mbarrier / bulk-copy PTX (sm_90+ forms, valid on sm_103a) ----
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+__device__ __forceinline__ void fence_mbar_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
+               "r"(bytes) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      " selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok) : "r"(smem_u32(bar)), "r"(parity) : "memory");
+  return ok != 0;
+}
+// Bounded wait: gives up after ~2 s of wall time and reports false.
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  for (uint32_t it = 0;; ++it) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((it & 255u) == 255u && globaltimer_ns() - t0 > 2000000000ull) return false;
+  }
+}
+__device__ __forceinline__ uint64_t l2_evict_first_policy() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+// 1-D bulk copy global -> shared, completion counted on `bar` (bytes % 16 == 0, both 16B aligned).
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar,
+                                         uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint "
+      "[%0], [%1], %2, [%3], %4;" ::"r"(smem_u32(dst)),
+      "l"(src), "r"(bytes), "r"(smem_u32(bar)), "l"(policy)
+      : "memory");
+}
+__device__ __forceinline__ void named_bar(int id, int nthreads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
+__device__ __forceinline__ void set_err(DevState* st, int code, int where) {
+  if (st == nullptr) return;
+  atomicOr(&st->err, code);
+  atomicCAS(&st->err_where, 0, where);
+}
+
+// top-2 with a total order: larger value first, lower index on ties
+struct Top2 {
+  float v1, v2;
+  int i1, i2;
+};
+__device__ __forceinline__ bool better(float va, int ia, float vb, int ib) {
+  return va > vb || (va == vb && ia < ib);
+}
+__device__ __forceinline__ void top2_init(Top2& t) {
+  t.v1 = -INFINITY; t.v2 = -INFINITY; t.i1 = 0x7fffffff; t.i2 = 0x7fffffff;
+}
+__device__ __forceinline__ void top2_push(Top2& t, float v, int i) {
+  if (better(v, i, t.v1, t.i1)) {
+    t.v2 = t.v1; t.i2 = t.i1; t.v1 = v; t.i1 = i;
+  } else if (better(v, i, t.v2, t.i2)) {
+    t.v2 = v; t.i2 = i;
+  }
+}
+__device__ __forceinline__ void top2_merge(Top2& a, const Top2& b) {
+  top2_push(a, b.v1, b.i1);
+  top2_push(a, b.v2, b.i2);
+}
+
+// Row-set of one launch: groups of consecutive rows that share a layer.
+struct RowGroup {
+  int layer, nv, pos0, vid0, rrow0;
+};
+
+// Fill `g` from the launch kind and the control block; returns the group count (0 if none).
+// Executed by one thread.  Sets an error flag for an out-of-step draft cache.
+__device__ __forceinline__ int build_rows(const Launch& lc, const Dims& D, DevState* st,
+                                          RowGroup* g) {
+  switch (lc.kind) {
+    case LK_DIAG: {
+      const int a = st->a, t = st->t;
+      for (int j = 0; j < a; ++j) {
+        g[j].layer = j * D.S + lc.sub; g[j].nv = 1; g[j].pos0 = t - j; g[j].vid0 = j;
+        g[j].rrow0 = (t - j) % (D.n + 1);
+      }
+      return a;
+    }
+    case LK_PDMROWS: {
+      const int R = st->t - st->pdm_len;
+      if (R < 1 || R > D.n + 1) {
+        set_err(st, ERR_PDM_ROWS, 100 + lc.sub);
+        return 0;
+      }
+      g[0].layer = lc.sub; g[0].nv = R; g[0].pos0 = st->pdm_len + 1; g[0].vid0 = 0; g[0].rrow0 = 0;
+      return 1;
+    }
+    case LK_ROWS:
+      g[0].layer = lc.sub; g[0].nv = lc.cnt; g[0].pos0 = lc.pos0; g[0].vid0 = 0; g[0].rrow0 = 0;
+      return 1;
+    case LK_AR:
+      g[0].layer = lc.sub; g[0].nv = 1; g[0].pos0 = st->t; g[0].vid0 = 0;
+      g[0].rrow0 = st->t % (D.n + 1);
+      return 1;
+    default:
+      return 0;
+  }
+}
+
+// ------------------------------------------------------------------------------------------
+// host-side launchers (implemented in the kernel translation units)
+// ------------------------------------------------------------------------------------------
+enum GemvOp { OP_QKV = 0, OP_O = 1, OP_GATEUP = 2, OP_DOWN = 3, OP_FC = 4, OP_HEAD = 5 };
+enum KernelKind { KK_QKV = 0, KK_ROPE = 1, KK_ATTN = 2, KK_O = 3, KK_GATEUP = 4, KK_DOWN = 5,
+                  KK_FC = 6, KK_HEAD = 7, KK_CTRL = 8 };
+
+struct GemvExplicit {  // stand-alone grouped GEMV
+  const void* W[kMaxGroups];
+  const float* x[kMaxGroups];
+  float* y[kMaxGroups];
+  int G, rows, cols;
+  const float* nw;
+};
+
+struct LaunchCfg {
+  int sms;
+  int gemv_grid;
+  int attn_grid_decode, attn_grid_multi;
+  int debug_logits;
+};
+
+cudaError_t launch_gemv(int op, const Dims& D, const Bufs& B, const Launch& lc,
+                        const LaunchCfg& cfg, cudaStream_t s);
+cudaError_t launch_gemv_explicit(const GemvExplicit& ge, int dtype, float eps, int grid,
+                                 cudaStream_t s);
+cudaError_t launch_rope(const Dims& D, const Bufs& B, const Launch& lc, cudaStream_t s);
+cudaError_t launch_attn(const Dims& D, const Bufs& B, const Launch& lc, const LaunchCfg& cfg,
+                        cudaStream_t s);
+size_t attn_smem_bytes(const Dims& D, bool multi);
+size_t attn_part_floats(int rows, int hq, int hd, int max_seq);
+cudaError_t gemv_setup_attributes();
+int gemv_head_grid(int dtype);
+int num_sms();
+cudaError_t attn_setup_attributes(size_t max_smem);
+int attn_grid(const Dims& D, bool multi);
+
+// control kernels
+cudaError_t launch_control_cycle(const Dims& D, const Bufs& B, cudaStream_t s);
+cudaError_t launch_control_ar(const Dims& D, const Bufs& B, cudaStream_t s);
+cudaError_t launch_prefill_embed(const Dims& D, const Bufs& B, float* h, float* anch, int pos0,
+                                 int cnt, cudaStream_t s);
+cudaError_t launch_prefill_finish(const Dims& D, const Bufs& B, int P, cudaStream_t s);
+cudaError_t launch_rollback(const Dims& D, const Bufs& B, int keep_len, int reseed,
+                            cudaStream_t s);
+cudaError_t launch_begin_generate(const Dims& D, const Bufs& B, int max_new, cudaStream_t s);
+cudaError_t launch_rope_tables(float* cosv, float* sinv, int max_seq, int hd, float theta,
+                               cudaStream_t s);
+
+}  // namespace spd

@@ -1,0 +1,240 @@
+"""End-to-end parity of the CUDA path with the oracle, through the C ABI.
+
+For each workload (seeded synthetic weights and prompt):
+* GPU plain AR vs the oracle teacher-forced on the GPU stream: every token equals the oracle's
+  argmax unless the oracle's top-2 gap is below 1e-2 (flagged near tie);
+* GPU SPD == GPU AR bit for bit (batch invariance), for several acceptance rates and raw drafts;
+* the verification trace is exactly the seeded coin set and the cycle count follows the refill
+  arithmetic;
+* cycle by cycle, state (t, a, v), residual and anchor rings, draft-module rows and the tokens at
+  each exit agree with the oracle's SPD run on the same drafts (max-abs relative error 1e-4 for the
+  fp32 workload, 2e-2 for bf16);
+* host rollback restores a state from which decoding repeats exactly.
+"""
+import numpy as np
+import pytest
+import torch
+
+import spd_inputs as si
+from oracle import model as om
+from oracle import spd as ospd
+
+from speculative_pipeline_decoding_gb300.binding import (DUMP_ANCHORS, DUMP_KVLEN, DUMP_PDM_Z,
+                                                        DUMP_RESID, DUMP_TRACE)
+
+pytestmark = pytest.mark.gpu
+NEAR_TIE = 1e-2
+
+
+@pytest.fixture(scope="module")
+def spd():
+    from speculative_pipeline_decoding_gb300 import build_ext
+    build_ext.build()
+    import speculative_pipeline_decoding_gb300 as spd
+    return spd
+
+
+SMALL_BF16 = si.Workload(
+    "small_bf16_gqa_n4",
+    si.ModelConfig(n_layers=8, d_model=512, n_heads=8, n_kv_heads=2, head_dim=64, d_ffn=1024,
+                   vocab=2048, dtype="bf16"),
+    n_stages=4, pdm_layers=2, anchors=(0, 2, 4, 6, 7), prompt_len=300, gen_len=48, alphas=(0.7,))
+
+
+def rel(a, b):
+    a, b = np.asarray(a, np.float64), np.asarray(b, np.float64)
+    return float(np.max(np.abs(a - b)) / max(1e-30, np.max(np.abs(b))))
+
+
+class Setup:
+    def __init__(self, spd, w, max_new=None):
+        self.w = w
+        self.G = max_new or w.gen_len
+        self.params = si.generate_weights(w, device="cuda")
+        self.cpu = {k: v.cpu() for k, v in self.params.items()}
+        self.prompt = si.prompt_tokens(w).tolist()
+        self.P = len(self.prompt)
+        self.eng = spd.Engine(spd.Config.from_workload(w, max_seq=self.P + self.G + w.n_stages + 2),
+                              self.params)
+        self.first = self.eng.prefill(self.prompt)
+        self.ar, _ = self.eng.generate_ar(self.G)
+        self.ar = self.ar.tolist()
+        self.models = ospd.build(w, self.cpu)
+
+    def modes(self, alpha):
+        P, G = self.P, self.G
+        first, last = P + 2, P + G
+        return first, self.ar[1:], si.override_modes(self.w.coin_seed, alpha, first, last)
+
+    def spd_run(self, alpha):
+        self.eng.rollback(self.P, self.first)
+        if alpha is not None:
+            first, ref, md = self.modes(alpha)
+            self.eng.set_draft_override(first, ref, md)
+        else:
+            self.eng.set_draft_override(self.P + 2, self.ar[1:], [0] * (self.G - 1))
+        toks, stats = self.eng.generate(self.G)
+        trace = self.eng.dump(DUMP_TRACE)
+        k = self.eng.state()["exits"]
+        return toks.tolist(), stats, trace[:, :k]
+
+
+def teacher_forced_check(models, prompt, stream):
+    target, _ = models
+    ref = om.greedy_ar(target, prompt, len(stream), forced=stream)
+    flagged = 0
+    for i, (g, o, gap) in enumerate(zip(stream, ref["tokens"], ref["gaps"])):
+        if g != o:
+            assert gap < NEAR_TIE, f"token {i}: gpu {g} oracle {o} gap {gap}"
+            flagged += 1
+    return flagged, ref
+
+
+def per_cycle_parity(S: Setup, alpha, n_cycles, tol):
+    """Run GPU and oracle SPD side by side on identical drafts; compare after every cycle."""
+    w, eng = S.w, S.eng
+    target, pdm = S.models
+    first, ref, md = S.modes(alpha)
+    eng.rollback(S.P, S.first)
+    eng.set_draft_override(first, ref, md)
+    modes = {q: m for q, m in zip(range(first, first + len(md)), md)}
+    refd = {q: r for q, r in zip(range(first, first + len(ref)), ref)}
+    run = ospd.SPDRun(target, pdm, w.n_stages, w.pdm_layers, w.anchors, S.prompt,
+                      S.P + S.G + w.n_stages + 2, modes, refd, record=True)
+    n, B = w.n_stages, list(w.anchors)
+    worst = {"resid": 0.0, "anch": 0.0, "pdm": 0.0}
+    for c in range(n_cycles):
+        info = run.cycle()
+        g = eng.cycle()
+        st = eng.state()
+        assert (st["t"], st["a"], st["v"]) == (run.t, run.a, run.v), (c, st, run.t, run.a, run.v)
+        if info["pdm_gap"] >= NEAR_TIE:
+            assert g["pdm_top1"] == info["pdm_top"][0], c
+        if info["exited"]:
+            assert g["exited"] == 1 and g["exit_pos"] == info["exit_pos"]
+            if info["target_gap"] >= NEAR_TIE:
+                assert g["target_top1"] == info["target_top"][0], c
+            assert g["accepted"] == int(info["accept"]), c
+        resid = eng.dump(DUMP_RESID)
+        for p, h in run.resid.items():
+            worst["resid"] = max(worst["resid"], rel(resid[p % (n + 1)], h))
+        anch = eng.dump(DUMP_ANCHORS)
+        for p in run.resid:
+            for b, vec in run.anchor[p].items():
+                worst["anch"] = max(worst["anch"], rel(anch[p % (n + 1), B.index(b)], vec))
+        z = eng.dump(DUMP_PDM_Z)
+        R = info["pdm_z"].shape[0]
+        worst["pdm"] = max(worst["pdm"], rel(z[:R], info["pdm_z"]))
+    for k, v in worst.items():
+        assert v < tol, (k, v)
+    return worst
+
+
+# ------------------------------------------------------------------------------------------------
+# tiny fp32 workload (full parity) and a small bf16 GQA workload
+# ------------------------------------------------------------------------------------------------
+@pytest.fixture(scope="module")
+def tiny_setup(spd):
+    return Setup(spd, si.WORKLOADS["tiny_f32_n2"])
+
+
+@pytest.fixture(scope="module")
+def small_setup(spd):
+    return Setup(spd, SMALL_BF16)
+
+
+def test_tiny_first_token_and_ar_stream_match_oracle(tiny_setup):
+    S = tiny_setup
+    flagged, ref = teacher_forced_check(S.models, S.prompt, S.ar)
+    assert S.ar[0] == S.first
+    assert flagged <= 2
+
+
+@pytest.mark.parametrize("alpha", [0.0, 0.7, 1.0, None])
+def test_tiny_spd_equals_ar_trace_equals_coins(tiny_setup, alpha):
+    S = tiny_setup
+    toks, stats, trace = S.spd_run(alpha)
+    assert toks == S.ar
+    assert list(trace[0]) == list(range(S.P + 2, S.P + S.G + 1))
+    if alpha is not None:
+        acc = [bool(x) for x in trace[1]]
+        assert acc == si.accept_mask(S.w.coin_seed, alpha, S.P + 2, S.P + S.G)
+        assert stats["cycles"] == ospd.expected_cycles(S.w.n_stages, acc)
+        assert stats["rejects"] == acc.count(False)
+
+
+def test_tiny_per_cycle_parity_with_oracle(tiny_setup):
+    worst = per_cycle_parity(tiny_setup, 0.7, 60, 1e-4)
+    print("tiny fp32 worst relative errors", worst)
+
+
+def test_small_bf16_ar_stream_matches_oracle(small_setup):
+    flagged, _ = teacher_forced_check(small_setup.models, small_setup.prompt, small_setup.ar)
+    assert flagged <= 3
+
+
+@pytest.mark.parametrize("alpha", [0.0, 0.7, None])
+def test_small_bf16_spd_equals_ar(small_setup, alpha):
+    S = small_setup
+    toks, stats, trace = S.spd_run(alpha)
+    assert toks == S.ar
+    if alpha is not None:
+        acc = [bool(x) for x in trace[1]]
+        assert acc == si.accept_mask(S.w.coin_seed, alpha, S.P + 2, S.P + S.G)
+        assert stats["cycles"] == ospd.expected_cycles(S.w.n_stages, acc)
+
+
+def test_small_bf16_per_cycle_parity_with_oracle(small_setup):
+    worst = per_cycle_parity(small_setup, 0.7, 40, 2e-2)
+    print("small bf16 worst relative errors", worst)
+
+
+def test_rollback_state_and_kv_lengths(tiny_setup):
+    S = tiny_setup
+    eng, n = S.eng, S.w.n_stages
+    first, ref, md = S.modes(0.0)  # every draft wrong: a reject at every exit
+    eng.rollback(S.P, S.first)
+    eng.set_draft_override(first, ref, md)
+    seen = 0
+    for _ in range(4 * n):
+        g = eng.cycle()
+        if g["exited"] and not g["accepted"]:
+            te = g["exit_pos"]
+            assert (g["t"], g["a"], g["v"]) == (te + 1, 1, te)
+            assert list(eng.dump(DUMP_KVLEN)) == [te] * S.w.model.n_layers
+            assert g["pushed_token"] == g["target_top1"]
+            seen += 1
+    assert seen >= 3
+    with pytest.raises(Exception):
+        eng.rollback(10 ** 6, 0)      # beyond the verified length
+    with pytest.raises(Exception):
+        eng.rollback(0, 0)
+
+
+# ------------------------------------------------------------------------------------------------
+# the 1.5B-class bf16 workload at full size (prompt 512, 256 tokens, n = 8, Ls = 4, alpha 0.8)
+# ------------------------------------------------------------------------------------------------
+@pytest.fixture(scope="module")
+def dense_setup(spd):
+    return Setup(spd, si.WORKLOADS["dense1.5b_bf16_n8"])
+
+
+def test_dense_full_size_spd_equals_ar_and_trace(dense_setup):
+    S = dense_setup
+    toks, stats, trace = S.spd_run(0.8)
+    assert toks == S.ar
+    acc = [bool(x) for x in trace[1]]
+    assert acc == si.accept_mask(S.w.coin_seed, 0.8, S.P + 2, S.P + S.G)
+    assert stats["cycles"] == ospd.expected_cycles(8, acc)
+
+
+def test_dense_full_size_sampled_tokens_match_oracle(dense_setup):
+    """Oracle teacher-forced on the first 16 GPU tokens (the oracle's cost grows with every token)."""
+    S = dense_setup
+    flagged, _ = teacher_forced_check(S.models, S.prompt, S.ar[:16])
+    assert flagged <= 1
+
+
+def test_dense_full_size_first_cycles_parity(dense_setup):
+    worst = per_cycle_parity(dense_setup, 0.8, 12, 2e-2)
+    print("dense1.5b bf16 worst relative errors", worst)
