@@ -779,13 +779,18 @@ int spd_attention(const float* q, const void* k_cache, const void* v_cache, int3
                                          (size_t)kMaxTiles * n_kv_heads * sizeof(int));
   lc.act.pos_arr = pos;
   lc.act.kc = k_cache; lc.act.vc = v_cache;
+  cudaGetLastError();  // start from a clean error state
   cudaError_t e = attn_setup_attributes(attn_smem_bytes(D, false));
-  if (e != cudaSuccess) return fail(nullptr, SPD_ECUDA, "%s", cudaGetErrorString(e));
+  if (e != cudaSuccess)
+    return fail(nullptr, SPD_ECUDA, "attention smem attribute (%zu B): %s", attn_smem_bytes(D, false),
+                cudaGetErrorString(e));
   LaunchCfg LC;
   memset(&LC, 0, sizeof(LC));
   LC.attn_grid_decode = attn_grid(D, false);
   e = launch_attn(D, B, lc, LC, reinterpret_cast<cudaStream_t>(stream));
-  if (e != cudaSuccess) return fail(nullptr, SPD_ECUDA, "%s", cudaGetErrorString(e));
+  if (e != cudaSuccess)
+    return fail(nullptr, SPD_ECUDA, "attention launch (grid %d): %s", LC.attn_grid_decode,
+                cudaGetErrorString(e));
   return SPD_OK;
 }
 

@@ -337,16 +337,17 @@ int attn_grid(const Dims& D, bool multi) {
   return num_sms() * (occ > 0 ? occ : 1);
 }
 
-// Allow the largest dynamic shared memory the device grants (never lowered by a later call).
+// Raise the kernels' dynamic shared-memory limit to `need` (never lowered by a later call).
 cudaError_t attn_setup_attributes(size_t need) {
-  int dev = 0, optin = 0;
-  cudaGetDevice(&dev);
-  cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
-  const int lim = optin - (int)sizeof(Tile) * kMaxTiles - 64;
-  if ((size_t)lim < need) return cudaErrorInvalidValue;
-  cudaError_t e = cudaFuncSetAttribute(attn_kernel<float>, cudaFuncAttributeMaxDynamicSharedMemorySize, lim);
+  static size_t current = 0;
+  if (need <= current) return cudaSuccess;
+  cudaError_t e = cudaFuncSetAttribute(attn_kernel<float>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)need);
   if (e != cudaSuccess) return e;
-  return cudaFuncSetAttribute(attn_kernel<__nv_bfloat16>, cudaFuncAttributeMaxDynamicSharedMemorySize, lim);
+  e = cudaFuncSetAttribute(attn_kernel<__nv_bfloat16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)need);
+  if (e == cudaSuccess) current = need;
+  return e;
 }
 
 cudaError_t launch_attn(const Dims& D, const Bufs& B, const Launch& lc, const LaunchCfg& cfg,
