@@ -274,7 +274,7 @@ def main_spd(args):
         toks, st = eng.generate_ar(G)
         return toks, st
 
-    def timed(fn, K, W, clocks=None):
+    def timed(fn, K, W, clocks=None, tag="spd_other"):
         for _ in range(W):
             fn()
         barrier(world)
@@ -283,6 +283,7 @@ def main_spd(args):
         if clocks:
             clocks.start()
         launches = 0
+        torch.cuda.nvtx.range_push(tag)
         e0.record(stream)
         last = None
         for _ in range(K):
@@ -290,6 +291,7 @@ def main_spd(args):
             launches += last[1]["kernel_launches"] + 1  # + the rollback kernel
         e1.record(stream)
         torch.cuda.synchronize()
+        torch.cuda.nvtx.range_pop()
         ck = clocks.stop() if clocks else None
         barrier(world)
         return e0.elapsed_time(e1), last, launches, ck
@@ -298,7 +300,7 @@ def main_spd(args):
     toks, _ = spd_step()
     lossless = toks.tolist() == ar_list
     clk = Clocks(local)
-    ms, (toks, st), launches, clocks = timed(spd_step, args.steps, args.warmup, clk)
+    ms, (toks, st), launches, clocks = timed(spd_step, args.steps, args.warmup, clk, tag="spd_timed")
     ms_max = max_over_ranks(ms, world)
     cycles = st["cycles"]
     value = world * args.steps * G / (ms_max / 1e3)
