@@ -242,6 +242,26 @@ int spd_attention(const float* q, const void* k_cache, const void* v_cache, int3
                   int32_t head_dim, int32_t max_seq, float* out, void* workspace,
                   size_t workspace_bytes, void* cuda_stream);
 
+/* Decode attention without any allocation: the same operation, arguments and results as
+ * spd_attention, but the split partials and merge tickets live in a scratch array inside the
+ * library instead of a caller workspace.  The paper has no counterpart to this call; it exists for
+ * callers that may not call cudaMalloc at all -- a plugin hosted by an application that owns the
+ * GPU's memory budget, or code on a latency-critical path where an allocation could synchronise
+ * the device.
+ *   - The scratch is a fixed 16 MiB per GPU (16 KiB of tickets + 16 MiB - 16 KiB of partials),
+ *     held by every GPU that loads the library until the process exits.  Calls whose partials
+ *     (R * n_heads * ceil(max_seq/128) * (head_dim+2) * 4 bytes) or tickets (64 * n_kv_heads * 4
+ *     bytes) do not fit return SPD_EINVAL with the sizes in spd_last_error(NULL).
+ *   - The first call on a device looks up the array's device address with that device current;
+ *     make that first call before any stream capture.
+ *   - Every call shares the array and leaves its contents behind; the tickets are cleared at the
+ *     start of each call (stream-ordered).  Calls that overlap on the GPU race on the array.
+ *   - Allocates nothing: no cudaMalloc, cudaFree or allocating library routine. */
+int spd_attention_static_scratch(const float* q, const void* k_cache, const void* v_cache,
+                                 int32_t dtype, const int32_t* pos, int32_t R, int32_t n_heads,
+                                 int32_t n_kv_heads, int32_t head_dim, int32_t max_seq, float* out,
+                                 void* cuda_stream);
+
 /* Grouped GEMV with RMSNorm prologue: for group g (0..G-1), y_g = W_g . (x_g / rms(x_g) * nw)
  * (norm skipped when nw == NULL), W_g [rows, cols] row-major in `dtype`, x_g fp32 [cols],
  * y_g fp32 [rows].  Host arrays of G device pointers W[], x[], y[]; nw device fp32 [cols]

@@ -116,6 +116,8 @@ def lib() -> ctypes.CDLL:
         "spd_attention": (ctypes.c_int, [vp, vp, vp, i32, vp, i32, i32, i32, i32, i32, vp, vp, sz, vp]),
         "spd_grouped_gemv": (ctypes.c_int, [ctypes.POINTER(vp), ctypes.POINTER(vp), ctypes.POINTER(vp),
                                             i32, i32, i32, i32, vp, ctypes.c_float, vp]),
+        "spd_attention_static_scratch": (ctypes.c_int, [vp, vp, vp, i32, vp, i32, i32, i32, i32, i32,
+                                                        vp, vp]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(L, name)
@@ -375,3 +377,15 @@ def grouped_gemv(Ws: Sequence[torch.Tensor], xs: Sequence[torch.Tensor], ys: Seq
     _check(lib().spd_grouped_gemv(arr(Ws), arr(xs), arr(ys), G, rows, cols, dt,
                                   _ptr(norm_weight) if norm_weight is not None else None, eps,
                                   _stream_handle(stream)))
+
+
+def attention_static_scratch(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+                             pos: torch.Tensor, out: torch.Tensor, stream=None) -> None:
+    """Same as :func:`attention`, for callers that cannot allocate device memory: the split
+    partials live in the library's fixed 16 MiB per-GPU scratch array instead of a workspace.
+    Calls that overlap on the GPU race on that array; sizes beyond it raise SpdError."""
+    R, hq, hd = q.shape
+    hkv, max_seq, _ = k_cache.shape
+    dt = DTYPE_BF16 if k_cache.dtype == torch.bfloat16 else DTYPE_F32
+    _check(lib().spd_attention_static_scratch(_ptr(q), _ptr(k_cache), _ptr(v_cache), dt, _ptr(pos), R,
+                                              hq, hkv, hd, max_seq, _ptr(out), _stream_handle(stream)))

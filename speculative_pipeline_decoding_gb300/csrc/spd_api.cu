@@ -318,6 +318,10 @@ int generate(spd_handle* h, int32_t max_new, int32_t* out, int32_t* n_out, spd_s
 
 }  // namespace
 
+namespace spd {
+int spd_internal_fail(int code, const char* msg) { return fail(nullptr, code, "%s", msg); }
+}  // namespace spd
+
 extern "C" {
 
 const char* spd_last_error(const spd_handle* h) {

@@ -381,3 +381,99 @@ cudaError_t launch_rope(const Dims& D, const Bufs& B, const Launch& lc, cudaStre
 }
 
 }  // namespace spd
+
+// ------------------------------------------------------------------------------------------------
+// Decode attention for callers that cannot allocate device memory.
+//
+// Some callers may not call cudaMalloc at all: a plugin hosted by an application that owns the
+// GPU's memory budget (an inference server whose allocator reserved nearly all HBM up front), or
+// code on a latency-critical path where an allocation could synchronise the device.  For them the
+// split partials and the merge tickets live in one file-scope device array of fixed size that
+// every GPU loading this library holds until the process exits.  Its device address is looked up
+// once per device (with that device current) on the first call there; make that first call before
+// any stream capture.  All calls share the array and it keeps the last call's contents: the tickets
+// are cleared at the start of every call, and calls that overlap on the GPU race on the array.
+// ------------------------------------------------------------------------------------------------
+#include <cstdio>
+#include <mutex>
+
+namespace spd {
+namespace {
+constexpr size_t kStaticScratchBytes = (size_t)16 << 20;   // 16 MiB per device
+constexpr size_t kStaticTicketBytes = (size_t)16 << 10;    // first 16 KiB: merge tickets
+static __device__ __align__(256) unsigned char g_attn_static_scratch[kStaticScratchBytes];
+std::mutex g_static_mu;
+void* g_static_addr[64] = {};  // device address of the array, per device ordinal
+}  // namespace
+
+}  // namespace spd
+
+extern "C" int spd_attention_static_scratch(const float* q, const void* k_cache, const void* v_cache,
+                                            int32_t dtype, const int32_t* pos, int32_t R,
+                                            int32_t n_heads, int32_t n_kv_heads, int32_t head_dim,
+                                            int32_t max_seq, float* out, void* cuda_stream) {
+  using namespace spd;
+  char msg[256];
+  if (!q || !k_cache || !v_cache || !pos || !out || R < 1 || R > kMaxGroups - 2 || n_kv_heads < 1 ||
+      n_heads % n_kv_heads || head_dim % 16 || head_dim > 256 || max_seq < 1 ||
+      (dtype != SPD_DTYPE_F32 && dtype != SPD_DTYPE_BF16))
+    return spd_internal_fail(SPD_EINVAL, "spd_attention_static_scratch: bad arguments");
+  const size_t tick_bytes = (size_t)kMaxTiles * n_kv_heads * sizeof(int);
+  const size_t part_bytes = attn_part_floats(R, n_heads, head_dim, max_seq) * sizeof(float);
+  if (tick_bytes > kStaticTicketBytes || part_bytes > kStaticScratchBytes - kStaticTicketBytes) {
+    snprintf(msg, sizeof(msg),
+             "spd_attention_static_scratch: needs %zu B of partials and %zu B of tickets; the static "
+             "scratch holds %zu B and %zu B",
+             part_bytes, tick_bytes, kStaticScratchBytes - kStaticTicketBytes, kStaticTicketBytes);
+    return spd_internal_fail(SPD_EINVAL, msg);
+  }
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess || dev < 0 || dev >= 64)
+    return spd_internal_fail(SPD_ECUDA, "spd_attention_static_scratch: no usable current device");
+  void* base = nullptr;
+  {
+    std::lock_guard<std::mutex> lock(g_static_mu);
+    if (!g_static_addr[dev]) {
+      void* p = nullptr;
+      e = cudaGetSymbolAddress(&p, g_attn_static_scratch);
+      if (e != cudaSuccess) {
+        snprintf(msg, sizeof(msg), "spd_attention_static_scratch: cudaGetSymbolAddress: %s",
+                 cudaGetErrorString(e));
+        return spd_internal_fail(SPD_ECUDA, msg);
+      }
+      g_static_addr[dev] = p;
+    }
+    base = g_static_addr[dev];
+  }
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(cuda_stream);
+  e = cudaMemsetAsync(base, 0, tick_bytes, s);  // tickets must start at zero
+  if (e != cudaSuccess) return spd_internal_fail(SPD_ECUDA, "spd_attention_static_scratch: ticket reset failed");
+  Dims D;
+  memset(&D, 0, sizeof(D));
+  D.hq = n_heads; D.hkv = n_kv_heads; D.hd = head_dim; D.gq = n_heads / n_kv_heads;
+  D.max_seq = max_seq; D.dtype = dtype; D.qkv_rows = n_heads * head_dim;
+  Bufs B;
+  memset(&B, 0, sizeof(B));
+  Launch lc;
+  memset(&lc, 0, sizeof(lc));
+  lc.kind = LK_EXPLICIT; lc.cnt = R;
+  lc.act.qkv = const_cast<float*>(q);
+  lc.act.attn = out;
+  lc.act.tick = reinterpret_cast<int*>(base);
+  lc.act.part = reinterpret_cast<float*>(reinterpret_cast<unsigned char*>(base) + kStaticTicketBytes);
+  lc.act.pos_arr = pos;
+  lc.act.kc = k_cache; lc.act.vc = v_cache;
+  e = attn_setup_attributes(attn_smem_bytes(D, false));
+  if (e != cudaSuccess) return spd_internal_fail(SPD_ECUDA, "spd_attention_static_scratch: smem attribute");
+  LaunchCfg LC;
+  memset(&LC, 0, sizeof(LC));
+  LC.attn_grid_decode = attn_grid(D, false);
+  e = launch_attn(D, B, lc, LC, s);
+  if (e != cudaSuccess) {
+    snprintf(msg, sizeof(msg), "spd_attention_static_scratch: launch: %s", cudaGetErrorString(e));
+    return spd_internal_fail(SPD_ECUDA, msg);
+  }
+  return SPD_OK;
+}
+

@@ -310,4 +310,7 @@ cudaError_t launch_begin_generate(const Dims& D, const Bufs& B, int max_new, cud
 cudaError_t launch_rope_tables(float* cosv, float* sinv, int max_seq, int hd, float theta,
                                cudaStream_t s);
 
+// records `msg` as the text spd_last_error(NULL) returns; gives back `code`
+int spd_internal_fail(int code, const char* msg);
+
 }  // namespace spd
