@@ -45,6 +45,8 @@ struct GG {
 struct GemvParams {
   int op;
   int explicit_mode;
+  int mma_ok;   // bf16 weights, every column count a multiple of 16 (tensor-core path allowed)
+  int max_nv;   // largest vector count a group of this launch can have
   int debug_logits;
   float eps;
   Dims D;
@@ -476,6 +478,559 @@ gemv_kernel(const __grid_constant__ GemvParams p) {
   }
 }
 
+// ------------------------------------------------------------------------------------------------
+// Single-vector engine (one input vector per group: the stage-diagonal step, plain AR, the heads,
+// the stand-alone operator).  A stage holds 32 weight rows x 2 KB (a 1024-column bf16 chunk) in a
+// 3-deep, 192 KB ring, one CTA per SM.  Each consumer warp owns whole rows of the tile (rows
+// w, w+8, ...): lane l multiplies the chunk's 16-byte column vectors l, l+32, ... with its slice of
+// the activation held in registers and reused over the warp's rows, partial sums stay in registers
+// across chunks, and a row ends with one xor-tree warp reduction.  No block-wide barrier is taken
+// while streaming, so the copy engine is the only thing the consumers wait for.  A row's result
+// depends only on the column count, not on the tile, the warp or the other groups of the launch.
+// ------------------------------------------------------------------------------------------------
+constexpr int k1Rows = 32;          // physical weight rows per stage
+constexpr int k1ChunkBytes = 2048;  // bytes of each row per stage
+constexpr int k1Stages = 3;
+constexpr int k1Ring = k1Stages * k1Rows * k1ChunkBytes;
+
+template <int OP, typename WT>
+__global__ void __launch_bounds__(kGemvThreads, 1)
+gemv1_kernel(const __grid_constant__ GemvParams p) {
+  extern __shared__ __align__(128) unsigned char ring[];
+  constexpr int NW = (OP == OP_GATEUP) ? 2 : 1;
+  constexpr int VEC = WTraits<WT>::kVec;
+  constexpr int ESZ = sizeof(WT);
+  constexpr int TR = k1Rows / NW;             // output rows per tile
+  constexpr int RPW = TR / 8;                 // output rows per consumer warp
+  constexpr int CW = k1ChunkBytes / ESZ;      // columns per chunk
+  constexpr int VPL = CW / VEC / 32;          // column vectors per lane per chunk
+  constexpr int STAGE = k1Rows * k1ChunkBytes;
+  constexpr int NCW = kGemvConsumerWarps;
+
+  __shared__ GG gg[kMaxGroups];
+  __shared__ int s_ng, s_total;
+  __shared__ __align__(8) uint64_t full_bar[k1Stages];
+  __shared__ __align__(8) uint64_t empty_bar[k1Stages];
+  __shared__ Top2 hred[NCW][2];
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  DevState* st = p.B.st;
+  if (tid == 0) {
+    const bool skip = !p.explicit_mode && (st->done || st->err);
+    const int ng = skip ? 0 : resolve_groups(p, gg);
+    int total = 0;
+    for (int i = 0; i < ng; ++i) {
+      gg[i].row_begin = total;
+      total += gg[i].rows;
+    }
+    s_ng = ng; s_total = total;
+    for (int i = 0; i < k1Stages; ++i) {
+      mbar_init(&full_bar[i], 1);
+      mbar_init(&empty_bar[i], NCW);
+    }
+    fence_mbar_init();
+  }
+  __syncthreads();
+  const int ng = s_ng;
+  if (ng == 0) {
+    if (OP == OP_HEAD && tid == 0) {
+      float* hp = p.B.head_part + (size_t)blockIdx.x * 8;
+      for (int k = 0; k < 2; ++k) {
+        hp[k * 4 + 0] = -INFINITY; hp[k * 4 + 1] = __int_as_float(0x7fffffff);
+        hp[k * 4 + 2] = -INFINITY; hp[k * 4 + 3] = __int_as_float(0x7fffffff);
+      }
+    }
+    return;
+  }
+  const long long total = s_total;
+  const int r_begin = (int)(total * blockIdx.x / gridDim.x);
+  const int r_end = (int)(total * (blockIdx.x + 1) / gridDim.x);
+
+  if (warp == NCW) {
+    // ------------------------------ producer warp ------------------------------
+    const uint64_t pol = l2_evict_first_policy();
+    uint32_t ctr = 0;
+    bool failed = false;
+    int g = 0;
+    for (int r = r_begin; r < r_end && !failed;) {
+      while (r >= gg[g].row_begin + gg[g].rows) ++g;
+      const GG& G = gg[g];
+      const int rl = r - G.row_begin;
+      const int tr = min(TR, min(r_end - r, G.rows - rl));
+      for (int c0 = 0; c0 < G.cols; c0 += CW) {
+        const uint32_t brow = (uint32_t)min(CW, G.cols - c0) * ESZ;
+        const int s = ctr % k1Stages;
+        if (ctr >= (uint32_t)k1Stages &&
+            !mbar_wait_bounded(&empty_bar[s], ((ctr / k1Stages) - 1) & 1)) {
+          if (lane == 0) set_err(st, ERR_TIMEOUT, 40 + OP);
+          failed = true;
+          break;
+        }
+        if (lane == 0) mbar_arrive_expect_tx(&full_bar[s], brow * tr * NW);
+        __syncwarp();
+        if (lane < tr * NW) {
+          const int wi = lane / tr, ri = lane % tr;
+          const int row = rl + ri;
+          const unsigned char* src;
+          if (NW == 2) {
+            src = (const unsigned char*)G.w[wi] + (size_t)row * G.cols * ESZ;
+          } else {
+            const int sg = row < G.seg1 ? 0 : (row < G.seg2 ? 1 : 2);
+            const int off = sg == 0 ? 0 : (sg == 1 ? G.seg1 : G.seg2);
+            src = (const unsigned char*)G.w[sg] + (size_t)(row - off) * G.cols * ESZ;
+          }
+          bulk_g2s(ring + (size_t)s * STAGE + (size_t)(wi * TR + ri) * k1ChunkBytes,
+                   src + (size_t)c0 * ESZ, brow, &full_bar[s], pol);
+        }
+        ++ctr;
+      }
+      r += tr;
+    }
+    if (failed && lane == 0) {
+      const uint32_t first = ctr > (uint32_t)k1Stages ? ctr - k1Stages : 0;
+      for (uint32_t c = first; c < ctr; ++c) mbar_wait_bounded(&full_bar[c % k1Stages], (c / k1Stages) & 1);
+    }
+    return;
+  }
+
+  // ------------------------------ consumer warps ------------------------------
+  uint32_t ctr = 0;
+  bool failed = false;
+  int g = 0, last_g = -1;
+  float rstd = 1.f;
+  Top2 loc[2];
+  top2_init(loc[0]);
+  top2_init(loc[1]);
+  const int V = p.D.V;
+  for (int r = r_begin; r < r_end;) {
+    while (r >= gg[g].row_begin + gg[g].rows) ++g;
+    const GG& G = gg[g];
+    const int rl = r - G.row_begin;
+    const int tr = min(TR, min(r_end - r, G.rows - rl));
+    const float* xr = G.x + (size_t)(G.xrow0 % G.xring) * G.xstride;
+    if (g != last_g) {
+      if (G.normw) {  // every warp forms the same rstd in the same order
+        float sq = 0.f;
+        for (int c = lane * 4; c < G.cols; c += 128) {
+          const float4 q = *reinterpret_cast<const float4*>(xr + c);
+          sq += q.x * q.x; sq += q.y * q.y; sq += q.z * q.z; sq += q.w * q.w;
+        }
+        sq = warp_sum(sq);
+        rstd = 1.0f / sqrtf(sq / (float)G.cols + p.eps);
+      }
+      last_g = g;
+    }
+    float acc[RPW][NW];
+#pragma unroll
+    for (int i = 0; i < RPW; ++i)
+#pragma unroll
+      for (int j = 0; j < NW; ++j) acc[i][j] = 0.f;
+    for (int c0 = 0; c0 < G.cols; c0 += CW) {
+      const int nvec = min(CW, G.cols - c0) / VEC;
+      const int s = ctr % k1Stages;
+      if (!failed && !mbar_wait_bounded(&full_bar[s], (ctr / k1Stages) & 1)) {
+        if (lane == 0) set_err(st, ERR_TIMEOUT, 50 + OP);
+        failed = true;
+      }
+      if (!failed) {
+        const unsigned char* sb = ring + (size_t)s * STAGE;
+        float xv[VPL][VEC];
+#pragma unroll
+        for (int j = 0; j < VPL; ++j) {
+          const int k = lane + 32 * j;
+          if (k < nvec) {
+            const int col = c0 + k * VEC;
+#pragma unroll
+            for (int e = 0; e < VEC; e += 4) {
+              const float4 q = *reinterpret_cast<const float4*>(xr + col + e);
+              xv[j][e] = q.x; xv[j][e + 1] = q.y; xv[j][e + 2] = q.z; xv[j][e + 3] = q.w;
+            }
+            if (G.normw) {
+#pragma unroll
+              for (int e = 0; e < VEC; e += 4) {
+                const float4 nw4 = *reinterpret_cast<const float4*>(G.normw + col + e);
+                xv[j][e] = xv[j][e] * rstd * nw4.x;
+                xv[j][e + 1] = xv[j][e + 1] * rstd * nw4.y;
+                xv[j][e + 2] = xv[j][e + 2] * rstd * nw4.z;
+                xv[j][e + 3] = xv[j][e + 3] * rstd * nw4.w;
+              }
+            }
+          }
+        }
+#pragma unroll
+        for (int i = 0; i < RPW; ++i) {
+          const int ri = warp + NCW * i;
+          if (ri < tr) {
+#pragma unroll
+            for (int wi = 0; wi < NW; ++wi) {
+              const unsigned char* rowp = sb + (size_t)(wi * TR + ri) * k1ChunkBytes;
+#pragma unroll
+              for (int j = 0; j < VPL; ++j) {
+                const int k = lane + 32 * j;
+                if (k < nvec) {
+                  const uint4 q = *reinterpret_cast<const uint4*>(rowp + k * 16);
+                  float wf[VEC];
+                  WTraits<WT>::unpack(q, wf);
+#pragma unroll
+                  for (int e = 0; e < VEC; ++e) acc[i][wi] = fmaf(wf[e], xv[j][e], acc[i][wi]);
+                }
+              }
+            }
+          }
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty_bar[s]);
+      ++ctr;
+    }
+    // epilogue: one warp reduction per row
+#pragma unroll
+    for (int i = 0; i < RPW; ++i) {
+      const int ri = warp + NCW * i;
+      if (ri < tr) {
+        float y[NW];
+#pragma unroll
+        for (int wi = 0; wi < NW; ++wi) y[wi] = warp_sum(acc[i][wi]);
+        if (lane == 0 && !failed) {
+          const int row = rl + ri;
+          if (OP == OP_HEAD) {
+            top2_push(loc[G.kind], y[0], row);
+            if (p.debug_logits) p.B.logits[(size_t)G.kind * V + row] = y[0];
+          } else {
+            float* yp = G.y + (size_t)(G.yrow0 % G.yring) * G.ystride + row;
+            if (OP == OP_GATEUP) {
+              *yp = (y[0] / (1.0f + expf(-y[0]))) * y[NW - 1];
+            } else if (OP == OP_O || OP == OP_DOWN) {
+              const float hn = *yp + y[0];
+              *yp = hn;
+              if (OP == OP_DOWN && G.anch) G.anch[(size_t)(G.arow0 % G.aring) * G.astride + row] = hn;
+            } else {
+              *yp = y[0];
+            }
+          }
+        }
+      }
+    }
+    r += tr;
+  }
+  if (OP == OP_HEAD) {
+    if (lane == 0) { hred[warp][0] = loc[0]; hred[warp][1] = loc[1]; }
+    named_bar(1, NCW * 32);
+    if (tid == 0) {
+      float* hp = p.B.head_part + (size_t)blockIdx.x * 8;
+      for (int k = 0; k < 2; ++k) {
+        Top2 m = hred[0][k];
+        for (int i = 1; i < NCW; ++i) top2_merge(m, hred[i][k]);
+        hp[k * 4 + 0] = m.v1; hp[k * 4 + 1] = __int_as_float(m.i1);
+        hp[k * 4 + 2] = m.v2; hp[k * 4 + 3] = __int_as_float(m.i2);
+      }
+    }
+  }
+}
+
+template <int OP, typename WT>
+int grid1_of() {
+  static int grid = 0;
+  if (grid == 0) {
+    int occ = 0;
+    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, gemv1_kernel<OP, WT>, kGemvThreads, k1Ring);
+    grid = num_sms() * (occ > 0 ? occ : 1);
+  }
+  return grid;
+}
+
+template <int OP, typename WT>
+cudaError_t launch1(const GemvParams& p, int grid, cudaStream_t s) {
+  if (grid <= 0) grid = grid1_of<OP, WT>();
+  gemv1_kernel<OP, WT><<<grid, kGemvThreads, k1Ring, s>>>(p);
+  return cudaGetLastError();
+}
+
+// ------------------------------------------------------------------------------------------------
+// Multi-vector engine on tensor cores (bf16 weights; draft-module rows and prefill blocks, where
+// up to 64 input vectors share each weight row).  y[row][v] = W[row,:] . x_v is a skinny dense
+// contraction, done with mma.sync m16n8k16 (bf16 x bf16 -> fp32): the weight tile is the A operand
+// (16 rows, loaded with ldmatrix from shared memory rows padded by 16 bytes so the 8 row addresses
+// of a matrix fall in distinct banks), the vectors are the B operand.  The fp32 activations are
+// split as x = hi + lo with hi = bf16(x), lo = bf16(x - hi), and both halves are multiplied into
+// the same fp32 accumulator, which keeps about 17 significant bits of every activation.
+// A tile is 16 output rows (x2 weights for gate/up); a stage carries 1536 columns of them; the 8
+// consumer warps take interleaved 16-column k-steps and their partial sums are added in warp order
+// once per tile.
+// ------------------------------------------------------------------------------------------------
+constexpr int kMColsNW = 1536;                 // columns x weights per stage
+constexpr int kMStages = 3;
+constexpr int kMPitchPad = 16;                 // bytes of padding per shared-memory row
+constexpr int kMMaxNT = 8;                     // n-tiles of 8 vectors (64 vectors)
+constexpr int kMStageBytes = 16 * (kMColsNW * 2 + 2 * kMPitchPad);
+constexpr int kMRing = kMStages * kMStageBytes;
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo_k, float hi_k) {
+  const __nv_bfloat162 v = __floats2bfloat162_rn(lo_k, hi_k);
+  return *reinterpret_cast<const uint32_t*>(&v);
+}
+
+__device__ __forceinline__ void ldmatrix_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
+                                            uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3) : "r"(addr));
+}
+
+__device__ __forceinline__ void mma_bf16(float* c, const uint32_t* a, uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+template <int OP, int NT>
+__global__ void __launch_bounds__(kGemvThreads, 1)
+gemvmma_kernel(const __grid_constant__ GemvParams p) {
+  extern __shared__ __align__(128) unsigned char ring[];
+  constexpr int NW = (OP == OP_GATEUP) ? 2 : 1;
+  constexpr int CW = kMColsNW / NW;                  // columns per stage
+  constexpr int PITCH = CW * 2 + kMPitchPad;         // bytes per shared-memory row
+  constexpr int NCW = kGemvConsumerWarps;
+  constexpr int NRED = NW * NT * 4;                  // accumulator floats per thread
+
+  __shared__ GG gg[kMaxGroups];
+  __shared__ int s_ng, s_total;
+  __shared__ __align__(8) uint64_t full_bar[kMStages];
+  __shared__ __align__(8) uint64_t empty_bar[kMStages];
+  __shared__ float rstd_s[kGemvMaxNV];
+  __shared__ float red[NCW][NRED][32];
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  DevState* st = p.B.st;
+  if (tid == 0) {
+    const bool skip = st->done || st->err;
+    const int ng = skip ? 0 : resolve_groups(p, gg);
+    int total = 0;
+    for (int i = 0; i < ng; ++i) {
+      gg[i].row_begin = total;
+      total += gg[i].rows;
+    }
+    s_ng = ng; s_total = total;
+    for (int i = 0; i < kMStages; ++i) {
+      mbar_init(&full_bar[i], 1);
+      mbar_init(&empty_bar[i], NCW);
+    }
+    fence_mbar_init();
+  }
+  __syncthreads();
+  if (s_ng == 0) return;
+  // spans of whole 16-row tiles
+  const long long tiles = (s_total + 15) / 16;
+  const int r_begin = (int)(tiles * blockIdx.x / gridDim.x) * 16;
+  const int r_end = min(s_total, (int)(tiles * (blockIdx.x + 1) / gridDim.x) * 16);
+
+  if (warp == NCW) {
+    const uint64_t pol = l2_evict_first_policy();
+    uint32_t ctr = 0;
+    bool failed = false;
+    int g = 0;
+    for (int r = r_begin; r < r_end && !failed;) {
+      while (r >= gg[g].row_begin + gg[g].rows) ++g;
+      const GG& G = gg[g];
+      const int rl = r - G.row_begin;
+      const int tr = min(16, min(r_end - r, G.rows - rl));
+      for (int c0 = 0; c0 < G.cols; c0 += CW) {
+        const uint32_t brow = (uint32_t)min(CW, G.cols - c0) * 2;
+        const int s = ctr % kMStages;
+        if (ctr >= (uint32_t)kMStages &&
+            !mbar_wait_bounded(&empty_bar[s], ((ctr / kMStages) - 1) & 1)) {
+          if (lane == 0) set_err(st, ERR_TIMEOUT, 60 + OP);
+          failed = true;
+          break;
+        }
+        if (lane == 0) mbar_arrive_expect_tx(&full_bar[s], brow * tr * NW);
+        __syncwarp();
+        if (lane < tr * NW) {
+          const int wi = lane / tr, ri = lane % tr;
+          const int row = rl + ri;
+          const unsigned char* src;
+          if (NW == 2) {
+            src = (const unsigned char*)G.w[wi] + (size_t)row * G.cols * 2;
+          } else {
+            const int sg = row < G.seg1 ? 0 : (row < G.seg2 ? 1 : 2);
+            const int off = sg == 0 ? 0 : (sg == 1 ? G.seg1 : G.seg2);
+            src = (const unsigned char*)G.w[sg] + (size_t)(row - off) * G.cols * 2;
+          }
+          bulk_g2s(ring + (size_t)s * kMStageBytes + (size_t)(wi * 16 + ri) * PITCH,
+                   src + (size_t)c0 * 2, brow, &full_bar[s], pol);
+        }
+        ++ctr;
+      }
+      r += tr;
+    }
+    if (failed && lane == 0) {
+      const uint32_t first = ctr > (uint32_t)kMStages ? ctr - kMStages : 0;
+      for (uint32_t c = first; c < ctr; ++c) mbar_wait_bounded(&full_bar[c % kMStages], (c / kMStages) & 1);
+    }
+    return;
+  }
+
+  // ------------------------------ consumer warps ------------------------------
+  const int gq = lane >> 2, tq = lane & 3;  // mma fragment coordinates
+  // ldmatrix row address of this lane: matrix (lane/8): rows 0-7 / 8-15, k 0-7 / 8-15
+  const int lm_row = (lane & 7) + 8 * ((lane >> 3) & 1);
+  const int lm_k = 8 * (lane >> 4);
+  uint32_t ctr = 0;
+  bool failed = false;
+  int g = 0, last_g = -1;
+  for (int r = r_begin; r < r_end;) {
+    while (r >= gg[g].row_begin + gg[g].rows) ++g;
+    const GG& G = gg[g];
+    const int rl = r - G.row_begin;
+    const int tr = min(16, min(r_end - r, G.rows - rl));
+    const int nv = G.nv;
+    if (g != last_g) {
+      if (G.normw) {
+        for (int v = warp; v < nv; v += NCW) {
+          const float* xr = G.x + (size_t)((G.xrow0 + v) % G.xring) * G.xstride;
+          float sq = 0.f;
+          for (int c = lane * 4; c < G.cols; c += 128) {
+            const float4 q = *reinterpret_cast<const float4*>(xr + c);
+            sq += q.x * q.x; sq += q.y * q.y; sq += q.z * q.z; sq += q.w * q.w;
+          }
+          sq = warp_sum(sq);
+          if (lane == 0) rstd_s[v] = 1.0f / sqrtf(sq / (float)G.cols + p.eps);
+        }
+      }
+      named_bar(1, NCW * 32);
+      last_g = g;
+    }
+    // this lane's B rows: vector n = nt*8 + gq
+    const float* xrow[NT];
+    float rsv[NT];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+      const int v = nt * 8 + gq;
+      xrow[nt] = v < nv ? G.x + (size_t)((G.xrow0 + v) % G.xring) * G.xstride : nullptr;
+      rsv[nt] = (v < nv && G.normw) ? rstd_s[v] : 1.f;
+    }
+    float acc[NW][NT][4];
+#pragma unroll
+    for (int i = 0; i < NW; ++i)
+#pragma unroll
+      for (int j = 0; j < NT; ++j)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) acc[i][j][e] = 0.f;
+    for (int c0 = 0; c0 < G.cols; c0 += CW) {
+      const int ksteps = min(CW, G.cols - c0) / 16;
+      const int s = ctr % kMStages;
+      if (!failed && !mbar_wait_bounded(&full_bar[s], (ctr / kMStages) & 1)) {
+        if (lane == 0) set_err(st, ERR_TIMEOUT, 70 + OP);
+        failed = true;
+      }
+      if (!failed) {
+        const uint32_t sb = smem_u32(ring + (size_t)s * kMStageBytes);
+        for (int ks = warp; ks < ksteps; ks += NCW) {
+          const int col = c0 + ks * 16;
+          uint32_t a[NW][4];
+#pragma unroll
+          for (int wi = 0; wi < NW; ++wi)
+            ldmatrix_x4(sb + (uint32_t)((wi * 16 + lm_row) * PITCH + (ks * 16 + lm_k) * 2), a[wi][0],
+                        a[wi][1], a[wi][2], a[wi][3]);
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt) {
+            float x0 = 0.f, x1 = 0.f, x2 = 0.f, x3 = 0.f;
+            if (xrow[nt]) {
+              const int k0 = col + 2 * tq;
+              const float2 u = *reinterpret_cast<const float2*>(xrow[nt] + k0);
+              const float2 w8 = *reinterpret_cast<const float2*>(xrow[nt] + k0 + 8);
+              x0 = u.x; x1 = u.y; x2 = w8.x; x3 = w8.y;
+              if (G.normw) {
+                const float2 n0 = *reinterpret_cast<const float2*>(G.normw + k0);
+                const float2 n8 = *reinterpret_cast<const float2*>(G.normw + k0 + 8);
+                x0 = x0 * rsv[nt] * n0.x; x1 = x1 * rsv[nt] * n0.y;
+                x2 = x2 * rsv[nt] * n8.x; x3 = x3 * rsv[nt] * n8.y;
+              }
+            }
+            const __nv_bfloat16 h0 = __float2bfloat16_rn(x0), h1 = __float2bfloat16_rn(x1);
+            const __nv_bfloat16 h2 = __float2bfloat16_rn(x2), h3 = __float2bfloat16_rn(x3);
+            const uint32_t bh0 = pack_bf16x2(__bfloat162float(h0), __bfloat162float(h1));
+            const uint32_t bh1 = pack_bf16x2(__bfloat162float(h2), __bfloat162float(h3));
+            const uint32_t bl0 = pack_bf16x2(x0 - __bfloat162float(h0), x1 - __bfloat162float(h1));
+            const uint32_t bl1 = pack_bf16x2(x2 - __bfloat162float(h2), x3 - __bfloat162float(h3));
+#pragma unroll
+            for (int wi = 0; wi < NW; ++wi) {
+              mma_bf16(acc[wi][nt], a[wi], bh0, bh1);
+              mma_bf16(acc[wi][nt], a[wi], bl0, bl1);
+            }
+          }
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty_bar[s]);
+      ++ctr;
+    }
+    // add the 8 warps' partial tiles in warp order, then the epilogue
+#pragma unroll
+    for (int i = 0; i < NW; ++i)
+#pragma unroll
+      for (int j = 0; j < NT; ++j)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) red[warp][(i * NT + j) * 4 + e][lane] = acc[i][j][e];
+    named_bar(1, NCW * 32);
+    for (int idx = tid; idx < 16 * nv; idx += NCW * 32) {
+      const int m = idx / nv, v = idx % nv;
+      if (m >= tr || failed) continue;
+      const int nt = v / 8, nn = v % 8;
+      const int ln = (m % 8) * 4 + nn / 2;
+      const int e = (m >= 8 ? 2 : 0) + (nn & 1);
+      float y[NW];
+#pragma unroll
+      for (int wi = 0; wi < NW; ++wi) {
+        float sum = 0.f;
+#pragma unroll
+        for (int w8 = 0; w8 < NCW; ++w8) sum += red[w8][(wi * NT + nt) * 4 + e][ln];
+        y[wi] = sum;
+      }
+      const int row = rl + m;
+      float* yp = G.y + (size_t)((G.yrow0 + v) % G.yring) * G.ystride + row;
+      if (OP == OP_GATEUP) {
+        *yp = (y[0] / (1.0f + expf(-y[0]))) * y[NW - 1];
+      } else if (OP == OP_O || OP == OP_DOWN) {
+        const float hn = *yp + y[0];
+        *yp = hn;
+        if (OP == OP_DOWN && G.anch) G.anch[(size_t)((G.arow0 + v) % G.aring) * G.astride + row] = hn;
+      } else {
+        *yp = y[0];
+      }
+    }
+    named_bar(1, NCW * 32);  // `red` is rewritten by the next tile
+    r += tr;
+  }
+}
+
+template <int OP, int NT>
+int gridm_of() {
+  static int grid = 0;
+  if (grid == 0) {
+    int occ = 0;
+    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, gemvmma_kernel<OP, NT>, kGemvThreads, kMRing);
+    grid = num_sms() * (occ > 0 ? occ : 1);
+  }
+  return grid;
+}
+
+template <int OP, int NT>
+cudaError_t launchm_nt(const GemvParams& p, cudaStream_t s) {
+  gemvmma_kernel<OP, NT><<<gridm_of<OP, NT>(), kGemvThreads, kMRing, s>>>(p);
+  return cudaGetLastError();
+}
+
+// n-tiles needed for the largest vector count of the launch: 1 (<= 8), 2 (<= 16), 3 (<= 24), 4 (<= 32)
+template <int OP>
+cudaError_t launchm(const GemvParams& p, int max_nv, cudaStream_t s) {
+  if (max_nv <= 8) return launchm_nt<OP, 1>(p, s);
+  if (max_nv <= 16) return launchm_nt<OP, 2>(p, s);
+  if (max_nv <= 24) return launchm_nt<OP, 3>(p, s);
+  return launchm_nt<OP, 4>(p, s);
+}
+
 // persistent grid: every SM holds as many CTAs as fit (registers, shared memory)
 template <int OP, typename WT, int NVB>
 int grid_of() {
@@ -497,7 +1052,9 @@ cudaError_t launch_one(const GemvParams& p, int grid, cudaStream_t s) {
 
 template <int OP, typename WT>
 cudaError_t launch_nv(const GemvParams& p, int grid, bool multi, cudaStream_t s) {
-  return multi ? launch_one<OP, WT, 4>(p, grid, s) : launch_one<OP, WT, 1>(p, grid, s);
+  if (!multi) return launch1<OP, WT>(p, grid, s);
+  if (sizeof(WT) == 2 && p.mma_ok) return launchm<OP>(p, p.max_nv, s);
+  return launch_one<OP, WT, 4>(p, grid, s);
 }
 
 template <typename WT>
@@ -508,7 +1065,7 @@ cudaError_t launch_op(const GemvParams& p, int grid, bool multi, cudaStream_t s)
     case OP_GATEUP: return launch_nv<OP_GATEUP, WT>(p, grid, multi, s);
     case OP_DOWN: return launch_nv<OP_DOWN, WT>(p, grid, multi, s);
     case OP_FC: return launch_nv<OP_FC, WT>(p, grid, multi, s);
-    default: return launch_one<OP_HEAD, WT, 1>(p, grid, s);
+    default: return launch1<OP_HEAD, WT>(p, grid, s);
   }
 }
 
@@ -517,15 +1074,36 @@ cudaError_t set_attr_one() {
   return cudaFuncSetAttribute(gemv_kernel<OP, WT, NVB>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                               kRing);
 }
+template <int OP, typename WT>
+cudaError_t set_attr1() {
+  return cudaFuncSetAttribute(gemv1_kernel<OP, WT>, cudaFuncAttributeMaxDynamicSharedMemorySize, k1Ring);
+}
+template <int OP>
+cudaError_t set_attrm() {
+  cudaError_t e;
+  if ((e = cudaFuncSetAttribute(gemvmma_kernel<OP, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize, kMRing)))
+    return e;
+  if ((e = cudaFuncSetAttribute(gemvmma_kernel<OP, 2>, cudaFuncAttributeMaxDynamicSharedMemorySize, kMRing)))
+    return e;
+  if ((e = cudaFuncSetAttribute(gemvmma_kernel<OP, 3>, cudaFuncAttributeMaxDynamicSharedMemorySize, kMRing)))
+    return e;
+  return cudaFuncSetAttribute(gemvmma_kernel<OP, 4>, cudaFuncAttributeMaxDynamicSharedMemorySize, kMRing);
+}
+
 template <typename WT>
 cudaError_t set_attr_wt() {
   cudaError_t e = cudaSuccess;
+  if (sizeof(WT) == 2) {
+    if ((e = set_attrm<OP_QKV>()) || (e = set_attrm<OP_O>()) || (e = set_attrm<OP_GATEUP>()) ||
+        (e = set_attrm<OP_DOWN>()) || (e = set_attrm<OP_FC>()))
+      return e;
+  }
 #define SPD_A(op)                                              \
-  if ((e = set_attr_one<op, WT, 1>()) != cudaSuccess) return e; \
+  if ((e = set_attr1<op, WT>()) != cudaSuccess) return e; \
   if ((e = set_attr_one<op, WT, 4>()) != cudaSuccess) return e;
   SPD_A(OP_QKV) SPD_A(OP_O) SPD_A(OP_GATEUP) SPD_A(OP_DOWN) SPD_A(OP_FC)
 #undef SPD_A
-  return set_attr_one<OP_HEAD, WT, 1>();
+  return set_attr1<OP_HEAD, WT>();
 }
 
 }  // namespace
@@ -542,7 +1120,7 @@ int num_sms() {
 }
 
 int gemv_head_grid(int dtype) {
-  return dtype == SPD_DTYPE_BF16 ? grid_of<OP_HEAD, __nv_bfloat16, 1>() : grid_of<OP_HEAD, float, 1>();
+  return dtype == SPD_DTYPE_BF16 ? grid1_of<OP_HEAD, __nv_bfloat16>() : grid1_of<OP_HEAD, float>();
 }
 
 cudaError_t gemv_setup_attributes() {
@@ -558,6 +1136,9 @@ cudaError_t launch_gemv(int op, const Dims& D, const Bufs& B, const Launch& lc,
   p.op = op; p.explicit_mode = 0; p.debug_logits = cfg.debug_logits; p.eps = D.eps;
   p.D = D; p.B = B; p.lc = lc;
   const bool multi = (lc.kind == LK_PDMROWS || lc.kind == LK_ROWS) && op != OP_HEAD;
+  p.max_nv = lc.kind == LK_PDMROWS ? D.n + 1 : (lc.kind == LK_ROWS ? lc.cnt : 1);
+  p.mma_ok = D.dtype == SPD_DTYPE_BF16 && D.d % 16 == 0 && D.ffn % 16 == 0 && (D.hq * D.hd) % 16 == 0 &&
+             p.max_nv <= 32;
   const int grid = op == OP_HEAD ? B.head_grid : 0;  // 0: the instantiation's persistent grid
   return D.dtype == SPD_DTYPE_BF16 ? launch_op<__nv_bfloat16>(p, grid, multi, s)
                                    : launch_op<float>(p, grid, multi, s);
@@ -569,8 +1150,8 @@ cudaError_t launch_gemv_explicit(const GemvExplicit& ge, int dtype, float eps, i
   memset(&p, 0, sizeof(p));
   p.op = OP_QKV; p.explicit_mode = 1; p.eps = eps; p.ge = ge;
   (void)grid;
-  return dtype == SPD_DTYPE_BF16 ? launch_one<OP_QKV, __nv_bfloat16, 1>(p, 0, s)
-                                 : launch_one<OP_QKV, float, 1>(p, 0, s);
+  return dtype == SPD_DTYPE_BF16 ? launch1<OP_QKV, __nv_bfloat16>(p, 0, s)
+                                 : launch1<OP_QKV, float>(p, 0, s);
 }
 
 }  // namespace spd
