@@ -321,9 +321,9 @@ def main_spd(args):
     ar_tps = max(3, args.steps // 2) * G / (ms_ar / 1e3)
 
     # --- target only (no draft module), and draft module serialised on the main stream ---
-    eng.set_options(B.OPT_GRAPHS | B.OPT_TARGET_ONLY)
+    eng.set_options(B.OPT_GRAPHS | B.OPT_PDL | B.OPT_TARGET_ONLY)
     ms_tgt, (toks_t, st_t), _, _ = timed(spd_step, max(3, args.steps // 2), 1)
-    eng.set_options(B.OPT_GRAPHS)
+    eng.set_options(B.OPT_GRAPHS | B.OPT_PDL)  # draft module as its own launches
     ms_ser, _, _, _ = timed(spd_step, max(3, args.steps // 2), 1)
     Kx = max(3, args.steps // 2)
     t_cycle = ms_step / cycles
@@ -336,7 +336,7 @@ def main_spd(args):
     spd_step()
     kt = eng.kernel_times()
     eng.time_kernels(False)
-    eng.set_options(B.OPT_GRAPHS | B.OPT_PDM_STREAM)
+    eng.set_options(B.OPT_DEFAULT)
     pdm_alone = sum(v[1] for k, v in kt.items() if k.startswith("draft_")) / cycles
     dom = max((k for k in B.KIND_NAMES if not k.startswith("draft_")),
               key=lambda k: kt[k][1])

@@ -57,8 +57,10 @@ enum { SPD_DTYPE_F32 = 0, SPD_DTYPE_BF16 = 1 };
  *   n_stages | n_layers; 1 <= pdm_layers <= n_layers/n_stages (the masking condition of the
  *   SPD summary 核心方法: the PDM fits inside one stage forward);
  *   anchors strictly increasing, anchors[0] == 0, anchors[n_anchors-1] <= n_layers;
- *   n_heads % n_kv_heads == 0; head_dim even and a multiple of 8 (<= 256); d_model, d_ffn and
- *   n_heads*head_dim multiples of 8 (16-byte rows for bulk copies). */
+ *   n_heads % n_kv_heads == 0; head_dim a multiple of 16 (<= 256: a GEMV tile holds whole RoPE
+ *   pairs); d_model, d_ffn multiples of 8 (16-byte rows for bulk copies), 16 for bf16 models;
+ *   d_model, d_ffn, n_heads*head_dim <= 16384 (the single-vector GEMV stages its input in shared
+ *   memory); fp32 models also need n_anchors*d_model <= 16384. */
 typedef struct spd_config {
     int32_t n_layers;       /* L                                                */
     int32_t d_model;        /* d                                                */
@@ -177,13 +179,18 @@ int spd_rollback(spd_handle* h, int32_t keep_len, int32_t reseed_token);
 int spd_set_draft_override(spd_handle* h, int32_t first_pos, int32_t count,
                            const int32_t* ref_tokens, const uint8_t* modes);
 
-/* Execution options (bit flags), default SPD_OPT_GRAPHS | SPD_OPT_PDM_STREAM. */
+/* Execution options (bit flags), default SPD_OPT_GRAPHS | SPD_OPT_PDL. */
 #define SPD_OPT_GRAPHS       1  /* replay captured CUDA graphs instead of eager launches      */
-#define SPD_OPT_PDM_STREAM   2  /* run the draft module on the library's second stream        */
+#define SPD_OPT_COSCHED      2  /* draft layer s rides in the GEMV launches of target sub-step s
+                                   (SPD summary 方法步骤详情 steps 1 and 4 in one pass over HBM);
+                                   without it the draft module runs as its own launches before
+                                   the target step (serialised)                                */
 #define SPD_OPT_TARGET_ONLY  4  /* skip the draft module (timing of the target step only);
                                    drafts come from the override (mode 2 then uses ref+1 mod V)
                                    or repeat the token at t                                    */
 #define SPD_OPT_DEBUG_LOGITS 8  /* keep full fp32 logits of the last head launch for dumps     */
+#define SPD_OPT_PDL         16  /* programmatic dependent launch: a kernel may start (and stream
+                                   its weights) while its predecessor drains                   */
 int spd_set_options(spd_handle* h, int32_t flags);
 
 /* Copy internal state to a HOST buffer of `bytes` bytes (synchronising).  Layouts:
@@ -207,9 +214,10 @@ int spd_debug_dump(spd_handle* h, int32_t what, void* host_dst, size_t bytes);
 /* Per-kernel-kind device time of eager launches, for roofline reporting.  When enabled, graphs
  * are bypassed and each launch is bracketed by CUDA events on its own stream; spd_kernel_times
  * returns, per kind, launches and summed milliseconds, and resets them.
- * Kinds 0..8 are target-stack launches (stage-diagonal, AR or prefill): 0 qkv, 1 rope/KV append,
- * 2 attention, 3 o-proj, 4 gate/up, 5 down, 6 anchor FC, 7 vocab head, 8 control; kinds 9..17 are
- * the same operators on the draft-module stack. */
+ * Kinds 0..8 are target-stack launches (stage-diagonal, AR or prefill): 0 qkv (with RoPE and
+ * the KV append), 1 unused (kept for layout stability), 2 attention, 3 o-proj, 4 gate/up, 5 down,
+ * 6 anchor FC, 7 vocab head, 8 control; kinds 9..17 are the same operators on the draft-module
+ * stack.  A co-scheduled launch (SPD_OPT_COSCHED) is counted under its target kind. */
 #define SPD_NUM_KINDS 18
 int spd_time_kernels(spd_handle* h, int32_t enable);
 int spd_kernel_times(spd_handle* h, int64_t* launches, double* ms, int32_t n_kinds);
@@ -265,8 +273,9 @@ int spd_attention_static_scratch(const float* q, const void* k_cache, const void
 /* Grouped GEMV with RMSNorm prologue: for group g (0..G-1), y_g = W_g . (x_g / rms(x_g) * nw)
  * (norm skipped when nw == NULL), W_g [rows, cols] row-major in `dtype`, x_g fp32 [cols],
  * y_g fp32 [rows].  Host arrays of G device pointers W[], x[], y[]; nw device fp32 [cols]
- * shared by all groups or NULL.  Same streaming engine as the cycle (bulk copies into a
- * shared-memory ring, fp32 accumulation, fixed reduction order). */
+ * shared by all groups or NULL.  1 <= G <= 34, 8 <= cols <= 16384, cols % 8 == 0.  Same
+ * streaming engine as the cycle (bulk copies into a shared-memory ring, fp32 accumulation, fixed
+ * reduction order). */
 int spd_grouped_gemv(const void* const* W, const float* const* x, float* const* y, int32_t G,
                      int32_t rows, int32_t cols, int32_t dtype, const float* nw, float eps,
                      void* cuda_stream);

@@ -1,13 +1,15 @@
 // C ABI of the SPD engine (declared in include/spd.h): handle, memory, and the enqueueing of
 // prefill, SPD cycles, plain AR steps and the host-side rollback.
 //
-// A cycle is enqueued as (SPD summary, 方法步骤详情 steps 1-5):
-//   draft stream  : anchor FC over the staircase rows -> Ls x (QKV, RoPE/KV append, attention,
-//                   o-proj, gate/up, down) on the draft rows                      (steps 2-4)
-//   main stream   : for s in 0..S-1: the same six launches over the stage diagonal (step 1)
-//   join, then    : vocab head (exiting token + draft row) -> control (verify / rollback, step 5)
-// With graphs enabled the whole cycle is captured once and replayed; all per-cycle state lives in
-// the device control block, so replays run back to back without host synchronisation.
+// A cycle is enqueued as (SPD summary, 方法步骤详情 steps 1-5), all on one stream:
+//   anchor FC over the staircase rows of the draft module                       (steps 2-3)
+//   for s in 0..S-1: QKV(+RoPE, KV append), attention, o-proj, gate/up, down of the stage
+//     diagonal (step 1); draft layer s (s < Ls) rides in the same GEMV launches (step 4)
+//   vocab head (exiting token + draft row), control (verify / rollback / reseed, step 5)
+// With SPD_OPT_PDL every launch may start while its predecessor drains (weights stream early; the
+// activations are read after griddepcontrol.wait).  With graphs enabled the whole cycle is captured
+// once and replayed; all per-cycle state lives in the device control block, so replays run back to
+// back without host synchronisation.
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
@@ -36,13 +38,14 @@ struct spd_handle {
   Bufs B;
   LaunchCfg LC;
   int esz = 2;
-  cudaStream_t s_main = nullptr, s_pdm = nullptr;
+  cudaStream_t s_main = nullptr;
   bool own_main = false;
-  cudaEvent_t ev_fork = nullptr, ev_join = nullptr, ev_t0 = nullptr, ev_t1 = nullptr;
+  cudaEvent_t ev_t0 = nullptr, ev_t1 = nullptr;
   std::vector<void*> allocs;
   Act act_t{}, act_p{}, act_head{}, act_pf{}, act_pfp{};
   float* p_z = nullptr;
-  int opts = SPD_OPT_GRAPHS | SPD_OPT_PDM_STREAM;
+  int opts = SPD_OPT_GRAPHS | SPD_OPT_PDL;
+  bool st_dirty = true;         // the last kernel enqueued may have written the control block
   bool prefilled = false;
   int P = 0;
   cudaGraphExec_t g_cycle = nullptr;
@@ -123,29 +126,44 @@ struct Timed {
 
 constexpr int kDraftKinds = 9;  // kinds 9..17: the same operators on the draft-module stack
 
-int run_gemv(spd_handle* h, int op, const Launch& lc, cudaStream_t s) {
+bool use_pdl(const spd_handle* h) { return (h->opts & SPD_OPT_PDL) != 0; }
+
+// One GEMV launch of operator `op` over the rows of `a` and, when given, the rows of `b` (the
+// draft module's rows riding in a target launch).
+int run_gemv(spd_handle* h, int op, const Launch& a, const Launch* b, cudaStream_t s) {
   static const int kind_of[] = {KK_QKV, KK_O, KK_GATEUP, KK_DOWN, KK_FC, KK_HEAD};
-  Timed tm(h, kind_of[op] + (lc.stack == 1 ? kDraftKinds : 0), s);
-  SPD_CUDA(h, launch_gemv(op, h->D, h->B, lc, h->LC, s));
+  GemvPart parts[2];
+  parts[0].op = op;
+  parts[0].lc = a;
+  int np = 1;
+  if (b) {
+    parts[1].op = op;
+    parts[1].lc = *b;
+    np = 2;
+  }
+  Timed tm(h, kind_of[op] + (a.stack == 1 ? kDraftKinds : 0), s);
+  SPD_CUDA(h, launch_gemv(parts, np, h->D, h->B, h->LC, use_pdl(h), h->st_dirty, s));
+  h->st_dirty = false;
   return SPD_OK;
 }
 
-// one decoder layer for the rows a launch descriptor selects (6 launches)
-int enqueue_layer(spd_handle* h, Launch lc, cudaStream_t s) {
+int run_attn(spd_handle* h, const Launch& lc, cudaStream_t s) {
+  Timed tm(h, KK_ATTN + (lc.stack == 1 ? kDraftKinds : 0), s);
+  SPD_CUDA(h, launch_attn(h->D, h->B, lc, h->LC, use_pdl(h) && !h->st_dirty, s));
+  h->st_dirty = false;
+  return SPD_OK;
+}
+
+// One decoder layer (or the layer-s slice of a co-scheduled step) for the rows of `lc` and, when
+// given, `extra` (5 launches; the draft rows need their own attention launch).
+int enqueue_layer(spd_handle* h, const Launch& lc, const Launch* extra, cudaStream_t s) {
   int rc;
-  if ((rc = run_gemv(h, OP_QKV, lc, s))) return rc;
-  const int off = lc.stack == 1 ? kDraftKinds : 0;
-  {
-    Timed tm(h, KK_ROPE + off, s);
-    SPD_CUDA(h, launch_rope(h->D, h->B, lc, s));
-  }
-  {
-    Timed tm(h, KK_ATTN + off, s);
-    SPD_CUDA(h, launch_attn(h->D, h->B, lc, h->LC, s));
-  }
-  if ((rc = run_gemv(h, OP_O, lc, s))) return rc;
-  if ((rc = run_gemv(h, OP_GATEUP, lc, s))) return rc;
-  return run_gemv(h, OP_DOWN, lc, s);
+  if ((rc = run_gemv(h, OP_QKV, lc, extra, s))) return rc;
+  if ((rc = run_attn(h, lc, s))) return rc;
+  if (extra && (rc = run_attn(h, *extra, s))) return rc;
+  if ((rc = run_gemv(h, OP_O, lc, extra, s))) return rc;
+  if ((rc = run_gemv(h, OP_GATEUP, lc, extra, s))) return rc;
+  return run_gemv(h, OP_DOWN, lc, extra, s);
 }
 
 Launch mk(int kind, int stack, int sub, const Act& act, int pos0 = 0, int cnt = 0) {
@@ -155,44 +173,40 @@ Launch mk(int kind, int stack, int sub, const Act& act, int pos0 = 0, int cnt = 
   return lc;
 }
 
-int enqueue_pdm(spd_handle* h, cudaStream_t s) {
-  int rc;
-  if ((rc = run_gemv(h, OP_FC, mk(LK_PDMROWS, 1, 0, h->act_p), s))) return rc;
-  for (int lp = 0; lp < h->D.Ls; ++lp)
-    if ((rc = enqueue_layer(h, mk(LK_PDMROWS, 1, lp, h->act_p), s))) return rc;
-  return SPD_OK;
-}
-
 int enqueue_cycle(spd_handle* h) {
   int rc;
   const bool pdm = !(h->opts & SPD_OPT_TARGET_ONLY);
-  const bool fork = pdm && (h->opts & SPD_OPT_PDM_STREAM);
+  const bool cos = pdm && (h->opts & SPD_OPT_COSCHED);
   cudaStream_t sm = h->s_main;
-  if (fork) {
-    SPD_CUDA(h, cudaEventRecord(h->ev_fork, sm));
-    SPD_CUDA(h, cudaStreamWaitEvent(h->s_pdm, h->ev_fork, 0));
-    if ((rc = enqueue_pdm(h, h->s_pdm))) return rc;
-    SPD_CUDA(h, cudaEventRecord(h->ev_join, h->s_pdm));
-  } else if (pdm) {
-    if ((rc = enqueue_pdm(h, sm))) return rc;
+  h->st_dirty = true;  // the previous cycle's control kernel (or the host) wrote the control block
+  if (pdm) {
+    if ((rc = run_gemv(h, OP_FC, mk(LK_PDMROWS, 1, 0, h->act_p), nullptr, sm))) return rc;
+    if (!cos)  // serialised draft module: its Ls layers before the target step
+      for (int lp = 0; lp < h->D.Ls; ++lp)
+        if ((rc = enqueue_layer(h, mk(LK_PDMROWS, 1, lp, h->act_p), nullptr, sm))) return rc;
   }
-  for (int s = 0; s < h->D.S; ++s)
-    if ((rc = enqueue_layer(h, mk(LK_DIAG, 0, s, h->act_t), sm))) return rc;
-  if (fork) SPD_CUDA(h, cudaStreamWaitEvent(sm, h->ev_join, 0));
-  if ((rc = run_gemv(h, OP_HEAD, mk(LK_DIAG, 0, 0, h->act_head), sm))) return rc;
+  for (int s = 0; s < h->D.S; ++s) {
+    const Launch lt = mk(LK_DIAG, 0, s, h->act_t);
+    const Launch lp = mk(LK_PDMROWS, 1, s, h->act_p);
+    if ((rc = enqueue_layer(h, lt, (cos && s < h->D.Ls) ? &lp : nullptr, sm))) return rc;
+  }
+  if ((rc = run_gemv(h, OP_HEAD, mk(LK_DIAG, 0, 0, h->act_head), nullptr, sm))) return rc;
   Timed tm(h, KK_CTRL, sm);
   SPD_CUDA(h, launch_control_cycle(h->D, h->B, sm));
+  h->st_dirty = true;
   return SPD_OK;
 }
 
 int enqueue_ar_step(spd_handle* h) {
   int rc;
   cudaStream_t sm = h->s_main;
+  h->st_dirty = true;
   for (int l = 0; l < h->D.L; ++l)
-    if ((rc = enqueue_layer(h, mk(LK_AR, 0, l, h->act_t), sm))) return rc;
-  if ((rc = run_gemv(h, OP_HEAD, mk(LK_AR, 0, 0, h->act_head), sm))) return rc;
+    if ((rc = enqueue_layer(h, mk(LK_AR, 0, l, h->act_t), nullptr, sm))) return rc;
+  if ((rc = run_gemv(h, OP_HEAD, mk(LK_AR, 0, 0, h->act_head), nullptr, sm))) return rc;
   Timed tm(h, KK_CTRL, sm);
   SPD_CUDA(h, launch_control_ar(h->D, h->B, sm));
+  h->st_dirty = true;
   return SPD_OK;
 }
 
@@ -331,15 +345,11 @@ const char* spd_last_error(const spd_handle* h) {
 void spd_destroy(spd_handle* h) {
   if (!h) return;
   if (h->s_main) cudaStreamSynchronize(h->s_main);
-  if (h->s_pdm) cudaStreamSynchronize(h->s_pdm);
   drop_graphs(h);
   for (void* p : h->allocs) cudaFree(p);
   for (cudaEvent_t e : h->pool) cudaEventDestroy(e);
-  if (h->ev_fork) cudaEventDestroy(h->ev_fork);
-  if (h->ev_join) cudaEventDestroy(h->ev_join);
   if (h->ev_t0) cudaEventDestroy(h->ev_t0);
   if (h->ev_t1) cudaEventDestroy(h->ev_t1);
-  if (h->s_pdm) cudaStreamDestroy(h->s_pdm);
   if (h->own_main && h->s_main) cudaStreamDestroy(h->s_main);
   if (h->host_state) cudaFreeHost(h->host_state);
   delete h;
@@ -367,6 +377,12 @@ int spd_create(const spd_config* cfg, const spd_weights* w, void* cuda_stream, s
   if (c.n_heads % c.n_kv_heads != 0) return fail(nullptr, SPD_EINVAL, "n_heads %% n_kv_heads != 0");
   if (c.head_dim % 16 != 0 || c.head_dim > 256)
     return fail(nullptr, SPD_EINVAL, "head_dim must be a multiple of 16, <= 256");
+  if (c.d_model > kGemvMaxCols || c.d_ffn > kGemvMaxCols || c.n_heads * c.head_dim > kGemvMaxCols)
+    return fail(nullptr, SPD_EINVAL, "d_model, d_ffn and n_heads*head_dim must be <= %d", kGemvMaxCols);
+  if (c.dtype == SPD_DTYPE_BF16 && (c.d_model % 16 || c.d_ffn % 16))
+    return fail(nullptr, SPD_EINVAL, "bf16 models need d_model and d_ffn multiples of 16");
+  if (c.dtype == SPD_DTYPE_F32 && c.n_anchors * c.d_model > kGemvMaxCols)
+    return fail(nullptr, SPD_EINVAL, "fp32 models need n_anchors*d_model <= %d", kGemvMaxCols);
   if (c.d_model % 8 || c.d_ffn % 8) return fail(nullptr, SPD_EINVAL, "d_model and d_ffn must be multiples of 8");
   if (c.dtype != SPD_DTYPE_F32 && c.dtype != SPD_DTYPE_BF16) return fail(nullptr, SPD_EINVAL, "bad dtype");
   const int gq = c.n_heads / c.n_kv_heads;
@@ -510,9 +526,6 @@ int spd_create(const spd_config* cfg, const spd_weights* w, void* cuda_stream, s
     e = cudaStreamCreate(&h->s_main);  // blocking: orders with the legacy default stream
     h->own_main = true;
   }
-  if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&h->s_pdm, cudaStreamNonBlocking);
-  if (e == cudaSuccess) e = cudaEventCreateWithFlags(&h->ev_fork, cudaEventDisableTiming);
-  if (e == cudaSuccess) e = cudaEventCreateWithFlags(&h->ev_join, cudaEventDisableTiming);
   if (e == cudaSuccess) e = cudaEventCreate(&h->ev_t0);
   if (e == cudaSuccess) e = cudaEventCreate(&h->ev_t1);
   if (e == cudaSuccess) e = gemv_setup_attributes();
@@ -558,14 +571,15 @@ int spd_prefill(spd_handle* h, const int32_t* tokens, int32_t P, int32_t* first_
   for (int p0 = 1; p0 <= P; p0 += kPrefillBlock) {
     cnt = P - p0 + 1 < kPrefillBlock ? P - p0 + 1 : kPrefillBlock;
     SPD_CUDA(h, launch_prefill_embed(D, h->B, h->act_pf.resid, h->act_pf.anch, p0, cnt, s));
+    h->st_dirty = true;
     for (int l = 0; l < D.L; ++l)
-      if ((rc = enqueue_layer(h, mk(LK_ROWS, 0, l, h->act_pf, p0, cnt), s))) return rc;
+      if ((rc = enqueue_layer(h, mk(LK_ROWS, 0, l, h->act_pf, p0, cnt), nullptr, s))) return rc;
     // draft-module prefix rows at depth n (cached verified features, SPD v3 App. A.1)
-    if ((rc = run_gemv(h, OP_FC, mk(LK_ROWS, 1, 0, h->act_pfp, p0, cnt), s))) return rc;
+    if ((rc = run_gemv(h, OP_FC, mk(LK_ROWS, 1, 0, h->act_pfp, p0, cnt), nullptr, s))) return rc;
     for (int lp = 0; lp < D.Ls; ++lp)
-      if ((rc = enqueue_layer(h, mk(LK_ROWS, 1, lp, h->act_pfp, p0, cnt), s))) return rc;
+      if ((rc = enqueue_layer(h, mk(LK_ROWS, 1, lp, h->act_pfp, p0, cnt), nullptr, s))) return rc;
   }
-  if ((rc = run_gemv(h, OP_HEAD, mk(LK_ROWS, 0, 0, h->act_pf, P - cnt + 1, cnt), s))) return rc;
+  if ((rc = run_gemv(h, OP_HEAD, mk(LK_ROWS, 0, 0, h->act_pf, P - cnt + 1, cnt), nullptr, s))) return rc;
   SPD_CUDA(h, launch_prefill_finish(D, h->B, P, s));
   h->P = P;
   h->prefilled = true;
@@ -638,10 +652,10 @@ int spd_set_draft_override(spd_handle* h, int32_t first_pos, int32_t count, cons
 
 int spd_set_options(spd_handle* h, int32_t flags) {
   if (!h) return SPD_EINVAL;
-  if (flags & ~(SPD_OPT_GRAPHS | SPD_OPT_PDM_STREAM | SPD_OPT_TARGET_ONLY | SPD_OPT_DEBUG_LOGITS))
+  if (flags & ~(SPD_OPT_GRAPHS | SPD_OPT_COSCHED | SPD_OPT_TARGET_ONLY | SPD_OPT_DEBUG_LOGITS | SPD_OPT_PDL))
     return fail(h, SPD_EINVAL, "unknown option bits");
   SPD_CUDA(h, cudaStreamSynchronize(h->s_main));
-  if ((flags ^ h->opts) & (SPD_OPT_PDM_STREAM | SPD_OPT_TARGET_ONLY | SPD_OPT_DEBUG_LOGITS))
+  if ((flags ^ h->opts) & (SPD_OPT_COSCHED | SPD_OPT_TARGET_ONLY | SPD_OPT_DEBUG_LOGITS | SPD_OPT_PDL))
     drop_graphs(h);
   h->opts = flags;
   h->LC.debug_logits = (flags & SPD_OPT_DEBUG_LOGITS) ? 1 : 0;
@@ -728,8 +742,8 @@ int spd_cycle_bytes(const spd_handle* h, int32_t t, int32_t fill, int32_t exited
   const int a = fill < 0 ? 0 : (fill > D.n ? D.n : fill);
   double kv = 0.0;
   for (int j = 0; j < a; ++j) kv += (double)(t - j) * D.S * kvrow;
-  out[KK_QKV] = a * D.S * qkv;
-  out[KK_ROPE] = a * D.S * kvrow;
+  out[KK_QKV] = a * D.S * (qkv + kvrow);  // the QKV launch also appends K and V to the cache
+  out[KK_ROPE] = 0.0;
   out[KK_ATTN] = kv;
   out[KK_O] = a * D.S * wo;
   out[KK_GATEUP] = a * D.S * gu;
@@ -737,7 +751,8 @@ int spd_cycle_bytes(const spd_handle* h, int32_t t, int32_t fill, int32_t exited
   out[KK_HEAD] = exited ? (double)D.V * D.d * e : 0.0;
   if (with_pdm) {  // draft-module kinds 9..17
     const int o = 9;
-    out[o + KK_QKV] = D.Ls * qkv;
+    // draft rows of a cycle: about fill + 1 (the in-flight rows and the row verified last cycle)
+    out[o + KK_QKV] = D.Ls * (qkv + (double)(a + 1) * kvrow);
     out[o + KK_O] = D.Ls * wo;
     out[o + KK_GATEUP] = D.Ls * gu;
     out[o + KK_DOWN] = D.Ls * dn;
@@ -761,7 +776,7 @@ size_t spd_attention_workspace_bytes(int32_t R, int32_t n_heads, int32_t n_kv_he
 int spd_attention(const float* q, const void* k_cache, const void* v_cache, int32_t dtype,
                   const int32_t* pos, int32_t R, int32_t n_heads, int32_t n_kv_heads, int32_t head_dim,
                   int32_t max_seq, float* out, void* workspace, size_t ws_bytes, void* stream) {
-  if (!q || !k_cache || !v_cache || !pos || !out || !workspace || R < 1 || R > kMaxGroups - 2 ||
+  if (!q || !k_cache || !v_cache || !pos || !out || !workspace || R < 1 || R > kMaxAttnRows ||
       n_kv_heads < 1 || n_heads % n_kv_heads || head_dim % 16 || head_dim > 256 || max_seq < 1 ||
       (dtype != SPD_DTYPE_F32 && dtype != SPD_DTYPE_BF16))
     return fail(nullptr, SPD_EINVAL, "spd_attention: bad arguments");
@@ -791,7 +806,7 @@ int spd_attention(const float* q, const void* k_cache, const void* v_cache, int3
   LaunchCfg LC;
   memset(&LC, 0, sizeof(LC));
   LC.attn_grid_decode = attn_grid(D, false);
-  e = launch_attn(D, B, lc, LC, reinterpret_cast<cudaStream_t>(stream));
+  e = launch_attn(D, B, lc, LC, false, reinterpret_cast<cudaStream_t>(stream));
   if (e != cudaSuccess)
     return fail(nullptr, SPD_ECUDA, "attention launch (grid %d): %s", LC.attn_grid_decode,
                 cudaGetErrorString(e));
@@ -801,7 +816,7 @@ int spd_attention(const float* q, const void* k_cache, const void* v_cache, int3
 int spd_grouped_gemv(const void* const* W, const float* const* x, float* const* y, int32_t G,
                      int32_t rows, int32_t cols, int32_t dtype, const float* nw, float eps,
                      void* stream) {
-  if (!W || !x || !y || G < 1 || G > kMaxGroups || rows < 1 || cols < 8 || cols % 8 ||
+  if (!W || !x || !y || G < 1 || G > kMaxExplicit || rows < 1 || cols < 8 || cols % 8 || cols > kGemvMaxCols ||
       (dtype != SPD_DTYPE_F32 && dtype != SPD_DTYPE_BF16))
     return fail(nullptr, SPD_EINVAL, "spd_grouped_gemv: bad arguments");
   GemvExplicit ge;
@@ -814,7 +829,7 @@ int spd_grouped_gemv(const void* const* W, const float* const* x, float* const* 
   if (nw && !aligned16(nw)) return fail(nullptr, SPD_EINVAL, "spd_grouped_gemv: norm weight unaligned");
   ge.G = G; ge.rows = rows; ge.cols = cols; ge.nw = nw;
   cudaError_t e = gemv_setup_attributes();
-  if (e == cudaSuccess) e = launch_gemv_explicit(ge, dtype, eps, 0, reinterpret_cast<cudaStream_t>(stream));
+  if (e == cudaSuccess) e = launch_gemv_explicit(ge, dtype, eps, reinterpret_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return fail(nullptr, SPD_ECUDA, "%s", cudaGetErrorString(e));
   return SPD_OK;
 }

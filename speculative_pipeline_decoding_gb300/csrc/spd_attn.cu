@@ -1,24 +1,19 @@
-// Decode attention over per-layer KV caches, and the RoPE + KV-append step before it.
+// Decode attention over per-layer KV caches.
 //
-// rope_append: each row's q and k (fp32, from the QKV GEMV) are rotated (rotate-half pairing
-// i <-> i+hd/2, cos/sin tables of angle (pos-1)*theta^(-2i/hd) formed in fp64); q is written back,
-// k and v are rounded to the cache dtype and stored at [layer][kv_head][pos-1].  A separate launch
-// is needed because rows of one multi-row launch (draft rows, prefill blocks) read each other's K/V.
-//
-// attention: work item = (query tile, kv head, key chunk of 128 positions).  A tile holds up to 8
-// query rows of one layer (1 row per token in the stage-diagonal step); all query heads of the
-// grouped-query group share the K/V chunk, which is bulk-copied into shared memory once.  Scores use
-// 16-dim lane slices reduced with xor shuffles, softmax is per chunk (max, exp, sum), and the chunk
-// partial (o, m, l) goes to global scratch.  The last item of a (tile, kv head) to finish (atomic
-// ticket, no spinning) merges the partials of each query in chunk order.  The number of chunks
-// depends only on the query position, so a token's result does not depend on its batch.
+// The query rows arrive already rotated (RoPE is applied in the QKV epilogue of the GEMV engine,
+// which also appends k and v to the cache).  Work item = (query tile, kv head, key chunk of 128
+// positions).  A tile holds up to 8 query rows of one layer (1 row per token in the stage-diagonal
+// step); all query heads of the grouped-query group share the K/V chunk, which is bulk-copied into
+// shared memory once.  Scores use 16-dim lane slices reduced with xor shuffles, softmax is per chunk
+// (max, exp, sum), and the chunk partial (o, m, l) goes to global scratch.  The last item of a
+// (tile, kv head) to finish (atomic ticket, no spinning) merges the partials of each query in chunk
+// order.  The number of chunks depends only on the query position, so a token's result does not
+// depend on its batch.
 #include "spd_internal.cuh"
 
 namespace spd {
 
 namespace {
-
-constexpr int kBig = 1 << 30;
 
 struct AttnParams {
   Dims D;
@@ -101,6 +96,8 @@ attn_kernel(const __grid_constant__ AttnParams p) {
     fence_mbar_init();
   }
   __syncthreads();
+  pdl_wait();  // q and the K/V appended by the previous kernel are visible from here on
+  pdl_trigger();
   const int n_items = s_items;
   if (n_items == 0) return;
 
@@ -252,67 +249,6 @@ attn_kernel(const __grid_constant__ AttnParams p) {
   }
 }
 
-template <typename WT>
-__global__ void __launch_bounds__(256) rope_kernel(const __grid_constant__ AttnParams p) {
-  __shared__ RowGroup rg[kMaxGroups];
-  __shared__ int s_nr;
-  const Dims& D = p.D;
-  DevState* st = p.B.st;
-  if (threadIdx.x == 0) {
-    const bool skip = st->done || st->err;
-    s_nr = skip ? 0 : build_rows(p.lc, D, st, rg);
-  }
-  __syncthreads();
-  // this block's row
-  int row = blockIdx.x, g = 0;
-  while (g < s_nr && row >= rg[g].nv) { row -= rg[g].nv; ++g; }
-  if (g >= s_nr) return;
-  const int pos = rg[g].pos0 + row;
-  const int layer = rg[g].layer;
-  const int hd = D.hd, half = hd / 2;
-  float* q = p.lc.act.qkv + (size_t)(rg[g].vid0 + row) * D.qkv_rows;
-  const float* cs = p.B.rope_cos + (size_t)(pos - 1) * half;
-  const float* sn = p.B.rope_sin + (size_t)(pos - 1) * half;
-  WT* kc = reinterpret_cast<WT*>(p.lc.stack == 0 ? p.B.kc : p.B.pkc);
-  WT* vc = reinterpret_cast<WT*>(p.lc.stack == 0 ? p.B.vc : p.B.pvc);
-  const size_t layer_elems = (size_t)D.hkv * D.max_seq * hd;
-  const int nrot = (D.hq + D.hkv) * half;
-  for (int idx = threadIdx.x; idx < nrot; idx += blockDim.x) {
-    const int h = idx / half, i = idx % half;
-    float* base = q + (size_t)h * hd;
-    const float x1 = base[i], x2 = base[i + half];
-    const float c = cs[i], s = sn[i];
-    const float y1 = x1 * c - x2 * s;
-    const float y2 = x2 * c + x1 * s;
-    if (h < D.hq) {
-      base[i] = y1;
-      base[i + half] = y2;
-    } else {
-      const int kh = h - D.hq;
-      WT* dst = kc + layer * layer_elems + ((size_t)kh * D.max_seq + (pos - 1)) * hd;
-      dst[i] = WTraits<WT>::from_f(y1);
-      dst[i + half] = WTraits<WT>::from_f(y2);
-    }
-  }
-  const float* vsrc = q + (size_t)(D.hq + D.hkv) * hd;
-  for (int idx = threadIdx.x; idx < D.hkv * hd; idx += blockDim.x) {
-    const int kh = idx / hd, e = idx % hd;
-    vc[layer * layer_elems + ((size_t)kh * D.max_seq + (pos - 1)) * hd + e] =
-        WTraits<WT>::from_f(vsrc[idx]);
-  }
-  if (threadIdx.x == 0 && p.lc.stack == 0 && p.B.kvlen) p.B.kvlen[layer] = pos;
-}
-
-int max_rows_of(const Dims& D, const Launch& lc) {
-  switch (lc.kind) {
-    case LK_DIAG: return D.n;
-    case LK_PDMROWS: return D.n + 1;
-    case LK_ROWS: return lc.cnt;
-    case LK_AR: return 1;
-    default: return lc.cnt;
-  }
-}
-
 }  // namespace
 
 size_t attn_smem_bytes(const Dims& D, bool multi) {
@@ -351,7 +287,7 @@ cudaError_t attn_setup_attributes(size_t need) {
 }
 
 cudaError_t launch_attn(const Dims& D, const Bufs& B, const Launch& lc, const LaunchCfg& cfg,
-                        cudaStream_t s) {
+                        bool pdl, cudaStream_t s) {
   AttnParams p;
   memset(&p, 0, sizeof(p));
   p.D = D; p.B = B; p.lc = lc;
@@ -360,24 +296,19 @@ cudaError_t launch_attn(const Dims& D, const Bufs& B, const Launch& lc, const La
   p.qh_max = p.qt * D.gq;
   const size_t smem = attn_smem_bytes(D, multi);
   const int grid = multi ? cfg.attn_grid_multi : cfg.attn_grid_decode;
-  if (D.dtype == SPD_DTYPE_BF16)
-    attn_kernel<__nv_bfloat16><<<grid, kAttnThreads, smem, s>>>(p);
-  else
-    attn_kernel<float><<<grid, kAttnThreads, smem, s>>>(p);
-  return cudaGetLastError();
-}
-
-cudaError_t launch_rope(const Dims& D, const Bufs& B, const Launch& lc, cudaStream_t s) {
-  AttnParams p;
-  memset(&p, 0, sizeof(p));
-  p.D = D; p.B = B; p.lc = lc;
-  const int grid = max_rows_of(D, lc);
-  if (grid <= 0) return cudaSuccess;
-  if (D.dtype == SPD_DTYPE_BF16)
-    rope_kernel<__nv_bfloat16><<<grid, 256, 0, s>>>(p);
-  else
-    rope_kernel<float><<<grid, 256, 0, s>>>(p);
-  return cudaGetLastError();
+  cudaLaunchConfig_t lcfg;
+  memset(&lcfg, 0, sizeof(lcfg));
+  lcfg.gridDim = dim3(grid);
+  lcfg.blockDim = dim3(kAttnThreads);
+  lcfg.dynamicSmemBytes = smem;
+  lcfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  lcfg.attrs = attr;
+  lcfg.numAttrs = pdl ? 1 : 0;
+  if (D.dtype == SPD_DTYPE_BF16) return cudaLaunchKernelEx(&lcfg, attn_kernel<__nv_bfloat16>, p);
+  return cudaLaunchKernelEx(&lcfg, attn_kernel<float>, p);
 }
 
 }  // namespace spd
@@ -414,7 +345,7 @@ extern "C" int spd_attention_static_scratch(const float* q, const void* k_cache,
                                             int32_t max_seq, float* out, void* cuda_stream) {
   using namespace spd;
   char msg[256];
-  if (!q || !k_cache || !v_cache || !pos || !out || R < 1 || R > kMaxGroups - 2 || n_kv_heads < 1 ||
+  if (!q || !k_cache || !v_cache || !pos || !out || R < 1 || R > kMaxAttnRows || n_kv_heads < 1 ||
       n_heads % n_kv_heads || head_dim % 16 || head_dim > 256 || max_seq < 1 ||
       (dtype != SPD_DTYPE_F32 && dtype != SPD_DTYPE_BF16))
     return spd_internal_fail(SPD_EINVAL, "spd_attention_static_scratch: bad arguments");
@@ -469,7 +400,7 @@ extern "C" int spd_attention_static_scratch(const float* q, const void* k_cache,
   LaunchCfg LC;
   memset(&LC, 0, sizeof(LC));
   LC.attn_grid_decode = attn_grid(D, false);
-  e = launch_attn(D, B, lc, LC, s);
+  e = launch_attn(D, B, lc, LC, false, s);
   if (e != cudaSuccess) {
     snprintf(msg, sizeof(msg), "spd_attention_static_scratch: launch: %s", cudaGetErrorString(e));
     return spd_internal_fail(SPD_ECUDA, msg);

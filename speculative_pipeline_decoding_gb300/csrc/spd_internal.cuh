@@ -19,17 +19,14 @@
 
 namespace spd {
 
-constexpr int kMaxGroups = 34;      // >= n_stages + 2
+constexpr int kMaxGroups = 72;      // one launch: n_stages target groups + n_stages+1 draft rows (+ splits)
+constexpr int kMaxAttnRows = 32;    // query rows of the stand-alone attention operators
+constexpr int kMaxExplicit = 34;    // groups of the stand-alone grouped GEMV
+constexpr int kGemvMaxCols = 16384; // input columns of a single-vector GEMV group (staged in smem)
 constexpr int kMaxTiles = 64;       // attention query tiles per launch
 constexpr int kPrefillBlock = 32;   // prompt rows per prefill pass
 constexpr int kAttnChunk = 128;     // keys per attention split (fixed: split count depends on length only)
 constexpr int kAttnQT = 8;          // query rows per attention tile for multi-row launches
-constexpr int kGemvTR = 4;          // rows per GEMV tile
-constexpr int kGemvConsumerWarps = 8;
-constexpr int kGemvThreads = (kGemvConsumerWarps + 1) * 32;
-constexpr int kGemvRingBytes = 96 * 1024;
-constexpr int kGemvMaxStages = 8;
-constexpr int kGemvMaxNV = 64;      // vectors per group (prefill block rows)
 constexpr int kAttnThreads = 256;
 
 // ------------------------------------------------------------------------------------------
@@ -189,6 +186,13 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
       "l"(src), "r"(bytes), "r"(smem_u32(bar)), "l"(policy)
       : "memory");
 }
+// Programmatic dependent launch: wait for the previous kernel of the stream (no-op when the kernel
+// was launched without the attribute), and allow the next kernel to be scheduled.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 __device__ __forceinline__ void named_bar(int id, int nthreads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
@@ -269,9 +273,9 @@ enum KernelKind { KK_QKV = 0, KK_ROPE = 1, KK_ATTN = 2, KK_O = 3, KK_GATEUP = 4,
                   KK_FC = 6, KK_HEAD = 7, KK_CTRL = 8 };
 
 struct GemvExplicit {  // stand-alone grouped GEMV
-  const void* W[kMaxGroups];
-  const float* x[kMaxGroups];
-  float* y[kMaxGroups];
+  const void* W[kMaxExplicit];
+  const float* x[kMaxExplicit];
+  float* y[kMaxExplicit];
   int G, rows, cols;
   const float* nw;
 };
@@ -283,13 +287,21 @@ struct LaunchCfg {
   int debug_logits;
 };
 
-cudaError_t launch_gemv(int op, const Dims& D, const Bufs& B, const Launch& lc,
-                        const LaunchCfg& cfg, cudaStream_t s);
-cudaError_t launch_gemv_explicit(const GemvExplicit& ge, int dtype, float eps, int grid,
-                                 cudaStream_t s);
-cudaError_t launch_rope(const Dims& D, const Bufs& B, const Launch& lc, cudaStream_t s);
+// One operator over the rows a launch descriptor selects; a GEMV launch carries one or two parts
+// (the target's stage-diagonal groups and the draft module's rows of the same operator).
+struct GemvPart {
+  int op;
+  Launch lc;
+};
+
+// pdl: launch with programmatic stream serialisation (the kernel may start before its predecessor
+// ends; it waits with griddepcontrol.wait before touching activations).  resolve_after_wait: the
+// predecessor may have written the control block, so the rows are resolved after that wait.
+cudaError_t launch_gemv(const GemvPart* parts, int nparts, const Dims& D, const Bufs& B,
+                        const LaunchCfg& cfg, bool pdl, bool resolve_after_wait, cudaStream_t s);
+cudaError_t launch_gemv_explicit(const GemvExplicit& ge, int dtype, float eps, cudaStream_t s);
 cudaError_t launch_attn(const Dims& D, const Bufs& B, const Launch& lc, const LaunchCfg& cfg,
-                        cudaStream_t s);
+                        bool pdl, cudaStream_t s);
 size_t attn_smem_bytes(const Dims& D, bool multi);
 size_t attn_part_floats(int rows, int hq, int hd, int max_seq);
 cudaError_t gemv_setup_attributes();
