@@ -57,10 +57,9 @@ enum { SPD_DTYPE_F32 = 0, SPD_DTYPE_BF16 = 1 };
  *   n_stages | n_layers; 1 <= pdm_layers <= n_layers/n_stages (the masking condition of the
  *   SPD summary 核心方法: the PDM fits inside one stage forward);
  *   anchors strictly increasing, anchors[0] == 0, anchors[n_anchors-1] <= n_layers;
- *   n_heads % n_kv_heads == 0; head_dim a multiple of 16 (<= 256: a GEMV tile holds whole RoPE
- *   pairs); d_model, d_ffn multiples of 8 (16-byte rows for bulk copies), 16 for bf16 models;
- *   d_model, d_ffn, n_heads*head_dim <= 16384 (the single-vector GEMV stages its input in shared
- *   memory); fp32 models also need n_anchors*d_model <= 16384. */
+ *   n_heads % n_kv_heads == 0; head_dim a multiple of 64 (<= 256: a 64-row GEMV tile holds 32
+ *   rows of a head and their RoPE partners); d_model, d_ffn multiples of 8 (16-byte rows for the
+ *   tensor copies), 16 for bf16 models. */
 typedef struct spd_config {
     int32_t n_layers;       /* L                                                */
     int32_t d_model;        /* d                                                */
@@ -273,9 +272,9 @@ int spd_attention_static_scratch(const float* q, const void* k_cache, const void
 /* Grouped GEMV with RMSNorm prologue: for group g (0..G-1), y_g = W_g . (x_g / rms(x_g) * nw)
  * (norm skipped when nw == NULL), W_g [rows, cols] row-major in `dtype`, x_g fp32 [cols],
  * y_g fp32 [rows].  Host arrays of G device pointers W[], x[], y[]; nw device fp32 [cols]
- * shared by all groups or NULL.  1 <= G <= 34, 8 <= cols <= 16384, cols % 8 == 0.  Same
- * streaming engine as the cycle (bulk copies into a shared-memory ring, fp32 accumulation, fixed
- * reduction order). */
+ * shared by all groups or NULL.  1 <= G <= 34, cols >= 8, cols % 8 == 0.  Same streaming engine
+ * as the cycle (2-D tensor copies into a shared-memory ring, fp32 accumulation, fixed reduction
+ * order); the G tensor maps live in stream-ordered scratch (cudaMallocAsync) for the launch. */
 int spd_grouped_gemv(const void* const* W, const float* const* x, float* const* y, int32_t G,
                      int32_t rows, int32_t cols, int32_t dtype, const float* nw, float eps,
                      void* cuda_stream);

@@ -375,14 +375,8 @@ int spd_create(const spd_config* cfg, const spd_weights* w, void* cuda_stream, s
   if (c.anchors[c.n_anchors - 1] > c.n_layers)
     return fail(nullptr, SPD_EINVAL, "anchors must be <= n_layers");
   if (c.n_heads % c.n_kv_heads != 0) return fail(nullptr, SPD_EINVAL, "n_heads %% n_kv_heads != 0");
-  if (c.head_dim % 16 != 0 || c.head_dim > 256)
-    return fail(nullptr, SPD_EINVAL, "head_dim must be a multiple of 16, <= 256");
-  if (c.d_model > kGemvMaxCols || c.d_ffn > kGemvMaxCols || c.n_heads * c.head_dim > kGemvMaxCols)
-    return fail(nullptr, SPD_EINVAL, "d_model, d_ffn and n_heads*head_dim must be <= %d", kGemvMaxCols);
-  if (c.dtype == SPD_DTYPE_BF16 && (c.d_model % 16 || c.d_ffn % 16))
-    return fail(nullptr, SPD_EINVAL, "bf16 models need d_model and d_ffn multiples of 16");
-  if (c.dtype == SPD_DTYPE_F32 && c.n_anchors * c.d_model > kGemvMaxCols)
-    return fail(nullptr, SPD_EINVAL, "fp32 models need n_anchors*d_model <= %d", kGemvMaxCols);
+  if (c.head_dim % 64 != 0 || c.head_dim > 256)
+    return fail(nullptr, SPD_EINVAL, "head_dim must be a multiple of 64, <= 256");
   if (c.d_model % 8 || c.d_ffn % 8) return fail(nullptr, SPD_EINVAL, "d_model and d_ffn must be multiples of 8");
   if (c.dtype != SPD_DTYPE_F32 && c.dtype != SPD_DTYPE_BF16) return fail(nullptr, SPD_EINVAL, "bad dtype");
   const int gq = c.n_heads / c.n_kv_heads;
@@ -451,6 +445,37 @@ int spd_create(const spd_config* cfg, const spd_weights* w, void* cuda_stream, s
       return fail(nullptr, e == cudaErrorMemoryAllocation ? SPD_ENOMEM : SPD_ECUDA, "%s", msg.c_str()); \
     }                                                                              \
   } while (0)
+  // tensor maps of every weight matrix the GEMV engine streams (7 per layer, FCs, two heads)
+  {
+    const int nmaps = 7 * (c.n_layers + c.pdm_layers) + c.n_anchors + 2;
+    CUtensorMap* dmaps;
+    ALLOC(dmaps, CUtensorMap, nmaps);
+    std::vector<CUtensorMap> hm(nmaps);
+    int k = 0;
+    const int qr = c.n_heads * c.head_dim, kr = c.n_kv_heads * c.head_dim;
+    auto enc = [&](const void* W, int rows, int cols) -> const CUtensorMap* {
+      if (e == cudaSuccess) e = gemv_encode_map(&hm[k], W, rows, cols, c.dtype);
+      return dmaps + k++;
+    };
+    auto layer_maps = [&](LayerW& o) {
+      o.tq = enc(o.wq, qr, c.d_model); o.tk = enc(o.wk, kr, c.d_model); o.tv = enc(o.wv, kr, c.d_model);
+      o.to = enc(o.wo, c.d_model, qr);
+      o.tg = enc(o.wg, c.d_ffn, c.d_model); o.tu = enc(o.wu, c.d_ffn, c.d_model);
+      o.td = enc(o.wd, c.d_model, c.d_ffn);
+    };
+    for (auto& o : tl) layer_maps(o);
+    for (auto& o : pl) layer_maps(o);
+    for (int j = 0; j < c.n_anchors; ++j)
+      B.tm_fc[j] = B.fc[j] ? enc(B.fc[j], c.d_model, (j + 1) * c.d_model) : nullptr;
+    B.tm_lm = enc(B.lm_head, c.vocab, c.d_model);
+    B.tm_pdm = enc(B.pdm_head, c.vocab, c.d_model);
+    if (e == cudaSuccess) e = cudaMemcpy(dmaps, hm.data(), sizeof(CUtensorMap) * nmaps, cudaMemcpyHostToDevice);
+    if (e != cudaSuccess) {
+      std::string msg = cudaGetErrorString(e);
+      spd_destroy(h);
+      return fail(nullptr, SPD_ECUDA, "tensor maps: %s", msg.c_str());
+    }
+  }
   LayerW *dtl, *dpl;
   ALLOC(dtl, LayerW, c.n_layers);
   ALLOC(dpl, LayerW, c.pdm_layers);
@@ -816,7 +841,7 @@ int spd_attention(const float* q, const void* k_cache, const void* v_cache, int3
 int spd_grouped_gemv(const void* const* W, const float* const* x, float* const* y, int32_t G,
                      int32_t rows, int32_t cols, int32_t dtype, const float* nw, float eps,
                      void* stream) {
-  if (!W || !x || !y || G < 1 || G > kMaxExplicit || rows < 1 || cols < 8 || cols % 8 || cols > kGemvMaxCols ||
+  if (!W || !x || !y || G < 1 || G > kMaxExplicit || rows < 1 || cols < 8 || cols % 8 ||
       (dtype != SPD_DTYPE_F32 && dtype != SPD_DTYPE_BF16))
     return fail(nullptr, SPD_EINVAL, "spd_grouped_gemv: bad arguments");
   GemvExplicit ge;
@@ -828,8 +853,26 @@ int spd_grouped_gemv(const void* const* W, const float* const* x, float* const* 
   }
   if (nw && !aligned16(nw)) return fail(nullptr, SPD_EINVAL, "spd_grouped_gemv: norm weight unaligned");
   ge.G = G; ge.rows = rows; ge.cols = cols; ge.nw = nw;
-  cudaError_t e = gemv_setup_attributes();
-  if (e == cudaSuccess) e = launch_gemv_explicit(ge, dtype, eps, reinterpret_cast<cudaStream_t>(stream));
+  // tensor maps of the G weights: encoded here, held in stream-ordered scratch for this launch
+  std::vector<CUtensorMap> maps(G);
+  for (int g = 0; g < G; ++g) {
+    const cudaError_t em = gemv_encode_map(&maps[g], W[g], rows, cols, dtype);
+    if (em != cudaSuccess)
+      return fail(nullptr, SPD_ECUDA, "spd_grouped_gemv: tensor map %d: %s", g, cudaGetErrorString(em));
+  }
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  CUtensorMap* dmaps = nullptr;
+  cudaError_t e = cudaMallocAsync(reinterpret_cast<void**>(&dmaps), sizeof(CUtensorMap) * G, st);
+  if (e == cudaSuccess) e = cudaMemcpyAsync(dmaps, maps.data(), sizeof(CUtensorMap) * G, cudaMemcpyHostToDevice, st);
+  if (e == cudaSuccess) {
+    for (int g = 0; g < G; ++g) ge.tm[g] = dmaps + g;
+    e = gemv_setup_attributes();
+  }
+  if (e == cudaSuccess) e = launch_gemv_explicit(ge, dtype, eps, st);
+  if (dmaps) {
+    const cudaError_t ef = cudaFreeAsync(dmaps, st);
+    if (e == cudaSuccess) e = ef;
+  }
   if (e != cudaSuccess) return fail(nullptr, SPD_ECUDA, "%s", cudaGetErrorString(e));
   return SPD_OK;
 }

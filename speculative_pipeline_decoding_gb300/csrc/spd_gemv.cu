@@ -3,35 +3,42 @@
 // One launch computes y_g = W_g x_g for up to kMaxGroups groups.  Each group has its own weights,
 // operator and epilogue, so one launch can carry the stage-diagonal step of the target (the token
 // at depth j runs layer j*S+s, SPD summary 方法步骤详情 step 1) together with the draft module's rows
-// (steps 3-4).  Weight rows are streamed once from HBM with 1-D bulk copies (cp.async.bulk,
-// L2 evict-first) into a 4-deep ring of shared-memory stages guarded by mbarriers; one producer
-// warp issues the copies, eight consumer warps compute.
+// (steps 3-4).
+//
+// Weight streaming: one producer warp issues 2-D TMA tensor copies (cp.async.bulk.tensor, boxes of
+// 128 bytes x 32 rows with the 128-byte swizzle, L2 evict-first) into a 4-deep ring of 32 KB stages
+// guarded by mbarriers; a stage holds 64 weight rows x 512 bytes (4 boxes wide, 2 boxes high).
+// Every weight matrix has its own tensor map, encoded once when the handle is created.  Copies of
+// 4 KB keep the per-copy cost of the copy engine below the HBM time of the bytes it moves.
 //
 // Work split: every CTA of the persistent grid (one per SM) takes a contiguous share of the
-// launch's weight bytes, cut at row boundaries; tiles never straddle a group or a share.
+// launch's weight bytes, cut at 32-row boundaries; tiles never straddle a group or a share.
 //
-// Two compute paths:
-//  * single input vector (target step, plain AR, heads): the group's activation, RMS-normalised
-//    when the operator has a norm, is staged once in shared memory as fp32.  A stage holds 16
-//    weight rows x 2 KB; consumer warp w owns rows w and w+8 of the stage (for gate/up: the gate
-//    and up rows of one output), lane l the 16-byte column vectors l, l+32, l+64, l+96 of each
-//    2 KB chunk.  Partial sums stay in registers across chunks; a row ends with one xor-tree warp
-//    reduction.  A row's arithmetic depends only on its column count, never on the other groups
-//    of the launch, so a token's results are bit-identical in plain AR and in the SPD step.
+// Two compute paths, eight consumer warps:
+//  * single input vector (target step, plain AR, heads): warp w owns weight rows w, w+8, ..., w+56
+//    of the stage, lane l the 16-byte column vector l of each 512-byte row slice (bf16: columns
+//    8l..8l+7); the activation slice (RMS-normalised when the operator has a norm) comes through
+//    L1 and is reused over the warp's 8 rows.  Partial sums stay in registers across stages; a row
+//    ends with one xor-tree warp reduction.  A row's arithmetic depends only on its column count,
+//    never on the other groups of the launch, so a token's results are bit-identical in plain AR
+//    and in the SPD step.
 //  * several input vectors sharing the weights (draft-module rows, prefill blocks; bf16 weights):
-//    m16n8k16 bf16 tensor-core MMAs with fp32 accumulation.  A stage holds 32 rows x 1 KB; the fp32
-//    activations are split into bf16 high and low halves (x = hi + lo keeps ~16 significant bits)
-//    and both are multiplied into the accumulator; warps take interleaved 16-column k-steps and
-//    their partial tiles are added in warp order.
+//    m16n8k16 bf16 tensor-core MMAs with fp32 accumulation, the weight rows as the n8 operand
+//    (ldmatrix through the swizzle) and the vectors as the m16 operand.  The fp32 activations are
+//    split into bf16 high and low halves (x = hi + lo keeps ~16 significant bits) and both are
+//    multiplied into the accumulator.  Warp w takes the two 16-column k-steps 32w..32w+31 of every
+//    stage; the eight partial tiles are added in warp order at the end of a tile.
 //
 // Epilogues (per group):
 //   STORE   y = W x                                  (anchor FC, stand-alone operator)
 //   RESID   h += W x, anchor capture when the layer index + 1 = b_i   (o-proj, down)
 //   SWIGLU  u = silu(W_gate x) * (W_up x)            (gate/up; x = RMSNorm(h) * ffn_norm)
-//   QKV     x = RMSNorm(h) * attn_norm; q and k rotated by RoPE (rotate-half pairs i, i+hd/2, which
-//           a tile holds together), q written for attention, k and v rounded to the cache dtype and
-//           appended to the layer's KV cache at position pos-1
+//   QKV     x = RMSNorm(h) * attn_norm; q and k rotated by RoPE (rotate-half pairs i, i+hd/2: a tile
+//           holds 32 rows of a head and their 32 partners), q written for attention, k and v
+//           rounded to the cache dtype and appended to the layer's KV cache at position pos-1
 //   TOP2    logits of the vocab head; per-CTA top-2 (+ optional full logits for debugging)
+#include <cudaTypedefs.h>
+
 #include "spd_internal.cuh"
 
 namespace spd {
@@ -41,27 +48,23 @@ namespace {
 constexpr int kBig = 1 << 30;
 constexpr int kNCW = 8;                        // consumer warps
 constexpr int kThreads = (kNCW + 1) * 32;      // + one producer warp
-constexpr int kSlotsF = 16;                    // single-vector path: weight rows per stage
-constexpr int kChunkF = 2048;                  // bytes of each row per stage
-constexpr int kPitchF = kChunkF + 16;
-constexpr int kSlotsM = 32;                    // tensor-core path: weight rows per stage
-constexpr int kChunkM = 1024;
-constexpr int kPitchM = kChunkM + 16;          // 16-byte pad: ldmatrix rows in distinct banks
-constexpr int kStageBytes = (kSlotsF * kPitchF > kSlotsM * kPitchM) ? kSlotsF * kPitchF : kSlotsM * kPitchM;
+constexpr int kBoxRows = 32;                   // rows of one tensor-map box (128 bytes wide)
+constexpr int kBoxBytes = kBoxRows * 128;
+constexpr int kSlots = 64;                     // weight rows per stage (2 boxes high)
+constexpr int kStageBytes = kSlots * 512;      // 4 boxes wide
 constexpr int kStages = 4;
-constexpr int kXhatFloats = kGemvMaxCols;      // staged activation (single-vector groups)
-constexpr int kDynSmem = kStages * kStageBytes + kXhatFloats * 4;
-constexpr int kMaxNT = 4;                      // tensor-core path: up to 4 n-tiles of 8 vectors
-static_assert(kNCW * 2 * kMaxNT * 4 * 32 <= kXhatFloats, "mma reduction buffer must fit");
+constexpr int kRedFloats = kNCW * 8 * 4 * 32;  // tensor-core partial tiles of one m-tile (32 KB)
+constexpr int kDynSmem = 1024 + kStages * kStageBytes + kRedFloats * 4;
+constexpr int kMaxMT = 2;                      // tensor-core path: up to 2 m-tiles of 16 vectors
 
 enum Epi { EPI_STORE = 0, EPI_RESID = 1, EPI_SWIGLU = 2, EPI_QKV = 3, EPI_TOP2 = 4 };
 
 struct GG {
-  const void* w[3];            // weight segments (QKV: wq | wk | wv) ; gate/up: w[0] gate, w[1] up
+  const CUtensorMap* m[3];     // tensor maps of the segments (QKV: wq | wk | wv); gate/up: gate, up
   int seg1, seg2;              // first row of segment 1 and 2
   int rows, cols;              // output rows (gate/up: rows of each weight), input columns
   short nv, nw, epi, kind;     // vectors, weights per output row, epilogue, head kind
-  short mma, tr;               // tensor-core path; tile rows
+  short mma, tr;               // tensor-core path; tile height in output rows (64 / nw)
   const float* x; int xrow0, xring, xstride;
   float* y; int yrow0, yring, ystride;
   const float* normw;
@@ -109,25 +112,25 @@ __device__ int add_part(const GemvParams& p, const GemvPart& pt, GG* gg, int ng)
   const Act& A = lc.act;
   DevState* st = B.st;
   if (pt.op == OP_HEAD) {
-    auto add = [&](const float* x, int xrow0, int xring, const void* W, const float* nw, int kind) {
+    auto add = [&](const float* x, int xrow0, int xring, const CUtensorMap* W, const float* nw, int kind) {
       GG& o = gg[ng++];
       gg_clear(o);
-      o.w[0] = o.w[1] = o.w[2] = W;
+      o.m[0] = o.m[1] = o.m[2] = W;
       o.rows = D.V; o.cols = D.d;
       o.x = x; o.xrow0 = xrow0; o.xring = xring; o.xstride = D.d;
       o.y = nullptr; o.normw = nw; o.epi = EPI_TOP2; o.kind = kind;
     };
     if (lc.kind == LK_DIAG) {
-      if (st->a == D.n) add(B.resid, (st->t - D.n + 1) % (D.n + 1), D.n + 1, B.lm_head, B.final_norm, 0);
+      if (st->a == D.n) add(B.resid, (st->t - D.n + 1) % (D.n + 1), D.n + 1, B.tm_lm, B.final_norm, 0);
       if (!(st->flags & SF_TARGET_ONLY)) {
         const int R = st->t - st->pdm_len;
         if (R < 1 || R > D.n + 1) set_err(st, ERR_PDM_ROWS, 200);
-        else add(A.qkv /* draft rows z */, R - 1, kBig, B.pdm_head, B.pdm_norm, 1);
+        else add(A.qkv /* draft rows z */, R - 1, kBig, B.tm_pdm, B.pdm_norm, 1);
       }
     } else if (lc.kind == LK_AR) {
-      add(B.resid, st->t % (D.n + 1), D.n + 1, B.lm_head, B.final_norm, 0);
+      add(B.resid, st->t % (D.n + 1), D.n + 1, B.tm_lm, B.final_norm, 0);
     } else if (lc.kind == LK_ROWS) {
-      add(A.resid, lc.cnt - 1, kBig, B.lm_head, B.final_norm, 0);
+      add(A.resid, lc.cnt - 1, kBig, B.tm_lm, B.final_norm, 0);
     }
     return ng;
   }
@@ -137,7 +140,7 @@ __device__ int add_part(const GemvParams& p, const GemvPart& pt, GG* gg, int ng)
       const int f = D.ftab[D.n];
       GG& o = gg[ng++];
       gg_clear(o);
-      o.w[0] = o.w[1] = o.w[2] = B.fc[f];
+      o.m[0] = o.m[1] = o.m[2] = B.tm_fc[f];
       o.rows = D.d; o.cols = (f + 1) * D.d; o.nv = lc.cnt;
       o.x = A.anch; o.xstride = D.m * D.d;
       o.y = A.resid; o.ystride = D.d;
@@ -156,7 +159,7 @@ __device__ int add_part(const GemvParams& p, const GemvPart& pt, GG* gg, int ng)
       if (f != prev_f) {
         GG& o = gg[ng++];
         gg_clear(o);
-        o.w[0] = o.w[1] = o.w[2] = B.fc[f];
+        o.m[0] = o.m[1] = o.m[2] = B.tm_fc[f];
         o.rows = D.d; o.cols = (f + 1) * D.d; o.nv = 0;
         o.x = B.anch; o.xrow0 = pos % (D.n + 1); o.xring = D.n + 1; o.xstride = D.m * D.d;
         o.y = A.resid; o.yrow0 = r; o.ystride = D.d;
@@ -179,7 +182,7 @@ __device__ int add_part(const GemvParams& p, const GemvPart& pt, GG* gg, int ng)
     o.nv = rg[i].nv;
     switch (pt.op) {
       case OP_QKV:
-        o.w[0] = w.wq; o.w[1] = w.wk; o.w[2] = w.wv;
+        o.m[0] = w.tq; o.m[1] = w.tk; o.m[2] = w.tv;
         o.seg1 = hqd; o.seg2 = hqd + D.hkv * D.hd; o.rows = D.qkv_rows; o.cols = D.d;
         o.x = A.resid; o.xrow0 = rg[i].rrow0; o.xring = A.resid_ring; o.xstride = D.d;
         o.normw = (const float*)w.attn_norm;
@@ -191,14 +194,14 @@ __device__ int add_part(const GemvParams& p, const GemvPart& pt, GG* gg, int ng)
         o.kvlen = (lc.stack == 0 && B.kvlen) ? B.kvlen + rg[i].layer : nullptr;
         break;
       case OP_O:
-        o.w[0] = o.w[1] = o.w[2] = w.wo;
+        o.m[0] = o.m[1] = o.m[2] = w.to;
         o.rows = D.d; o.cols = hqd;
         o.x = A.attn; o.xrow0 = rg[i].vid0; o.xstride = hqd;
         o.y = A.resid; o.yrow0 = rg[i].rrow0; o.yring = A.resid_ring; o.ystride = D.d;
         o.epi = EPI_RESID;
         break;
       case OP_GATEUP:
-        o.w[0] = w.wg; o.w[1] = w.wu; o.w[2] = w.wu; o.nw = 2;
+        o.m[0] = w.tg; o.m[1] = w.tu; o.m[2] = w.tu; o.nw = 2;
         o.rows = D.ffn; o.cols = D.d;
         o.x = A.resid; o.xrow0 = rg[i].rrow0; o.xring = A.resid_ring; o.xstride = D.d;
         o.normw = (const float*)w.ffn_norm;
@@ -206,7 +209,7 @@ __device__ int add_part(const GemvParams& p, const GemvPart& pt, GG* gg, int ng)
         o.epi = EPI_SWIGLU;
         break;
       default: {  // OP_DOWN
-        o.w[0] = o.w[1] = o.w[2] = w.wd;
+        o.m[0] = o.m[1] = o.m[2] = w.td;
         o.rows = D.d; o.cols = D.ffn;
         o.x = A.u; o.xrow0 = rg[i].vid0; o.xstride = D.ffn;
         o.y = A.resid; o.yrow0 = rg[i].rrow0; o.yring = A.resid_ring; o.ystride = D.d;
@@ -227,7 +230,7 @@ __device__ int resolve_groups(const GemvParams& p, GG* gg) {
     for (int g = 0; g < p.ge.G; ++g) {
       GG& o = gg[ng++];
       gg_clear(o);
-      o.w[0] = o.w[1] = o.w[2] = p.ge.W[g];
+      o.m[0] = o.m[1] = o.m[2] = p.ge.tm[g];
       o.rows = p.ge.rows; o.cols = p.ge.cols;
       o.x = p.ge.x[g]; o.xstride = p.ge.cols;
       o.y = p.ge.y[g]; o.ystride = p.ge.rows;
@@ -236,13 +239,11 @@ __device__ int resolve_groups(const GemvParams& p, GG* gg) {
   } else {
     for (int i = 0; i < p.nparts; ++i) ng = add_part(p, p.part[i], gg, ng);
   }
-  // paths; split multi-vector groups the tensor cores cannot take
-  // (a tensor-core QKV tile holds 16 rotary pairs, so it needs head_dim/2 % 16 == 0)
+  // paths; without tensor cores (fp32 weights) a multi-vector group becomes one group per vector
   int out = ng;
   for (int g = ng - 1; g >= 0; --g) {
     GG& o = gg[g];
-    const bool mma_ok = p.has_mma && o.cols % 16 == 0 && (o.epi != EPI_QKV || (p.D.hd / 2) % 16 == 0);
-    if (o.nv > 1 && !mma_ok) {
+    if (o.nv > 1 && !p.has_mma) {
       const int nv = o.nv;
       if (out + nv - 1 > kMaxGroups) { set_err(p.B.st, ERR_BOUNDS, 90); return 0; }
       for (int k = out - 1; k > g; --k) gg[k + nv - 1] = gg[k];  // make room after g
@@ -259,11 +260,9 @@ __device__ int resolve_groups(const GemvParams& p, GG* gg) {
   long long cost = 0;
   for (int g = 0; g < ng; ++g) {
     GG& o = gg[g];
-    if (o.nv > 1 || o.cols > kXhatFloats) {
-      if (!(p.has_mma && o.cols % 16 == 0) || o.nv > 8 * kMaxNT) { set_err(p.B.st, ERR_BOUNDS, 91); return 0; }
-      o.mma = 1;
-    }
-    o.tr = (short)((o.mma ? kSlotsM : kSlotsF) / o.nw);
+    if (o.nv > 16 * kMaxMT) { set_err(p.B.st, ERR_BOUNDS, 91); return 0; }
+    o.mma = o.nv > 1;
+    o.tr = (short)(kSlots / o.nw);
     o.cost0 = cost;
     cost += (long long)o.rows * rowcost(o);
   }
@@ -271,15 +270,16 @@ __device__ int resolve_groups(const GemvParams& p, GG* gg) {
 }
 
 // Row boundary of weight-cost position X: first row of the group holding X whose cost prefix is
-// >= X; rows of the rotary region of a QKV group are rounded down to whole tiles so that each tile
-// holds complete (i, i+hd/2) pairs.  Monotone in X, so neighbouring shares meet exactly.
+// >= X, rounded down to a 32-row box (to a whole 64-row tile in the rotary region of a QKV group,
+// whose tiles hold complete (i, i+hd/2) pairs).  Monotone in X, so neighbouring shares meet exactly.
 __device__ void locate(const GG* gg, int ng, long long X, int& g, int& r) {
   g = 0;
   while (g < ng && X >= gg[g].cost0 + (long long)gg[g].rows * rowcost(gg[g])) ++g;
   if (g >= ng) { g = ng; r = 0; return; }
   const long long rc = rowcost(gg[g]);
   r = (int)((X - gg[g].cost0 + rc - 1) / rc);
-  if (gg[g].epi == EPI_QKV && r < gg[g].seg2) r -= r % gg[g].tr;
+  const int gran = (gg[g].epi == EPI_QKV && r < gg[g].seg2) ? kSlots : kBoxRows;
+  r -= r % gran;
   if (r >= gg[g].rows) { ++g; r = 0; }
 }
 
@@ -289,21 +289,29 @@ __device__ __forceinline__ float warp_sum(float v) {
   return v;
 }
 
-// Physical weight row of virtual row `r` of a group.  In the rotary region of a QKV group a tile
-// of 2P virtual rows holds rows i0..i0+P-1 and i0+hd/2..i0+hd/2+P-1 of one head (P = tile/2).
+// Physical weight row of virtual row `r` of a group.  In the rotary region of a QKV group a
+// 64-row tile holds rows i0..i0+31 of one head and their partners i0+hd/2..i0+hd/2+31.
 __device__ __forceinline__ int phys_row(const GG& G, int r, int hd) {
   if (G.epi != EPI_QKV || r >= G.seg2) return r;
-  const int P = G.tr / 2;
   const int h = r / hd, vb = r % hd;
-  const int blk = vb / G.tr, j = vb % G.tr;
-  return h * hd + (j < P ? blk * P + j : hd / 2 + blk * P + (j - P));
+  const int blk = vb / kSlots, j = vb % kSlots;
+  return h * hd + (j < kBoxRows ? blk * kBoxRows + j : hd / 2 + blk * kBoxRows + (j - kBoxRows));
 }
 
-__device__ __forceinline__ const unsigned char* row_src(const GG& G, int prow, int wi, int esz) {
-  if (G.nw == 2) return (const unsigned char*)G.w[wi] + (size_t)prow * G.cols * esz;
-  const int sg = prow < G.seg1 ? 0 : (prow < G.seg2 ? 1 : 2);
-  const int off = sg == 0 ? 0 : (sg == 1 ? G.seg1 : G.seg2);
-  return (const unsigned char*)G.w[sg] + (size_t)(prow - off) * G.cols * esz;
+__device__ __forceinline__ void tma_box(void* dst, const CUtensorMap* map, int x, int y, uint64_t* bar,
+                                        uint64_t pol) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(smem_u32(dst)), "l"(map), "r"(x), "r"(y),
+      "r"(smem_u32(bar)), "l"(pol)
+      : "memory");
+}
+
+// Byte offset in a stage of the 16-byte chunk `j` (0..31 across the 512-byte row slice) of slot
+// `slot` (0..63): box (slot/32, j/8), row slot%32, 128-byte swizzle (chunk ^ row % 8).
+__device__ __forceinline__ uint32_t stage_off(int slot, int j) {
+  const int rb = slot >> 5, rr = slot & 31;
+  return (uint32_t)(((rb * 4 + (j >> 3)) * kBoxBytes) + rr * 128 + (((j & 7) ^ (rr & 7)) << 4));
 }
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo_k, float hi_k) {
@@ -384,21 +392,22 @@ __device__ __forceinline__ void epilogue(const GemvParams& p, const GG& G, int v
 
 template <typename WT>
 __global__ void __launch_bounds__(kThreads, 1) gemv_engine(const __grid_constant__ GemvParams p) {
-  extern __shared__ __align__(128) unsigned char smem[];
-  unsigned char* ring = smem;
-  float* xhat = reinterpret_cast<float*>(smem + kStages * kStageBytes);
-  constexpr int VEC = WTraits<WT>::kVec;
-  constexpr int ESZ = sizeof(WT);
-  constexpr int CWF = kChunkF / ESZ;                  // columns per single-vector chunk
-  constexpr int CWM = kChunkM / 2;                    // columns per tensor-core chunk (bf16)
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  // the 128-byte swizzle wants 1024-byte aligned boxes
+  unsigned char* ring =
+      reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+  float* red = reinterpret_cast<float*>(ring + kStages * kStageBytes);
+  constexpr int VEC = WTraits<WT>::kVec;   // elements per 16-byte chunk
+  constexpr int CW = 512 / sizeof(WT);     // columns per stage
+  constexpr int BOXC = 128 / sizeof(WT);   // columns per box
 
   __shared__ GG gg[kMaxGroups];
   __shared__ int s_ng, s_gb, s_rb, s_ge, s_re;
   __shared__ __align__(8) uint64_t full_bar[kStages];
   __shared__ __align__(8) uint64_t empty_bar[kStages];
-  __shared__ float rstd_s[8 * kMaxNT];
+  __shared__ float rstd_s[16 * kMaxMT];
   __shared__ float wpart[kNCW];
-  __shared__ Top2 hred[kNCW][2];
+  __shared__ Top2 hred[kNCW * 8][2];
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   DevState* st = p.B.st;
@@ -412,7 +421,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_engine(const __grid_constant
     const bool skip = !p.explicit_mode && (st->done || st->err);
     const int ng = skip ? 0 : resolve_groups(p, gg);
     s_ng = ng;
-    long long total = ng ? gg[ng - 1].cost0 + (long long)gg[ng - 1].rows * rowcost(gg[ng - 1]) : 0;
+    const long long total = ng ? gg[ng - 1].cost0 + (long long)gg[ng - 1].rows * rowcost(gg[ng - 1]) : 0;
     int gb = ng, rb = 0, ge = ng, re = 0;
     if (ng) {
       locate(gg, ng, total * blockIdx.x / gridDim.x, gb, rb);
@@ -423,6 +432,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_engine(const __grid_constant
   __syncthreads();
   const int ng = s_ng;
   const int gbeg = s_gb, rbeg = s_rb, gend = s_ge, rend = s_re;
+  const int hd = p.D.hd;
 
   if (warp == kNCW) {
     // ------------------------------ producer warp ------------------------------
@@ -433,12 +443,22 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_engine(const __grid_constant
       const GG& G = gg[g];
       const int last = (g == gend) ? rend : G.rows;
       const int tr = min((int)G.tr, last - r);
-      const int nslot = G.mma ? kSlotsM : kSlotsF;
-      const int pitch = G.mma ? kPitchM : kPitchF;
-      const int cw = G.mma ? CWM : CWF;
-      const int per_w = nslot / G.nw;
-      for (int c0 = 0; c0 < G.cols; c0 += cw) {
-        const uint32_t brow = (uint32_t)min(cw, G.cols - c0) * ESZ;
+      const int nrb = G.nw == 2 ? 2 : (tr + kBoxRows - 1) / kBoxRows;  // row boxes per stage
+      // tensor map and first row of each row box
+      const CUtensorMap* m0;
+      const CUtensorMap* m1;
+      int y0, y1;
+      if (G.nw == 2) {
+        m0 = G.m[0]; m1 = G.m[1]; y0 = y1 = r;
+      } else {
+        const int p0 = phys_row(G, r, hd), p1 = phys_row(G, r + kBoxRows, hd);
+        const int s0 = p0 < G.seg1 ? 0 : (p0 < G.seg2 ? 1 : 2);
+        const int s1 = p1 < G.seg1 ? 0 : (p1 < G.seg2 ? 1 : 2);
+        m0 = G.m[s0]; m1 = G.m[s1];
+        y0 = p0 - (s0 == 0 ? 0 : (s0 == 1 ? G.seg1 : G.seg2));
+        y1 = p1 - (s1 == 0 ? 0 : (s1 == 1 ? G.seg1 : G.seg2));
+      }
+      for (int c0 = 0; c0 < G.cols; c0 += CW) {
         const int s = ctr % kStages;
         if (ctr >= (uint32_t)kStages &&
             !mbar_wait_bounded(&empty_bar[s], ((ctr / kStages) - 1) & 1)) {
@@ -446,15 +466,12 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_engine(const __grid_constant
           failed = true;
           break;
         }
-        if (lane == 0) mbar_arrive_expect_tx(&full_bar[s], brow * tr * G.nw);
+        if (lane == 0) mbar_arrive_expect_tx(&full_bar[s], (uint32_t)(nrb * 4 * kBoxBytes));
         __syncwarp();
-        if (lane < nslot) {
-          const int wi = lane / per_w, ri = lane % per_w;
-          if (ri < tr) {
-            const int prow = phys_row(G, r + ri, p.D.hd);
-            bulk_g2s(ring + (size_t)s * kStageBytes + (size_t)lane * pitch,
-                     row_src(G, prow, wi, ESZ) + (size_t)c0 * ESZ, brow, &full_bar[s], pol);
-          }
+        if (lane < nrb * 4) {
+          const int rb = lane >> 2, cb = lane & 3;
+          tma_box(ring + (size_t)s * kStageBytes + (size_t)(rb * 4 + cb) * kBoxBytes, rb ? m1 : m0,
+                  c0 + cb * BOXC, rb ? y1 : y0, &full_bar[s], pol);
         }
         ++ctr;
       }
@@ -477,20 +494,19 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_engine(const __grid_constant
   Top2 loc[2];
   top2_init(loc[0]);
   top2_init(loc[1]);
-  const int gq = lane >> 2, tq = lane & 3;                       // mma fragment coordinates
-  const int lm_row = (lane & 7) + 8 * ((lane >> 3) & 1), lm_k = 8 * (lane >> 4);
+  const int gq = lane >> 2, tq = lane & 3;   // mma fragment coordinates
+  float rstd = 1.f;                          // single-vector path: 1/rms of the group's input
   int last_g = -1;
   for (int g = gbeg, r = rbeg; g < gend || (g == gend && r < rend);) {
     const GG& G = gg[g];
     const int last = (g == gend) ? rend : G.rows;
     const int tr = min((int)G.tr, last - r);
-    if (g != last_g) {
-      // group entry: stage the (normalised) activation, or the per-vector rstd for the mma path
+    if (g != last_g) {  // group entry: 1/rms of the input vector(s)
       named_bar(1, NCT);
+      rstd = 1.f;
       if (!G.mma) {
-        const float* xr = G.x + (size_t)(G.xrow0 % G.xring) * G.xstride;
-        float rstd = 1.f;
         if (G.normw) {
+          const float* xr = G.x + (size_t)(G.xrow0 % G.xring) * G.xstride;
           float sq = 0.f;
           for (int c = tid * 4; c < G.cols; c += NCT * 4) {
             const float4 q = *reinterpret_cast<const float4*>(xr + c);
@@ -503,15 +519,6 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_engine(const __grid_constant
 #pragma unroll
           for (int w8 = 0; w8 < kNCW; ++w8) tot += wpart[w8];
           rstd = 1.0f / sqrtf(tot / (float)G.cols + p.eps);
-        }
-        for (int c = tid * 4; c < G.cols; c += NCT * 4) {
-          float4 q = *reinterpret_cast<const float4*>(xr + c);
-          if (G.normw) {
-            const float4 n4 = *reinterpret_cast<const float4*>(G.normw + c);
-            q.x = q.x * rstd * n4.x; q.y = q.y * rstd * n4.y;
-            q.z = q.z * rstd * n4.z; q.w = q.w * rstd * n4.w;
-          }
-          *reinterpret_cast<float4*>(xhat + c) = q;
         }
       } else if (G.normw) {
         for (int v = warp; v < G.nv; v += kNCW) {
@@ -530,43 +537,44 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_engine(const __grid_constant
     }
     if (!G.mma) {
       // ---------------- single-vector path ----------------
-      float acc0 = 0.f, acc1 = 0.f;   // slots warp and warp + 8
-      const bool v0 = G.nw == 2 ? warp < tr : warp < tr;
-      const bool v1 = G.nw == 2 ? warp < tr : warp + 8 < tr;
-      const unsigned char* sbase = ring;
-      for (int c0 = 0; c0 < G.cols; c0 += CWF) {
-        const int nvec = min(CWF, G.cols - c0) / VEC;
+      const float* xr = G.x + (size_t)(G.xrow0 % G.xring) * G.xstride;
+      float acc[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) acc[i] = 0.f;
+      for (int c0 = 0; c0 < G.cols; c0 += CW) {
         const int s = ctr % kStages;
         if (!failed && !mbar_wait_bounded(&full_bar[s], (ctr / kStages) & 1)) {
           if (lane == 0) set_err(st, ERR_TIMEOUT, 50);
           failed = true;
         }
         if (!failed) {
-          const unsigned char* sb = sbase + (size_t)s * kStageBytes;
-          const unsigned char* r0p = sb + (size_t)warp * kPitchF;
-          const unsigned char* r1p = sb + (size_t)(warp + 8) * kPitchF;
+          const int col = c0 + VEC * lane;
+          float xv[VEC];
+          if (col < G.cols) {
 #pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            const int k = lane + 32 * j;
-            if (k < nvec) {
-              float xv[VEC];
-#pragma unroll
-              for (int e = 0; e < VEC; e += 4) {
-                const float4 q = *reinterpret_cast<const float4*>(xhat + c0 + k * VEC + e);
-                xv[e] = q.x; xv[e + 1] = q.y; xv[e + 2] = q.z; xv[e + 3] = q.w;
+            for (int e = 0; e < VEC; e += 4) {
+              float4 q = *reinterpret_cast<const float4*>(xr + col + e);
+              if (G.normw) {
+                const float4 n4 = *reinterpret_cast<const float4*>(G.normw + col + e);
+                q.x = q.x * rstd * n4.x; q.y = q.y * rstd * n4.y;
+                q.z = q.z * rstd * n4.z; q.w = q.w * rstd * n4.w;
               }
-              if (v0) {
-                float wf[VEC];
-                WTraits<WT>::unpack(*reinterpret_cast<const uint4*>(r0p + k * 16), wf);
+              xv[e] = q.x; xv[e + 1] = q.y; xv[e + 2] = q.z; xv[e + 3] = q.w;
+            }
+          } else {
 #pragma unroll
-                for (int e = 0; e < VEC; ++e) acc0 = fmaf(wf[e], xv[e], acc0);
-              }
-              if (v1) {
-                float wf[VEC];
-                WTraits<WT>::unpack(*reinterpret_cast<const uint4*>(r1p + k * 16), wf);
+            for (int e = 0; e < VEC; ++e) xv[e] = 0.f;
+          }
+          const unsigned char* sb = ring + (size_t)s * kStageBytes;
 #pragma unroll
-                for (int e = 0; e < VEC; ++e) acc1 = fmaf(wf[e], xv[e], acc1);
-              }
+          for (int i = 0; i < 8; ++i) {
+            const int slot = warp + 8 * i;
+            const bool ok = G.nw == 2 ? ((slot & 31) < tr) : (slot < tr);
+            if (ok) {
+              float wf[VEC];
+              WTraits<WT>::unpack(*reinterpret_cast<const uint4*>(sb + stage_off(slot, lane)), wf);
+#pragma unroll
+              for (int e = 0; e < VEC; ++e) acc[i] = fmaf(wf[e], xv[e], acc[i]);
             }
           }
         }
@@ -574,78 +582,91 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_engine(const __grid_constant
         if (lane == 0) mbar_arrive(&empty_bar[s]);
         ++ctr;
       }
-      const float y0 = warp_sum(acc0), y1 = warp_sum(acc1);
-      if (lane == 0 && !failed) {
+      float sums[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) sums[i] = warp_sum(acc[i]);
+      if (!failed && lane < 8) {  // lane i finishes slot warp + 8i (and its partner slot + 32)
+        float y0 = 0.f, y1 = 0.f;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          if (k == lane) y0 = sums[k];
+          if (k == lane + 4) y1 = sums[k];
+        }
+        const int slot = warp + 8 * lane;
         if (G.nw == 2) {
-          if (v0) epilogue<WT>(p, G, 0, r + warp, y0, y1, false, loc);
+          if (lane < 4 && slot < tr) epilogue<WT>(p, G, 0, r + slot, y0, y1, false, loc);
         } else if (G.epi == EPI_QKV && r < G.seg2) {
-          if (v0) epilogue<WT>(p, G, 0, phys_row(G, r + warp, p.D.hd), y0, y1, true, loc);
-        } else {
-          if (v0) epilogue<WT>(p, G, 0, r + warp, y0, 0.f, false, loc);
-          if (v1) epilogue<WT>(p, G, 0, r + warp + 8, y1, 0.f, false, loc);
+          if (lane < 4) epilogue<WT>(p, G, 0, phys_row(G, r + slot, hd), y0, y1, true, loc);
+        } else if (slot < tr) {
+          epilogue<WT>(p, G, 0, r + slot, y0, 0.f, false, loc);
         }
       }
     } else {
       // ---------------- tensor-core path (bf16 weights, several vectors) ----------------
       const int nv = G.nv;
-      const int NT = (nv + 7) / 8;
-      const float* xrow[kMaxNT];
-      float rsv[kMaxNT];
+      const int MT = (nv + 15) / 16;
+      float acc[kMaxMT][8][4];
 #pragma unroll
-      for (int nt = 0; nt < kMaxNT; ++nt) {
-        const int v = nt * 8 + gq;
-        xrow[nt] = v < nv ? G.x + (size_t)((G.xrow0 + v) % G.xring) * G.xstride : nullptr;
-        rsv[nt] = (v < nv && G.normw) ? rstd_s[v] : 1.f;
-      }
-      float acc[2][kMaxNT][4];
+      for (int i = 0; i < kMaxMT; ++i)
 #pragma unroll
-      for (int i = 0; i < 2; ++i)
-#pragma unroll
-        for (int j = 0; j < kMaxNT; ++j)
+        for (int j = 0; j < 8; ++j)
 #pragma unroll
           for (int e = 0; e < 4; ++e) acc[i][j][e] = 0.f;
-      for (int c0 = 0; c0 < G.cols; c0 += CWM) {
-        const int ksteps = min(CWM, G.cols - c0) / 16;
+      // activation pair (k, k+1) of vector v, normalised, 0 outside the matrix
+      auto ldx = [&](int v, int k) -> float2 {
+        float2 q = make_float2(0.f, 0.f);
+        if (v < nv && k < G.cols) {
+          q = *reinterpret_cast<const float2*>(G.x + (size_t)((G.xrow0 + v) % G.xring) * G.xstride + k);
+          if (G.normw) {
+            const float2 n2 = *reinterpret_cast<const float2*>(G.normw + k);
+            const float rs = rstd_s[v];
+            q.x = q.x * rs * n2.x; q.y = q.y * rs * n2.y;
+          }
+        }
+        return q;
+      };
+      const int kb = warp * 32;                 // this warp's 32 columns of each stage
+      const int jb = (kb >> 3) + (lane >> 3);   // its ldmatrix chunk (0..31)
+      for (int c0 = 0; c0 < G.cols; c0 += CW) {
         const int s = ctr % kStages;
         if (!failed && !mbar_wait_bounded(&full_bar[s], (ctr / kStages) & 1)) {
           if (lane == 0) set_err(st, ERR_TIMEOUT, 60);
           failed = true;
         }
         if (!failed) {
-          const uint32_t sb = smem_u32(ring + (size_t)s * kStageBytes);
-          for (int ks = warp; ks < ksteps; ks += kNCW) {
-            const int col = c0 + ks * 16;
-            uint32_t a[2][4];
+          uint32_t ah[kMaxMT][2][4], al[kMaxMT][2][4];
 #pragma unroll
-            for (int at = 0; at < 2; ++at)
-              ldmatrix_x4(sb + (uint32_t)((at * 16 + lm_row) * kPitchM + (ks * 16 + lm_k) * 2), a[at][0],
-                          a[at][1], a[at][2], a[at][3]);
+          for (int mt = 0; mt < kMaxMT; ++mt) {
+            if (mt < MT) {
 #pragma unroll
-            for (int nt = 0; nt < kMaxNT; ++nt) {
-              if (nt < NT) {
-                float x0 = 0.f, x1 = 0.f, x2 = 0.f, x3 = 0.f;
-                if (xrow[nt]) {
-                  const int k0 = col + 2 * tq;
-                  const float2 u = *reinterpret_cast<const float2*>(xrow[nt] + k0);
-                  const float2 w8 = *reinterpret_cast<const float2*>(xrow[nt] + k0 + 8);
-                  x0 = u.x; x1 = u.y; x2 = w8.x; x3 = w8.y;
-                  if (G.normw) {
-                    const float2 n0 = *reinterpret_cast<const float2*>(G.normw + k0);
-                    const float2 n8 = *reinterpret_cast<const float2*>(G.normw + k0 + 8);
-                    x0 = x0 * rsv[nt] * n0.x; x1 = x1 * rsv[nt] * n0.y;
-                    x2 = x2 * rsv[nt] * n8.x; x3 = x3 * rsv[nt] * n8.y;
-                  }
+              for (int ks = 0; ks < 2; ++ks) {
+                const int k = c0 + kb + 16 * ks + 2 * tq;
+                const int v0 = mt * 16 + gq;
+                const float2 q[4] = {ldx(v0, k), ldx(v0 + 8, k), ldx(v0, k + 8), ldx(v0 + 8, k + 8)};
+#pragma unroll
+                for (int f = 0; f < 4; ++f) {
+                  const __nv_bfloat16 hx = __float2bfloat16_rn(q[f].x), hy = __float2bfloat16_rn(q[f].y);
+                  const float fx = __bfloat162float(hx), fy = __bfloat162float(hy);
+                  ah[mt][ks][f] = pack_bf16x2(fx, fy);
+                  al[mt][ks][f] = pack_bf16x2(q[f].x - fx, q[f].y - fy);
                 }
-                const __nv_bfloat16 h0 = __float2bfloat16_rn(x0), h1 = __float2bfloat16_rn(x1);
-                const __nv_bfloat16 h2 = __float2bfloat16_rn(x2), h3 = __float2bfloat16_rn(x3);
-                const uint32_t bh0 = pack_bf16x2(__bfloat162float(h0), __bfloat162float(h1));
-                const uint32_t bh1 = pack_bf16x2(__bfloat162float(h2), __bfloat162float(h3));
-                const uint32_t bl0 = pack_bf16x2(x0 - __bfloat162float(h0), x1 - __bfloat162float(h1));
-                const uint32_t bl1 = pack_bf16x2(x2 - __bfloat162float(h2), x3 - __bfloat162float(h3));
+              }
+            }
+          }
+          const uint32_t sb = smem_u32(ring + (size_t)s * kStageBytes);
 #pragma unroll
-                for (int at = 0; at < 2; ++at) {
-                  mma_bf16(acc[at][nt], a[at], bh0, bh1);
-                  mma_bf16(acc[at][nt], a[at], bl0, bl1);
+          for (int nt = 0; nt < 8; ++nt) {
+            const bool ok = G.nw == 2 ? (((nt * 8) & 31) < tr) : (nt * 8 < tr);
+            if (ok) {
+              uint32_t b0, b1, b2, b3;
+              ldmatrix_x4(sb + stage_off(nt * 8 + (lane & 7), jb), b0, b1, b2, b3);
+#pragma unroll
+              for (int mt = 0; mt < kMaxMT; ++mt) {
+                if (mt < MT) {
+                  mma_bf16(acc[mt][nt], ah[mt][0], b0, b1);
+                  mma_bf16(acc[mt][nt], al[mt][0], b0, b1);
+                  mma_bf16(acc[mt][nt], ah[mt][1], b2, b3);
+                  mma_bf16(acc[mt][nt], al[mt][1], b2, b3);
                 }
               }
             }
@@ -655,60 +676,58 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_engine(const __grid_constant
         if (lane == 0) mbar_arrive(&empty_bar[s]);
         ++ctr;
       }
-      // partial tiles of the 8 warps -> shared memory (the activation region is free here), added
-      // in warp order
-      float* red = xhat;  // [warp][at][nt][e][lane]
+      // per m-tile: the 8 warps' partial tiles -> shared memory, added in warp order
 #pragma unroll
-      for (int at = 0; at < 2; ++at)
+      for (int mt = 0; mt < kMaxMT; ++mt) {
+        if (mt < MT) {
 #pragma unroll
-        for (int nt = 0; nt < kMaxNT; ++nt)
+          for (int nt = 0; nt < 8; ++nt)
 #pragma unroll
-          for (int e = 0; e < 4; ++e)
-            if (nt < NT) red[(((warp * 2 + at) * kMaxNT + nt) * 4 + e) * 32 + lane] = acc[at][nt][e];
-      named_bar(1, NCT);
-      auto tot = [&](int at, int m, int v) {
-        const int nt = v / 8, nn = v % 8;
-        const int ln = (m % 8) * 4 + nn / 2;
-        const int e = (m >= 8 ? 2 : 0) + (nn & 1);
-        float sum = 0.f;
+            for (int e = 0; e < 4; ++e) red[((warp * 8 + nt) * 4 + e) * 32 + lane] = acc[mt][nt][e];
+          named_bar(1, NCT);
+          auto tot = [&](int slot, int vv) {
+            const int nt = slot >> 3, n = slot & 7;
+            const int ln = (vv & 7) * 4 + (n >> 1);
+            const int e = (vv >= 8 ? 2 : 0) + (n & 1);
+            float sum = 0.f;
 #pragma unroll
-        for (int w8 = 0; w8 < kNCW; ++w8) sum += red[(((w8 * 2 + at) * kMaxNT + nt) * 4 + e) * 32 + ln];
-        return sum;
-      };
-      if (!failed) {
-        if (G.nw == 2) {  // 16 rows: gate in A tile 0, up in A tile 1
-          for (int idx = tid; idx < 16 * nv; idx += NCT) {
-            const int m = idx / nv, v = idx % nv;
-            if (m < tr) epilogue<WT>(p, G, v, r + m, tot(0, m, v), tot(1, m, v), false, loc);
+            for (int w8 = 0; w8 < kNCW; ++w8) sum += red[((w8 * 8 + nt) * 4 + e) * 32 + ln];
+            return sum;
+          };
+          if (!failed) {
+            if (G.nw == 2 || (G.epi == EPI_QKV && r < G.seg2)) {  // gate/up, or rotary pairs
+              const bool pair = G.nw != 2;
+              for (int idx = tid; idx < 32 * 16; idx += NCT) {
+                const int m = idx >> 4, vv = idx & 15, v = mt * 16 + vv;
+                if (v < nv && m < tr)
+                  epilogue<WT>(p, G, v, pair ? phys_row(G, r + m, hd) : r + m, tot(m, vv), tot(m + 32, vv),
+                               pair, loc);
+              }
+            } else {
+              for (int idx = tid; idx < 64 * 16; idx += NCT) {
+                const int m = idx >> 4, vv = idx & 15, v = mt * 16 + vv;
+                if (v < nv && m < tr) epilogue<WT>(p, G, v, r + m, tot(m, vv), 0.f, false, loc);
+              }
+            }
           }
-        } else if (G.epi == EPI_QKV && r < G.seg2) {  // 16 rotary pairs (slot m, slot m+16)
-          for (int idx = tid; idx < 16 * nv; idx += NCT) {
-            const int m = idx / nv, v = idx % nv;
-            epilogue<WT>(p, G, v, phys_row(G, r + m, p.D.hd), tot(0, m, v), tot(1, m, v), true, loc);
-          }
-        } else {  // 32 rows in two A tiles
-          for (int idx = tid; idx < 32 * nv; idx += NCT) {
-            const int m = idx / nv, v = idx % nv;
-            if (m < tr) epilogue<WT>(p, G, v, r + m, tot(m / 16, m % 16, v), 0.f, false, loc);
-          }
+          named_bar(1, NCT);  // `red` is rewritten next
         }
       }
-      named_bar(1, NCT);  // `red` is rewritten by the next tile
     }
     r += tr;
     if (r >= last) { ++g; r = 0; }
   }
-  // head: per-CTA top-2 of each kind, warps merged in order
+  // head: per-CTA top-2 of each kind (the order of the merge does not change a top-2)
   bool head = false;
   for (int i = 0; i < ng; ++i) head |= gg[i].epi == EPI_TOP2;
   if (head || (ng == 0 && p.nparts > 0 && p.part[0].op == OP_HEAD)) {
-    if (lane == 0) { hred[warp][0] = loc[0]; hred[warp][1] = loc[1]; }
+    if (lane < 8) { hred[warp * 8 + lane][0] = loc[0]; hred[warp * 8 + lane][1] = loc[1]; }
     named_bar(1, NCT);
     if (tid == 0) {
       float* hp = p.B.head_part + (size_t)blockIdx.x * 8;
       for (int k = 0; k < 2; ++k) {
         Top2 m = hred[0][k];
-        for (int i = 1; i < kNCW; ++i) top2_merge(m, hred[i][k]);
+        for (int i = 1; i < kNCW * 8; ++i) top2_merge(m, hred[i][k]);
         hp[k * 4 + 0] = m.v1; hp[k * 4 + 1] = __int_as_float(m.i1);
         hp[k * 4 + 2] = m.v2; hp[k * 4 + 3] = __int_as_float(m.i2);
       }
@@ -780,6 +799,29 @@ cudaError_t launch_gemv_explicit(const GemvExplicit& ge, int dtype, float eps, c
   p.has_mma = 0;
   p.D.dtype = dtype; p.D.eps = eps;
   return dtype == SPD_DTYPE_BF16 ? launch_engine<__nv_bfloat16>(p, false, s) : launch_engine<float>(p, false, s);
+}
+
+cudaError_t gemv_encode_map(CUtensorMap* out, const void* W, int rows, int cols, int dtype) {
+  static PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
+  if (!encode) {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+    const cudaError_t e =
+        cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q);
+    if (e != cudaSuccess) return e;
+    if (q != cudaDriverEntryPointSuccess || !fn) return cudaErrorNotSupported;
+    encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  }
+  const int esz = dtype == SPD_DTYPE_BF16 ? 2 : 4;
+  const cuuint64_t gdim[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+  const cuuint64_t gstride[1] = {(cuuint64_t)cols * esz};
+  const cuuint32_t box[2] = {(cuuint32_t)(128 / esz), (cuuint32_t)kBoxRows};
+  const cuuint32_t estride[2] = {1, 1};
+  const CUresult r = encode(out, dtype == SPD_DTYPE_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32,
+                            2, const_cast<void*>(W), gdim, gstride, box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
 }  // namespace spd

@@ -11,6 +11,7 @@
 //   rope tables cos/sin [max_seq][hd/2] fp32 (angles formed in fp64)
 //   control block (DevState), token sequence, verification trace, draft override arrays.
 #pragma once
+#include <cuda.h>  // CUtensorMap (the type only; maps are encoded through the runtime's entry point)
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
 #include <stdint.h>
@@ -22,7 +23,6 @@ namespace spd {
 constexpr int kMaxGroups = 72;      // one launch: n_stages target groups + n_stages+1 draft rows (+ splits)
 constexpr int kMaxAttnRows = 32;    // query rows of the stand-alone attention operators
 constexpr int kMaxExplicit = 34;    // groups of the stand-alone grouped GEMV
-constexpr int kGemvMaxCols = 16384; // input columns of a single-vector GEMV group (staged in smem)
 constexpr int kMaxTiles = 64;       // attention query tiles per launch
 constexpr int kPrefillBlock = 32;   // prompt rows per prefill pass
 constexpr int kAttnChunk = 128;     // keys per attention split (fixed: split count depends on length only)
@@ -46,6 +46,7 @@ enum StateFlags { SF_TARGET_ONLY = 1 };
 
 struct LayerW {
   const void *attn_norm, *wq, *wk, *wv, *wo, *ffn_norm, *wg, *wu, *wd;
+  const CUtensorMap *tq, *tk, *tv, *to, *tg, *tu, *td;  // tensor maps of the seven matrices
 };
 
 struct Dims {
@@ -78,6 +79,9 @@ struct Bufs {
   const float* final_norm;
   const float* pdm_norm;
   const void* fc[SPD_MAX_ANCHORS];
+  const CUtensorMap* tm_fc[SPD_MAX_ANCHORS];
+  const CUtensorMap* tm_lm;
+  const CUtensorMap* tm_pdm;
 };
 
 // How the rows of one launch are formed from the control block.
@@ -273,6 +277,7 @@ enum KernelKind { KK_QKV = 0, KK_ROPE = 1, KK_ATTN = 2, KK_O = 3, KK_GATEUP = 4,
                   KK_FC = 6, KK_HEAD = 7, KK_CTRL = 8 };
 
 struct GemvExplicit {  // stand-alone grouped GEMV
+  const CUtensorMap* tm[kMaxExplicit];  // device copies of the weights' tensor maps
   const void* W[kMaxExplicit];
   const float* x[kMaxExplicit];
   float* y[kMaxExplicit];
@@ -305,6 +310,9 @@ cudaError_t launch_attn(const Dims& D, const Bufs& B, const Launch& lc, const La
 size_t attn_smem_bytes(const Dims& D, bool multi);
 size_t attn_part_floats(int rows, int hq, int hd, int max_seq);
 cudaError_t gemv_setup_attributes();
+// Encodes the tensor map the GEMV engine streams a row-major [rows, cols] weight matrix with
+// (boxes of 128 bytes x 32 rows, 128-byte swizzle).  Host call; returns a CUDA error code.
+cudaError_t gemv_encode_map(CUtensorMap* out, const void* W, int rows, int cols, int dtype);
 int gemv_head_grid(int dtype);
 int num_sms();
 cudaError_t attn_setup_attributes(size_t max_smem);

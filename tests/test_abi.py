@@ -34,7 +34,7 @@ def test_header_declares_the_survey_boundary():
 
 def _cfg(**kw):
     from speculative_pipeline_decoding_gb300.binding import Config
-    base = dict(n_layers=8, d_model=64, n_heads=4, n_kv_heads=2, head_dim=16, d_ffn=128, vocab=100,
+    base = dict(n_layers=8, d_model=256, n_heads=4, n_kv_heads=2, head_dim=64, d_ffn=512, vocab=100,
                 n_stages=2, pdm_layers=1, anchors=(0, 2, 4, 6, 8), dtype="f32", max_seq=64)
     base.update(kw)
     return Config(**base)
