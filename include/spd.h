@@ -178,7 +178,8 @@ int spd_rollback(spd_handle* h, int32_t keep_len, int32_t reseed_token);
 int spd_set_draft_override(spd_handle* h, int32_t first_pos, int32_t count,
                            const int32_t* ref_tokens, const uint8_t* modes);
 
-/* Execution options (bit flags), default SPD_OPT_GRAPHS | SPD_OPT_PDL. */
+/* Execution options (bit flags), default SPD_OPT_GRAPHS | SPD_OPT_COSCHED | SPD_OPT_PDL |
+ * SPD_OPT_STEP. */
 #define SPD_OPT_GRAPHS       1  /* replay captured CUDA graphs instead of eager launches      */
 #define SPD_OPT_COSCHED      2  /* draft layer s rides in the GEMV launches of target sub-step s
                                    (SPD summary 方法步骤详情 steps 1 and 4 in one pass over HBM);
@@ -190,6 +191,9 @@ int spd_set_draft_override(spd_handle* h, int32_t first_pos, int32_t count,
 #define SPD_OPT_DEBUG_LOGITS 8  /* keep full fp32 logits of the last head launch for dumps     */
 #define SPD_OPT_PDL         16  /* programmatic dependent launch: a kernel may start (and stream
                                    its weights) while its predecessor drains                   */
+#define SPD_OPT_STEP        32  /* one persistent cooperative kernel per cycle / AR step (one CTA
+                                   per SM, phases separated by grid barriers, weights streamed
+                                   across phase boundaries); off: one launch per operator      */
 int spd_set_options(spd_handle* h, int32_t flags);
 
 /* Copy internal state to a HOST buffer of `bytes` bytes (synchronising).  Layouts:
@@ -210,9 +214,10 @@ enum { SPD_DUMP_STATE = 0, SPD_DUMP_RESID = 1, SPD_DUMP_ANCHORS = 2, SPD_DUMP_PD
 size_t spd_dump_size(const spd_handle* h, int32_t what);
 int spd_debug_dump(spd_handle* h, int32_t what, void* host_dst, size_t bytes);
 
-/* Per-kernel-kind device time of eager launches, for roofline reporting.  When enabled, graphs
- * are bypassed and each launch is bracketed by CUDA events on its own stream; spd_kernel_times
- * returns, per kind, launches and summed milliseconds, and resets them.
+/* Per-kernel-kind device time, for roofline reporting.  When enabled, graphs are bypassed; each
+ * per-operator launch is bracketed by CUDA events on its own stream, and the step kernel records
+ * the time of each of its phases (grid barrier to grid barrier, on CTA 0).  spd_kernel_times
+ * returns, per kind, launches (or phase executions) and summed milliseconds, and resets them.
  * Kinds 0..8 are target-stack launches (stage-diagonal, AR or prefill): 0 qkv (with RoPE and
  * the KV append), 1 unused (kept for layout stability), 2 attention, 3 o-proj, 4 gate/up, 5 down,
  * 6 anchor FC, 7 vocab head, 8 control; kinds 9..17 are the same operators on the draft-module

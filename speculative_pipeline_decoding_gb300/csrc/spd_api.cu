@@ -44,7 +44,17 @@ struct spd_handle {
   std::vector<void*> allocs;
   Act act_t{}, act_p{}, act_head{}, act_pf{}, act_pfp{};
   float* p_z = nullptr;
-  int opts = SPD_OPT_GRAPHS | SPD_OPT_PDL;
+  int opts = SPD_OPT_GRAPHS | SPD_OPT_PDL | SPD_OPT_COSCHED | SPD_OPT_STEP;
+  // persistent step kernel: programs of phases for one cycle and one AR step
+  size_t step_smem = 0;               // 0: the step kernel does not fit this model
+  Phase* d_prog_cycle = nullptr;
+  Phase* d_prog_ar = nullptr;
+  int n_prog_cycle = 0, n_prog_ar = 0, cap_prog_cycle = 0, cap_prog_ar = 0;
+  std::vector<int> kinds_cycle, kinds_ar;
+  unsigned* d_bar = nullptr;          // grid barrier words
+  unsigned long long* d_ns_cycle = nullptr;  // per-phase accumulated time while timing
+  unsigned long long* d_ns_ar = nullptr;
+  int64_t timed_cycles = 0, timed_ar = 0;
   bool st_dirty = true;         // the last kernel enqueued may have written the control block
   bool prefilled = false;
   int P = 0;
@@ -166,31 +176,119 @@ int enqueue_layer(spd_handle* h, const Launch& lc, const Launch* extra, cudaStre
   return run_gemv(h, OP_DOWN, lc, extra, s);
 }
 
-Launch mk(int kind, int stack, int sub, const Act& act, int pos0 = 0, int cnt = 0) {
+Launch mk(int kind, int stack, int sub, const Act& act, int pos0, int cnt) {
   Launch lc;
   memset(&lc, 0, sizeof(lc));
   lc.kind = kind; lc.stack = stack; lc.sub = sub; lc.pos0 = pos0; lc.cnt = cnt; lc.act = act;
   return lc;
 }
 
+bool use_step(const spd_handle* h) { return (h->opts & SPD_OPT_STEP) && h->step_smem > 0; }
+
+Phase ph_gemv(int op, int kind, const Launch& a, const Launch* b) {
+  Phase P;
+  memset(&P, 0, sizeof(P));
+  P.type = PH_GEMV; P.kind = kind; P.nparts = b ? 2 : 1;
+  P.part[0].op = op; P.part[0].lc = a;
+  if (b) { P.part[1].op = op; P.part[1].lc = *b; }
+  return P;
+}
+
+Phase ph_attn(int kind, const Launch& a, const Launch* b) {
+  Phase P = ph_gemv(0, kind, a, b);
+  P.type = PH_ATTN;
+  return P;
+}
+
+// The five phases of one decoder layer (or of one co-scheduled stage-diagonal sub-step).
+void layer_phases(std::vector<Phase>& v, const Launch& lc, const Launch* extra) {
+  const int off = lc.stack == 1 ? 9 : 0;
+  v.push_back(ph_gemv(OP_QKV, KK_QKV + off, lc, extra));
+  v.push_back(ph_attn(KK_ATTN + off, lc, extra));
+  v.push_back(ph_gemv(OP_O, KK_O + off, lc, extra));
+  v.push_back(ph_gemv(OP_GATEUP, KK_GATEUP + off, lc, extra));
+  v.push_back(ph_gemv(OP_DOWN, KK_DOWN + off, lc, extra));
+}
+
+Launch mk(int kind, int stack, int sub, const Act& act, int pos0, int cnt);
+
+// Builds the cycle and AR programs for the current options and copies them to the device.
+int build_programs(spd_handle* h) {
+  if (h->step_smem == 0) return SPD_OK;
+  const Dims& D = h->D;
+  std::vector<Phase> cyc, ar;
+  const bool pdm = !(h->opts & SPD_OPT_TARGET_ONLY);
+  const bool cos = pdm && (h->opts & SPD_OPT_COSCHED);
+  if (pdm) {
+    cyc.push_back(ph_gemv(OP_FC, KK_FC + 9, mk(LK_PDMROWS, 1, 0, h->act_p, 0, 0), nullptr));
+    if (!cos)
+      for (int lp = 0; lp < D.Ls; ++lp) layer_phases(cyc, mk(LK_PDMROWS, 1, lp, h->act_p, 0, 0), nullptr);
+  }
+  for (int s = 0; s < D.S; ++s) {
+    const Launch lt = mk(LK_DIAG, 0, s, h->act_t, 0, 0);
+    const Launch lp = mk(LK_PDMROWS, 1, s, h->act_p, 0, 0);
+    layer_phases(cyc, lt, (cos && s < D.Ls) ? &lp : nullptr);
+  }
+  cyc.push_back(ph_gemv(OP_HEAD, KK_HEAD, mk(LK_DIAG, 0, 0, h->act_head, 0, 0), nullptr));
+  {
+    Phase c;
+    memset(&c, 0, sizeof(c));
+    c.type = PH_CTRL_CYCLE; c.kind = KK_CTRL;
+    cyc.push_back(c);
+  }
+  for (int l = 0; l < D.L; ++l) layer_phases(ar, mk(LK_AR, 0, l, h->act_t, 0, 0), nullptr);
+  ar.push_back(ph_gemv(OP_HEAD, KK_HEAD, mk(LK_AR, 0, 0, h->act_head, 0, 0), nullptr));
+  {
+    Phase c;
+    memset(&c, 0, sizeof(c));
+    c.type = PH_CTRL_AR; c.kind = KK_CTRL;
+    ar.push_back(c);
+  }
+  if ((int)cyc.size() > h->cap_prog_cycle || (int)ar.size() > h->cap_prog_ar)
+    return fail(h, SPD_ESTATE, "step program larger than its buffer");
+  SPD_CUDA(h, cudaMemcpy(h->d_prog_cycle, cyc.data(), sizeof(Phase) * cyc.size(), cudaMemcpyHostToDevice));
+  SPD_CUDA(h, cudaMemcpy(h->d_prog_ar, ar.data(), sizeof(Phase) * ar.size(), cudaMemcpyHostToDevice));
+  h->n_prog_cycle = (int)cyc.size();
+  h->n_prog_ar = (int)ar.size();
+  h->kinds_cycle.clear();
+  h->kinds_ar.clear();
+  for (const Phase& P : cyc) h->kinds_cycle.push_back(P.kind);
+  for (const Phase& P : ar) h->kinds_ar.push_back(P.kind);
+  return SPD_OK;
+}
+
+int enqueue_step(spd_handle* h, bool cycle) {
+  h->n_launch += 1;
+  unsigned long long* ns = nullptr;
+  if (h->timing) {
+    ns = cycle ? h->d_ns_cycle : h->d_ns_ar;
+    (cycle ? h->timed_cycles : h->timed_ar) += 1;
+  }
+  SPD_CUDA(h, launch_step(h->D, h->B, h->LC, cycle ? h->d_prog_cycle : h->d_prog_ar,
+                          cycle ? h->n_prog_cycle : h->n_prog_ar, h->d_bar, ns, h->step_smem, h->s_main));
+  h->st_dirty = true;
+  return SPD_OK;
+}
+
 int enqueue_cycle(spd_handle* h) {
+  if (use_step(h)) return enqueue_step(h, true);
   int rc;
   const bool pdm = !(h->opts & SPD_OPT_TARGET_ONLY);
   const bool cos = pdm && (h->opts & SPD_OPT_COSCHED);
   cudaStream_t sm = h->s_main;
   h->st_dirty = true;  // the previous cycle's control kernel (or the host) wrote the control block
   if (pdm) {
-    if ((rc = run_gemv(h, OP_FC, mk(LK_PDMROWS, 1, 0, h->act_p), nullptr, sm))) return rc;
+    if ((rc = run_gemv(h, OP_FC, mk(LK_PDMROWS, 1, 0, h->act_p, 0, 0), nullptr, sm))) return rc;
     if (!cos)  // serialised draft module: its Ls layers before the target step
       for (int lp = 0; lp < h->D.Ls; ++lp)
-        if ((rc = enqueue_layer(h, mk(LK_PDMROWS, 1, lp, h->act_p), nullptr, sm))) return rc;
+        if ((rc = enqueue_layer(h, mk(LK_PDMROWS, 1, lp, h->act_p, 0, 0), nullptr, sm))) return rc;
   }
   for (int s = 0; s < h->D.S; ++s) {
-    const Launch lt = mk(LK_DIAG, 0, s, h->act_t);
-    const Launch lp = mk(LK_PDMROWS, 1, s, h->act_p);
+    const Launch lt = mk(LK_DIAG, 0, s, h->act_t, 0, 0);
+    const Launch lp = mk(LK_PDMROWS, 1, s, h->act_p, 0, 0);
     if ((rc = enqueue_layer(h, lt, (cos && s < h->D.Ls) ? &lp : nullptr, sm))) return rc;
   }
-  if ((rc = run_gemv(h, OP_HEAD, mk(LK_DIAG, 0, 0, h->act_head), nullptr, sm))) return rc;
+  if ((rc = run_gemv(h, OP_HEAD, mk(LK_DIAG, 0, 0, h->act_head, 0, 0), nullptr, sm))) return rc;
   Timed tm(h, KK_CTRL, sm);
   SPD_CUDA(h, launch_control_cycle(h->D, h->B, sm));
   h->st_dirty = true;
@@ -198,12 +296,13 @@ int enqueue_cycle(spd_handle* h) {
 }
 
 int enqueue_ar_step(spd_handle* h) {
+  if (use_step(h)) return enqueue_step(h, false);
   int rc;
   cudaStream_t sm = h->s_main;
   h->st_dirty = true;
   for (int l = 0; l < h->D.L; ++l)
-    if ((rc = enqueue_layer(h, mk(LK_AR, 0, l, h->act_t), nullptr, sm))) return rc;
-  if ((rc = run_gemv(h, OP_HEAD, mk(LK_AR, 0, 0, h->act_head), nullptr, sm))) return rc;
+    if ((rc = enqueue_layer(h, mk(LK_AR, 0, l, h->act_t, 0, 0), nullptr, sm))) return rc;
+  if ((rc = run_gemv(h, OP_HEAD, mk(LK_AR, 0, 0, h->act_head, 0, 0), nullptr, sm))) return rc;
   Timed tm(h, KK_CTRL, sm);
   SPD_CUDA(h, launch_control_ar(h->D, h->B, sm));
   h->st_dirty = true;
@@ -512,7 +611,11 @@ int spd_create(const spd_config* cfg, const spd_weights* w, void* cuda_stream, s
   ALLOC(T.attn, float, (size_t)n * hqd);
   ALLOC(T.u, float, (size_t)n * f);
   const int part_rows_t = n > PB ? n : PB;
-  ALLOC(T.part, float, attn_part_floats(part_rows_t, c.n_heads, c.head_dim, c.max_seq));
+  {  // prefill blocks use 128-key chunks, the step kernel 64-key chunks
+    const size_t a1 = attn_part_floats(part_rows_t, c.n_heads, c.head_dim, c.max_seq, kAttnChunk);
+    const size_t a2 = attn_part_floats(n, c.n_heads, c.head_dim, c.max_seq, kStepChunk);
+    ALLOC(T.part, float, a1 > a2 ? a1 : a2);
+  }
   ALLOC(T.tick, int, (size_t)kMaxTiles * c.n_kv_heads);
   // draft rows
   Act& Pm = h->act_p;
@@ -521,7 +624,7 @@ int spd_create(const spd_config* cfg, const spd_weights* w, void* cuda_stream, s
   ALLOC(Pm.qkv, float, (size_t)(n + 2) * qkvr);
   ALLOC(Pm.attn, float, (size_t)(n + 2) * hqd);
   ALLOC(Pm.u, float, (size_t)(n + 2) * f);
-  ALLOC(Pm.part, float, attn_part_floats(n + 2, c.n_heads, c.head_dim, c.max_seq));
+  ALLOC(Pm.part, float, attn_part_floats(n + 2, c.n_heads, c.head_dim, c.max_seq, kStepChunk));
   ALLOC(Pm.tick, int, (size_t)kMaxTiles * c.n_kv_heads);
   // head: target rows in the ring, draft row z in act.qkv
   h->act_head = T;
@@ -540,7 +643,6 @@ int spd_create(const spd_config* cfg, const spd_weights* w, void* cuda_stream, s
   FP = F;
   ALLOC(FP.resid, float, (size_t)PB * d);
   FP.anch = F.anch;  // anchor source of the prefix rows for the draft FC
-#undef ALLOC
   e = cudaMallocHost(reinterpret_cast<void**>(&h->host_state), sizeof(DevState));
   if (e != cudaSuccess) { spd_destroy(h); return fail(nullptr, SPD_ENOMEM, "cudaMallocHost failed"); }
   memset(h->host_state, 0, sizeof(DevState));
@@ -557,6 +659,26 @@ int spd_create(const spd_config* cfg, const spd_weights* w, void* cuda_stream, s
   const size_t asm_ = attn_smem_bytes(D, true) > attn_smem_bytes(D, false) ? attn_smem_bytes(D, true)
                                                                            : attn_smem_bytes(D, false);
   if (e == cudaSuccess) e = attn_setup_attributes(asm_);
+  // persistent step kernel: programs, grid barrier, per-phase timers
+  h->step_smem = step_smem_bytes(D);
+  if (e == cudaSuccess && h->step_smem) {
+    e = step_setup_attributes(h->step_smem);
+    if (e != cudaSuccess) {  // the per-operator path remains
+      cudaGetLastError();
+      e = cudaSuccess;
+      h->step_smem = 0;
+    }
+  }
+  if (e == cudaSuccess && h->step_smem) {
+    h->cap_prog_cycle = 1 + 5 * (D.S + D.Ls) + 2;
+    h->cap_prog_ar = 5 * D.L + 2;
+    ALLOC(h->d_prog_cycle, Phase, h->cap_prog_cycle);
+    ALLOC(h->d_prog_ar, Phase, h->cap_prog_ar);
+    ALLOC(h->d_bar, unsigned, 2);
+    ALLOC(h->d_ns_cycle, unsigned long long, h->cap_prog_cycle);
+    ALLOC(h->d_ns_ar, unsigned long long, h->cap_prog_ar);
+  }
+#undef ALLOC
   if (e == cudaSuccess) {
     h->LC.sms = num_sms();
     h->LC.gemv_grid = 0;
@@ -570,6 +692,12 @@ int spd_create(const spd_config* cfg, const spd_weights* w, void* cuda_stream, s
     std::string msg = cudaGetErrorString(e);
     spd_destroy(h);
     return fail(nullptr, SPD_ECUDA, "setup: %s", msg.c_str());
+  }
+  int rcp;
+  if ((rcp = build_programs(h))) {
+    const std::string msg = h->err;
+    spd_destroy(h);
+    return fail(nullptr, rcp, "%s", msg.c_str());
   }
   *out = h;
   return SPD_OK;
@@ -587,6 +715,7 @@ int spd_prefill(spd_handle* h, const int32_t* tokens, int32_t P, int32_t* first_
   SPD_CUDA(h, cudaMemcpyAsync(h->B.seq + 1, tokens, sizeof(int32_t) * P, cudaMemcpyHostToDevice, s));
   SPD_CUDA(h, cudaMemsetAsync(h->B.ovr_mode, 0, D.max_seq + 2, s));
   SPD_CUDA(h, cudaMemsetAsync(h->B.st, 0, sizeof(DevState), s));
+  if (h->d_bar) SPD_CUDA(h, cudaMemsetAsync(h->d_bar, 0, 2 * sizeof(unsigned), s));
   const int flags = (h->opts & SPD_OPT_TARGET_ONLY) ? SF_TARGET_ONLY : 0;
   h->host_state->flags = flags;
   SPD_CUDA(h, cudaMemcpyAsync(&h->B.st->flags, &h->host_state->flags, sizeof(int),
@@ -653,6 +782,7 @@ int spd_rollback(spd_handle* h, int32_t keep_len, int32_t reseed_token) {
   if (reseed_token < 0 || reseed_token >= h->D.V) return fail(h, SPD_EINVAL, "reseed token out of range");
   if (keep_len + h->D.n + 2 > h->D.max_seq) return fail(h, SPD_EINVAL, "keep_len too large");
   SPD_CUDA(h, cudaMemsetAsync(&h->B.st->err, 0, sizeof(int), h->s_main));
+  if (h->d_bar) SPD_CUDA(h, cudaMemsetAsync(h->d_bar, 0, 2 * sizeof(unsigned), h->s_main));
   SPD_CUDA(h, launch_rollback(h->D, h->B, keep_len, reseed_token, h->s_main));
   return SPD_OK;
 }
@@ -677,12 +807,16 @@ int spd_set_draft_override(spd_handle* h, int32_t first_pos, int32_t count, cons
 
 int spd_set_options(spd_handle* h, int32_t flags) {
   if (!h) return SPD_EINVAL;
-  if (flags & ~(SPD_OPT_GRAPHS | SPD_OPT_COSCHED | SPD_OPT_TARGET_ONLY | SPD_OPT_DEBUG_LOGITS | SPD_OPT_PDL))
+  if (flags & ~(SPD_OPT_GRAPHS | SPD_OPT_COSCHED | SPD_OPT_TARGET_ONLY | SPD_OPT_DEBUG_LOGITS | SPD_OPT_PDL |
+                SPD_OPT_STEP))
     return fail(h, SPD_EINVAL, "unknown option bits");
   SPD_CUDA(h, cudaStreamSynchronize(h->s_main));
-  if ((flags ^ h->opts) & (SPD_OPT_COSCHED | SPD_OPT_TARGET_ONLY | SPD_OPT_DEBUG_LOGITS | SPD_OPT_PDL))
+  if ((flags ^ h->opts) & (SPD_OPT_COSCHED | SPD_OPT_TARGET_ONLY | SPD_OPT_DEBUG_LOGITS | SPD_OPT_PDL |
+                           SPD_OPT_STEP))
     drop_graphs(h);
   h->opts = flags;
+  int rcp;
+  if ((rcp = build_programs(h))) return rcp;
   h->LC.debug_logits = (flags & SPD_OPT_DEBUG_LOGITS) ? 1 : 0;
   h->host_state->flags = (flags & SPD_OPT_TARGET_ONLY) ? SF_TARGET_ONLY : 0;
   SPD_CUDA(h, cudaMemcpyAsync(&h->B.st->flags, &h->host_state->flags, sizeof(int),
@@ -746,6 +880,23 @@ int spd_kernel_times(spd_handle* h, int64_t* launches, double* ms, int32_t n_kin
   }
   h->recs.clear();
   h->pool_used = 0;
+  // step kernel: per-phase times (barrier to barrier on CTA 0) charged to the phases' kinds
+  auto take = [&](unsigned long long* dns, const std::vector<int>& kinds, int64_t runs) -> int {
+    if (!dns || kinds.empty()) return SPD_OK;
+    std::vector<unsigned long long> ns(kinds.size());
+    SPD_CUDA(h, cudaMemcpy(ns.data(), dns, sizeof(unsigned long long) * ns.size(), cudaMemcpyDeviceToHost));
+    SPD_CUDA(h, cudaMemset(dns, 0, sizeof(unsigned long long) * ns.size()));
+    if (!runs) return SPD_OK;
+    for (size_t i = 0; i < kinds.size(); ++i) {
+      h->launches[kinds[i]] += runs;
+      h->ms[kinds[i]] += ns[i] * 1e-6;
+    }
+    return SPD_OK;
+  };
+  int rc;
+  if ((rc = take(h->d_ns_cycle, h->kinds_cycle, h->timed_cycles))) return rc;
+  if ((rc = take(h->d_ns_ar, h->kinds_ar, h->timed_ar))) return rc;
+  h->timed_cycles = h->timed_ar = 0;
   for (int k = 0; k < n_kinds && k < SPD_NUM_KINDS; ++k) {
     if (launches) launches[k] = h->launches[k];
     if (ms) ms[k] = h->ms[k];

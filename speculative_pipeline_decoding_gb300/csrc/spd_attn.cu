@@ -9,7 +9,10 @@
 // (tile, kv head) to finish (atomic ticket, no spinning) merges the partials of each query in chunk
 // order.  The number of chunks depends only on the query position, so a token's result does not
 // depend on its batch.
-#include "spd_internal.cuh"
+// Stand-alone launches of decode attention (device code in spd_attn.cuh): prefill blocks, the
+// per-operator path used when the step kernel is not, and the stand-alone operators.  Chunks of
+// 128 keys; every CTA of the grid takes items blockIdx.x, blockIdx.x + gridDim.x, ...
+#include "spd_attn.cuh"
 
 namespace spd {
 
@@ -23,74 +26,19 @@ struct AttnParams {
   int qh_max;
 };
 
-struct Tile {
-  int layer, nq, pos0, vid0, nch, rec_off, item_off;
-  const unsigned char* kc;  // base of this layer's K cache (head 0, position 1)
-  const unsigned char* vc;
-};
-
-__device__ int build_tiles(const AttnParams& p, Tile* tiles, int* n_items) {
-  const Dims& D = p.D;
-  const Launch& lc = p.lc;
-  DevState* st = p.B.st;
-  RowGroup rg[kMaxGroups];
-  int nr;
-  if (lc.kind == LK_EXPLICIT) {
-    nr = lc.cnt;
-    for (int r = 0; r < nr; ++r) {
-      rg[r].layer = 0; rg[r].nv = 1; rg[r].pos0 = lc.act.pos_arr[r]; rg[r].vid0 = r; rg[r].rrow0 = 0;
-    }
-  } else {
-    nr = build_rows(lc, D, st, rg);
-  }
-  const int esz = D.dtype == SPD_DTYPE_BF16 ? 2 : 4;
-  const size_t layer_elems = (size_t)D.hkv * D.max_seq * D.hd;
-  int nt = 0, rec = 0, items = 0;
-  for (int i = 0; i < nr; ++i) {
-    for (int r0 = 0; r0 < rg[i].nv; r0 += p.qt) {
-      if (nt >= kMaxTiles) { set_err(st, ERR_BOUNDS, 400); *n_items = 0; return 0; }
-      Tile& T = tiles[nt++];
-      T.layer = rg[i].layer;
-      T.nq = min(p.qt, rg[i].nv - r0);
-      T.pos0 = rg[i].pos0 + r0;
-      T.vid0 = rg[i].vid0 + r0;
-      const int pos_last = T.pos0 + T.nq - 1;
-      T.nch = (pos_last + kAttnChunk - 1) / kAttnChunk;
-      T.rec_off = rec;
-      T.item_off = items;
-      rec += D.hkv * T.nch * T.nq * D.gq;
-      items += D.hkv * T.nch;
-      const void* kb;
-      const void* vb;
-      if (lc.kind == LK_EXPLICIT) { kb = lc.act.kc; vb = lc.act.vc; }
-      else if (lc.stack == 0) { kb = p.B.kc; vb = p.B.vc; }
-      else { kb = p.B.pkc; vb = p.B.pvc; }
-      T.kc = (const unsigned char*)kb + (size_t)T.layer * layer_elems * esz;
-      T.vc = (const unsigned char*)vb + (size_t)T.layer * layer_elems * esz;
-    }
-  }
-  *n_items = items;
-  return nt;
-}
-
 template <typename WT>
-__global__ void __launch_bounds__(kAttnThreads)
-attn_kernel(const __grid_constant__ AttnParams p) {
+__global__ void __launch_bounds__(kAttnThreads) attn_kernel(const __grid_constant__ AttnParams p) {
   extern __shared__ __align__(128) unsigned char sm[];
-  __shared__ Tile tiles[kMaxTiles];
+  __shared__ att::Tile tiles[kMaxTiles];
   __shared__ int s_nt, s_items, s_last, s_fail;
   __shared__ __align__(8) uint64_t kv_bar;
-  constexpr int ESZ = sizeof(WT);
-  const Dims& D = p.D;
-  const int hd = D.hd, GQ = D.gq, CK = kAttnChunk;
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   DevState* st = p.B.st;
-
-  if (tid == 0) {
+  if (threadIdx.x == 0) {
     const bool skip = p.lc.kind != LK_EXPLICIT && (st->done || st->err);
     int items = 0;
-    s_nt = skip ? 0 : build_tiles(p, tiles, &items);
-    s_items = s_nt ? items : 0;
+    const int nt = skip ? 0 : att::add_tiles(p.D, p.B, p.lc, p.qt, kAttnChunk, tiles, 0, &items);
+    s_nt = nt > 0 ? nt : 0;
+    s_items = nt > 0 ? items : 0;
     s_fail = 0;
     mbar_init(&kv_bar, 1);
     fence_mbar_init();
@@ -98,168 +46,20 @@ attn_kernel(const __grid_constant__ AttnParams p) {
   __syncthreads();
   pdl_wait();  // q and the K/V appended by the previous kernel are visible from here on
   pdl_trigger();
-  const int n_items = s_items;
-  if (n_items == 0) return;
-
-  WT* ks = reinterpret_cast<WT*>(sm);
-  WT* vs = reinterpret_cast<WT*>(sm + (size_t)CK * hd * ESZ);
-  float* qs = reinterpret_cast<float*>(sm + (size_t)2 * CK * hd * ESZ);
-  float* sc = qs + (size_t)p.qh_max * hd;
-  float* m_s = sc + (size_t)p.qh_max * CK;
-  float* l_s = m_s + p.qh_max;
-  const float scale = 1.0f / sqrtf((float)hd);
-  const int qkv_rows = D.qkv_rows;
-  const int hqd = D.hq * hd;
-  float* part = p.lc.act.part;
-  int* tick = p.lc.act.tick;
-  const int LPK = hd / 16;  // lanes per key
-  const int KPW = 32 / LPK;
+  if (s_items == 0) return;
   uint32_t phase = 0;
-
-  for (int item = blockIdx.x; item < n_items; item += gridDim.x) {
-    int T = 0;
-    while (T + 1 < s_nt && tiles[T + 1].item_off <= item) ++T;
-    const Tile& Ti = tiles[T];
-    const int rem = item - Ti.item_off;
-    const int kh = rem / Ti.nch, c = rem % Ti.nch;
-    const int QH = Ti.nq * GQ;
-    const int pos_last = Ti.pos0 + Ti.nq - 1;
-    const int key0 = c * CK;
-    const int nk = min(CK, pos_last - key0);
-    // K/V chunk -> shared memory (one bulk copy each)
-    if (tid == 0) {
-      const uint32_t bytes = (uint32_t)nk * hd * ESZ;
-      const size_t off = ((size_t)kh * D.max_seq + key0) * hd * ESZ;
-      mbar_arrive_expect_tx(&kv_bar, 2 * bytes);
-      const uint64_t pol = l2_evict_first_policy();
-      bulk_g2s(ks, Ti.kc + off, bytes, &kv_bar, pol);
-      bulk_g2s(vs, Ti.vc + off, bytes, &kv_bar, pol);
-    }
-    // queries (already rotated) -> shared memory
-    for (int idx = tid; idx < QH * hd; idx += kAttnThreads) {
-      const int qh = idx / hd, e = idx % hd;
-      const int r = qh / GQ, hg = qh % GQ;
-      qs[idx] = p.lc.act.qkv[(size_t)(Ti.vid0 + r) * qkv_rows + (kh * GQ + hg) * hd + e];
-    }
-    if (!mbar_wait_bounded(&kv_bar, phase)) s_fail = 1;
-    phase ^= 1;
-    __syncthreads();
-    if (s_fail) {  // uniform decision after the barrier
-      if (tid == 0) {
-        set_err(st, ERR_TIMEOUT, 30);
-        mbar_wait_bounded(&kv_bar, phase ^ 1);  // let the copies in flight land before leaving
-      }
-      break;
-    }
-    // scores
-    {
-      const int kl = lane / LPK, sub = lane % LPK;
-      for (int kb = warp * KPW; kb < CK; kb += 8 * KPW) {
-        const int kk = kb + kl;
-        float kf[16];
-        if (kk < nk) {
-          const WT* kr = ks + (size_t)kk * hd + sub * 16;
-#pragma unroll
-          for (int e = 0; e < 16; e += 16 / ESZ) {
-            const uint4 q4 = *reinterpret_cast<const uint4*>(kr + e);
-            WTraits<WT>::unpack(q4, kf + e);
-          }
-        } else {
-#pragma unroll
-          for (int e = 0; e < 16; ++e) kf[e] = 0.f;
-        }
-        for (int qh = 0; qh < QH; ++qh) {
-          const float* qv = qs + (size_t)qh * hd + sub * 16;
-          float dot = 0.f;
-#pragma unroll
-          for (int e = 0; e < 16; e += 4) {
-            const float4 q4 = *reinterpret_cast<const float4*>(qv + e);
-            dot = fmaf(kf[e], q4.x, dot);
-            dot = fmaf(kf[e + 1], q4.y, dot);
-            dot = fmaf(kf[e + 2], q4.z, dot);
-            dot = fmaf(kf[e + 3], q4.w, dot);
-          }
-          for (int o = LPK / 2; o > 0; o >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, o);
-          if (sub == 0 && kk < nk) {
-            const int pos_q = Ti.pos0 + qh / GQ;
-            sc[(size_t)qh * CK + kk] = (key0 + kk < pos_q) ? dot * scale : -INFINITY;
-          }
-        }
-      }
-    }
-    __syncthreads();
-    // per-chunk softmax statistics, one warp per query head
-    for (int qh = warp; qh < QH; qh += 8) {
-      float* srow = sc + (size_t)qh * CK;
-      float m = -INFINITY;
-      for (int k = lane; k < nk; k += 32) m = fmaxf(m, srow[k]);
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-      float l = 0.f;
-      for (int k = lane; k < nk; k += 32) {
-        const float pk = (m == -INFINITY) ? 0.f : expf(srow[k] - m);
-        srow[k] = pk;
-        l += pk;
-      }
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) l += __shfl_xor_sync(0xffffffffu, l, o);
-      if (lane == 0) { m_s[qh] = m; l_s[qh] = l; }
-    }
-    __syncthreads();
-    // unnormalised chunk output -> partial record (o[hd], m, l)
-    for (int idx = tid; idx < QH * hd; idx += kAttnThreads) {
-      const int qh = idx / hd, e = idx % hd;
-      const float* prow = sc + (size_t)qh * CK;
-      float o = 0.f;
-      for (int k = 0; k < nk; ++k) o = fmaf(prow[k], WTraits<WT>::to_f(vs[(size_t)k * hd + e]), o);
-      float* rec = part + ((size_t)Ti.rec_off + ((size_t)kh * Ti.nch + c) * QH + qh) * (hd + 2);
-      rec[e] = o;
-      if (e == 0) { rec[hd] = m_s[qh]; rec[hd + 1] = l_s[qh]; }
-    }
-    __threadfence();
-    __syncthreads();
-    if (tid == 0) {
-      const int old = atomicAdd(&tick[T * D.hkv + kh], 1);
-      s_last = (old == Ti.nch - 1);
-    }
-    __syncthreads();
-    if (s_last) {
-      __threadfence();
-      // merge this (tile, kv head): each query over its own chunks, in chunk order
-      for (int idx = tid; idx < QH * hd; idx += kAttnThreads) {
-        const int qh = idx / hd, e = idx % hd;
-        const int r = qh / GQ, hg = qh % GQ;
-        const int nc = (Ti.pos0 + r + CK - 1) / CK;
-        const float* base = part + ((size_t)Ti.rec_off + (size_t)kh * Ti.nch * QH + qh) * (hd + 2);
-        const size_t cstride = (size_t)QH * (hd + 2);
-        float M = -INFINITY;
-        for (int cc = 0; cc < nc; ++cc) M = fmaxf(M, __ldcg(base + cc * cstride + hd));
-        float Ls = 0.f, O = 0.f;
-        for (int cc = 0; cc < nc; ++cc) {
-          const float* rc = base + cc * cstride;
-          const float w = expf(__ldcg(rc + hd) - M);
-          Ls = fmaf(__ldcg(rc + hd + 1), w, Ls);
-          O = fmaf(__ldcg(rc + e), w, O);
-        }
-        p.lc.act.attn[(size_t)(Ti.vid0 + r) * hqd + (kh * GQ + hg) * hd + e] = O / Ls;
-      }
-      if (tid == 0) tick[T * D.hkv + kh] = 0;
-    }
-    __syncthreads();  // shared buffers are reused by the next item
-  }
+  att::run_items<WT, kAttnChunk>(p.D, st, tiles, s_nt, s_items, blockIdx.x, gridDim.x, p.qh_max, sm, &kv_bar,
+                                 phase, &s_fail, &s_last);
 }
 
 }  // namespace
 
 size_t attn_smem_bytes(const Dims& D, bool multi) {
-  const int esz = D.dtype == SPD_DTYPE_BF16 ? 2 : 4;
-  const int qh = (multi ? kAttnQT : 1) * D.gq;
-  return (size_t)2 * kAttnChunk * D.hd * esz + (size_t)qh * D.hd * 4 + (size_t)qh * kAttnChunk * 4 +
-         (size_t)2 * qh * 4;
+  return att::smem_bytes(D.hd, D.gq, D.dtype == SPD_DTYPE_BF16 ? 2 : 4, multi ? kAttnQT : 1, kAttnChunk);
 }
 
-size_t attn_part_floats(int rows, int hq, int hd, int max_seq) {
-  const int nch = (max_seq + kAttnChunk - 1) / kAttnChunk;
+size_t attn_part_floats(int rows, int hq, int hd, int max_seq, int ck) {
+  const int nch = (max_seq + ck - 1) / ck;
   return (size_t)rows * hq * nch * (hd + 2);
 }
 

@@ -1,0 +1,254 @@
+// Decode attention over per-layer KV caches: device code shared by the stand-alone attention
+// kernel (prefill blocks, stand-alone operators; chunks of 128 keys) and the persistent step
+// kernel (chunks of 64 keys).
+//
+// The query rows arrive already rotated (RoPE is applied in the QKV epilogue of the GEMV engine,
+// which also appends k and v to the cache).  Work item = (query tile, kv head, key chunk).  A tile
+// holds up to 8 query rows of one layer (1 row per token in the stage-diagonal step and in plain
+// AR); all query heads of the grouped-query group share the K/V chunk, which is bulk-copied into
+// shared memory once.  Scores use 16-dim lane slices reduced with xor shuffles, softmax is per
+// chunk (max, exp, sum), and the chunk partial (o, m, l) goes to global scratch.  The last item of
+// a (tile, kv head) to finish (atomic ticket, no spinning) merges the partials of each query in
+// chunk order.  The number of chunks depends only on the query position, so a token's result does
+// not depend on its batch.
+#pragma once
+#include "spd_internal.cuh"
+
+namespace spd {
+namespace att {
+
+constexpr int kThreads = 256;   // threads taking part (named barrier 2)
+
+struct Tile {
+  int layer, nq, pos0, vid0, nch, rec_off, item_off, tick_off;
+  const unsigned char* kc;  // base of this layer's K cache (head 0, position 1)
+  const unsigned char* vc;
+  const float* q;           // query rows [row][qkv_rows] (rotated q at the front)
+  float* out;               // attention output rows [row][hq*hd]
+  float* part;              // chunk partials of this tile's launch part
+  int* tick;                // merge tickets of this tile's launch part
+};
+
+// Appends the tiles of one part (a launch descriptor; rows of up to `qt` queries per tile).
+static __device__ int add_tiles(const Dims& D, const Bufs& B, const Launch& lc, int qt, int ck, Tile* tiles,
+                         int nt, int* items) {
+  DevState* st = B.st;
+  RowGroup rg[kMaxGroups];
+  int nr;
+  if (lc.kind == LK_EXPLICIT) {
+    nr = lc.cnt;
+    for (int r = 0; r < nr; ++r) {
+      rg[r].layer = 0; rg[r].nv = 1; rg[r].pos0 = lc.act.pos_arr[r]; rg[r].vid0 = r; rg[r].rrow0 = 0;
+    }
+  } else {
+    nr = build_rows(lc, D, st, rg);
+  }
+  const int esz = D.dtype == SPD_DTYPE_BF16 ? 2 : 4;
+  const size_t layer_elems = (size_t)D.hkv * D.max_seq * D.hd;
+  int rec = 0, local = 0;
+  for (int i = 0; i < nr; ++i) {
+    for (int r0 = 0; r0 < rg[i].nv; r0 += qt) {
+      if (nt >= kMaxTiles) { set_err(st, ERR_BOUNDS, 400); return -1; }
+      Tile& T = tiles[nt++];
+      T.layer = rg[i].layer;
+      T.nq = min(qt, rg[i].nv - r0);
+      T.pos0 = rg[i].pos0 + r0;
+      T.vid0 = rg[i].vid0 + r0;
+      const int pos_last = T.pos0 + T.nq - 1;
+      T.nch = (pos_last + ck - 1) / ck;
+      T.rec_off = rec;
+      T.item_off = *items;
+      T.tick_off = local * D.hkv;
+      rec += D.hkv * T.nch * T.nq * D.gq;
+      *items += D.hkv * T.nch;
+      ++local;
+      const void* kb;
+      const void* vb;
+      if (lc.kind == LK_EXPLICIT) { kb = lc.act.kc; vb = lc.act.vc; }
+      else if (lc.stack == 0) { kb = B.kc; vb = B.vc; }
+      else { kb = B.pkc; vb = B.pvc; }
+      T.kc = (const unsigned char*)kb + (size_t)T.layer * layer_elems * esz;
+      T.vc = (const unsigned char*)vb + (size_t)T.layer * layer_elems * esz;
+      T.q = lc.act.qkv; T.out = lc.act.attn; T.part = lc.act.part; T.tick = lc.act.tick;
+    }
+  }
+  return nt;
+}
+
+// Bytes of shared memory the item loop needs for chunks of `ck` keys and tiles of up to qt rows.
+__host__ __device__ inline size_t smem_bytes(int hd, int gq, int esz, int qt, int ck) {
+  const int qh = qt * gq;
+  return (size_t)2 * ck * hd * esz + (size_t)qh * hd * 4 + (size_t)qh * ck * 4 + (size_t)2 * qh * 4;
+}
+
+// Runs items item0, item0 + step, ... of the tiles on the 256 calling threads (threadIdx.x < 256).
+// `sm` (smem_bytes) and `kv_bar` (an initialised mbarrier, parity `phase`) belong to the caller;
+// `fail` is a shared flag.  Returns false if a bounded wait gave up.
+template <typename WT, int CK>
+static __device__ bool run_items(const Dims& D, DevState* st, const Tile* tiles, int nt, int n_items, int item0,
+                          int step, int qh_max, unsigned char* sm, uint64_t* kv_bar, uint32_t& phase,
+                          int* fail, int* last_flag) {
+  constexpr int ESZ = sizeof(WT);
+  const int hd = D.hd, GQ = D.gq;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  WT* ks = reinterpret_cast<WT*>(sm);
+  WT* vs = reinterpret_cast<WT*>(sm + (size_t)CK * hd * ESZ);
+  float* qs = reinterpret_cast<float*>(sm + (size_t)2 * CK * hd * ESZ);
+  float* sc = qs + (size_t)qh_max * hd;
+  float* m_s = sc + (size_t)qh_max * CK;
+  float* l_s = m_s + qh_max;
+  const float scale = 1.0f / sqrtf((float)hd);
+  const int qkv_rows = D.qkv_rows;
+  const int hqd = D.hq * hd;
+  const int LPK = hd / 16;  // lanes per key
+  const int KPW = 32 / LPK;
+  for (int item = item0; item < n_items; item += step) {
+    int T = 0;
+    while (T + 1 < nt && tiles[T + 1].item_off <= item) ++T;
+    const Tile& Ti = tiles[T];
+    const int rem = item - Ti.item_off;
+    const int kh = rem / Ti.nch, c = rem % Ti.nch;
+    const int QH = Ti.nq * GQ;
+    const int pos_last = Ti.pos0 + Ti.nq - 1;
+    const int key0 = c * CK;
+    const int nk = min(CK, pos_last - key0);
+    // K/V chunk -> shared memory (one bulk copy each)
+    if (tid == 0) {
+      const uint32_t bytes = (uint32_t)nk * hd * ESZ;
+      const size_t off = ((size_t)kh * D.max_seq + key0) * hd * ESZ;
+      mbar_arrive_expect_tx(kv_bar, 2 * bytes);
+      const uint64_t pol = l2_evict_first_policy();
+      bulk_g2s(ks, Ti.kc + off, bytes, kv_bar, pol);
+      bulk_g2s(vs, Ti.vc + off, bytes, kv_bar, pol);
+    }
+    // queries (already rotated) -> shared memory
+    for (int idx = tid; idx < QH * hd; idx += kThreads) {
+      const int qh = idx / hd, e = idx % hd;
+      const int r = qh / GQ, hg = qh % GQ;
+      qs[idx] = Ti.q[(size_t)(Ti.vid0 + r) * qkv_rows + (kh * GQ + hg) * hd + e];
+    }
+    if (!mbar_wait_bounded(kv_bar, phase)) *fail = 1;
+    phase ^= 1;
+    named_bar(2, kThreads);
+    if (*fail) {  // uniform decision after the barrier
+      if (tid == 0) {
+        set_err(st, ERR_TIMEOUT, 30);
+        mbar_wait_bounded(kv_bar, phase ^ 1);  // let the copies in flight land before leaving
+      }
+      return false;
+    }
+    // scores
+    {
+      const int kl = lane / LPK, sub = lane % LPK;
+      for (int kb = warp * KPW; kb < CK; kb += 8 * KPW) {
+        const int kk = kb + kl;
+        float kf[16];
+        if (kk < nk) {
+          const WT* kr = ks + (size_t)kk * hd + sub * 16;
+#pragma unroll
+          for (int e = 0; e < 16; e += 16 / ESZ) {
+            const uint4 q4 = *reinterpret_cast<const uint4*>(kr + e);
+            WTraits<WT>::unpack(q4, kf + e);
+          }
+        } else {
+#pragma unroll
+          for (int e = 0; e < 16; ++e) kf[e] = 0.f;
+        }
+        for (int qh = 0; qh < QH; ++qh) {
+          const float* qv = qs + (size_t)qh * hd + sub * 16;
+          float dot = 0.f;
+#pragma unroll
+          for (int e = 0; e < 16; e += 4) {
+            const float4 q4 = *reinterpret_cast<const float4*>(qv + e);
+            dot = fmaf(kf[e], q4.x, dot);
+            dot = fmaf(kf[e + 1], q4.y, dot);
+            dot = fmaf(kf[e + 2], q4.z, dot);
+            dot = fmaf(kf[e + 3], q4.w, dot);
+          }
+          for (int o = LPK / 2; o > 0; o >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, o);
+          if (sub == 0 && kk < nk) {
+            const int pos_q = Ti.pos0 + qh / GQ;
+            sc[(size_t)qh * CK + kk] = (key0 + kk < pos_q) ? dot * scale : -INFINITY;
+          }
+        }
+      }
+    }
+    named_bar(2, kThreads);
+    // per-chunk softmax statistics, one warp per query head
+    for (int qh = warp; qh < QH; qh += 8) {
+      float* srow = sc + (size_t)qh * CK;
+      float m = -INFINITY;
+      for (int k = lane; k < nk; k += 32) m = fmaxf(m, srow[k]);
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+      float l = 0.f;
+      for (int k = lane; k < nk; k += 32) {
+        const float pk = (m == -INFINITY) ? 0.f : expf(srow[k] - m);
+        srow[k] = pk;
+        l += pk;
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) l += __shfl_xor_sync(0xffffffffu, l, o);
+      if (lane == 0) { m_s[qh] = m; l_s[qh] = l; }
+    }
+    named_bar(2, kThreads);
+    // unnormalised chunk output -> partial record (o[hd], m, l).  With at most 128 outputs the
+    // keys are split between the two thread halves (lower half first, then added in that order).
+    const int nout = QH * hd;
+    const bool split = 2 * nout <= kThreads;
+    float* oh = qs;  // the queries are dead once the scores exist: scratch for the upper half
+    for (int idx = tid; idx < (split ? 2 * nout : nout); idx += kThreads) {
+      const int half = split ? idx / nout : 0;
+      const int o_i = split ? idx % nout : idx;
+      const int qh = o_i / hd, e = o_i % hd;
+      const float* prow = sc + (size_t)qh * CK;
+      const int k0 = split ? (half ? nk / 2 : 0) : 0;
+      const int k1 = split ? (half ? nk : nk / 2) : nk;
+      float o = 0.f;
+      for (int k = k0; k < k1; ++k) o = fmaf(prow[k], WTraits<WT>::to_f(vs[(size_t)k * hd + e]), o);
+      if (split && half) oh[o_i] = o;
+      if (split) named_bar(3, kThreads);  // every thread reaches it once (2 * nout <= kThreads)
+      if (!(split && half)) {
+        if (split) o += oh[o_i];
+        float* rec = Ti.part + ((size_t)Ti.rec_off + ((size_t)kh * Ti.nch + c) * QH + qh) * (hd + 2);
+        rec[e] = o;
+        if (e == 0) { rec[hd] = m_s[qh]; rec[hd + 1] = l_s[qh]; }
+      }
+    }
+    if (split && tid >= 2 * nout) named_bar(3, kThreads);  // threads without an output item
+    __threadfence();
+    named_bar(2, kThreads);
+    if (tid == 0) {
+      const int old = atomicAdd(&Ti.tick[Ti.tick_off + kh], 1);
+      *last_flag = (old == Ti.nch - 1);
+    }
+    named_bar(2, kThreads);
+    if (*last_flag) {
+      __threadfence();
+      // merge this (tile, kv head): each query over its own chunks, in chunk order
+      for (int idx = tid; idx < QH * hd; idx += kThreads) {
+        const int qh = idx / hd, e = idx % hd;
+        const int r = qh / GQ, hg = qh % GQ;
+        const int nc = (Ti.pos0 + r + CK - 1) / CK;
+        const float* base = Ti.part + ((size_t)Ti.rec_off + (size_t)kh * Ti.nch * QH + qh) * (hd + 2);
+        const size_t cstride = (size_t)QH * (hd + 2);
+        float M = -INFINITY;
+        for (int cc = 0; cc < nc; ++cc) M = fmaxf(M, __ldcg(base + cc * cstride + hd));
+        float Ls = 0.f, O = 0.f;
+        for (int cc = 0; cc < nc; ++cc) {
+          const float* rc = base + cc * cstride;
+          const float w = expf(__ldcg(rc + hd) - M);
+          Ls = fmaf(__ldcg(rc + hd + 1), w, Ls);
+          O = fmaf(__ldcg(rc + e), w, O);
+        }
+        Ti.out[(size_t)(Ti.vid0 + r) * hqd + (kh * GQ + hg) * hd + e] = O / Ls;
+      }
+      if (tid == 0) Ti.tick[Ti.tick_off + kh] = 0;
+    }
+    named_bar(2, kThreads);  // shared buffers are reused by the next item
+  }
+  return true;
+}
+
+}  // namespace att
+}  // namespace spd

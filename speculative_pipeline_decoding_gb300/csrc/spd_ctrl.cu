@@ -13,152 +13,26 @@
 //   no exit (warm-up / refill, a < n): the draft enters stage 1.
 //   draft-module cache length <- the pre-step v (rows at depth n are cached, SPD v3 App. A.1).
 // "Entering stage 1" writes the token's embedding into the residual ring and anchor b_0 = 0.
-#include "spd_internal.cuh"
+#include "spd_ctrl.cuh"
 
 namespace spd {
 
 namespace {
 
-template <typename WT>
-__device__ void push_embedding(const Dims& D, const Bufs& B, int tok, int slot) {
-  const WT* e = reinterpret_cast<const WT*>(B.embed) + (size_t)tok * D.d;
-  float* r = B.resid + (size_t)slot * D.d;
-  float* a0 = B.anch + (size_t)slot * D.m * D.d;
-  for (int c = threadIdx.x; c < D.d; c += blockDim.x) {
-    const float x = WTraits<WT>::to_f(e[c]);
-    r[c] = x;
-    a0[c] = x;
-  }
-}
-
-__device__ void reduce_head(const Bufs& B, Top2 (*red)[2]) {
-  Top2 acc[2];
-  top2_init(acc[0]);
-  top2_init(acc[1]);
-  for (int c = threadIdx.x; c < B.head_grid; c += blockDim.x) {
-    const float* hp = B.head_part + (size_t)c * 8;
-    for (int k = 0; k < 2; ++k) {
-      Top2 t;
-      t.v1 = hp[k * 4 + 0]; t.i1 = __float_as_int(hp[k * 4 + 1]);
-      t.v2 = hp[k * 4 + 2]; t.i2 = __float_as_int(hp[k * 4 + 3]);
-      top2_merge(acc[k], t);
-    }
-  }
-  red[threadIdx.x][0] = acc[0];
-  red[threadIdx.x][1] = acc[1];
-  __syncthreads();
-  for (int s = blockDim.x / 2; s > 0; s >>= 1) {
-    if ((int)threadIdx.x < s) {
-      top2_merge(red[threadIdx.x][0], red[threadIdx.x + s][0]);
-      top2_merge(red[threadIdx.x][1], red[threadIdx.x + s][1]);
-    }
-    __syncthreads();
-  }
-}
+using ctl::push_embedding;
 
 template <typename WT>
 __global__ void __launch_bounds__(256) control_cycle_kernel(Dims D, Bufs B) {
   __shared__ Top2 red[256][2];
   __shared__ int s_tok, s_slot;
-  DevState* st = B.st;
-  if (st->done || st->err) return;
-  reduce_head(B, red);
-  if (threadIdx.x == 0) {
-    const int n = D.n, P = st->P;
-    int t = st->t, a = st->a, v = st->v;
-    const int v_pre = v;
-    const bool target_only = (st->flags & SF_TARGET_ONLY) != 0;
-    s_tok = -1;
-    if (t + 1 > D.max_seq) {
-      set_err(st, ERR_BOUNDS, 500);
-    } else {
-      int p1 = red[0][1].i1, p2 = red[0][1].i2;
-      if (target_only) p1 = p2 = B.seq[t];
-      const int q = t + 1;
-      const int mode = B.ovr_mode[q];
-      const int ref = B.ovr_ref[q];
-      int draft = p1;
-      if (mode == 1) draft = ref;
-      else if (mode == 2) draft = target_only ? (ref + 1) % D.V : ((p1 != ref) ? p1 : p2);
-      st->pdm_top1 = p1; st->pdm_top2 = p2; st->draft = draft;
-      int push = draft;
-      if (a == n) {
-        const int te = t - n + 1;
-        const int y = red[0][0].i1;
-        const int succ = (te + 1 <= t) ? B.seq[te + 1] : draft;
-        const int accept = succ == y;
-        const int k = st->exits;
-        if (k < D.max_seq) {
-          B.trace[k] = te + 1;
-          B.trace[D.max_seq + k] = accept;
-        }
-        st->exits = k + 1;
-        st->last_exited = 1; st->last_exit_pos = te; st->last_accept = accept; st->target_top1 = y;
-        v = te;
-        if (accept) {
-          a -= 1;
-        } else {
-          st->rejects += 1;
-          for (int l = 0; l < D.L; ++l) B.kvlen[l] = te;
-          a = 0;
-          t = te;
-          push = y;
-        }
-      } else {
-        st->last_exited = 0; st->last_exit_pos = 0; st->last_accept = 0;
-      }
-      if (push < 0 || push >= D.V) {  // e.g. non-finite logits left no valid argmax
-        set_err(st, ERR_BOUNDS, 501);
-        push = -1;
-      }
-      if (!target_only) st->pdm_len = v_pre;
-      t += 1;
-      a += 1;
-      B.seq[t] = push;
-      st->pushed = push;
-      st->t = t; st->a = a; st->v = v;
-      st->cycles += 1;
-      if (v + 1 - P >= st->max_commit) st->done = 1;
-      s_tok = push;
-      s_slot = t % (n + 1);
-    }
-  }
-  __syncthreads();
-  if (s_tok >= 0) push_embedding<WT>(D, B, s_tok, s_slot);
+  ctl::control_cycle<WT>(D, B, red, s_tok, s_slot, 256, 1);
 }
 
 template <typename WT>
 __global__ void __launch_bounds__(256) control_ar_kernel(Dims D, Bufs B) {
   __shared__ Top2 red[256][2];
   __shared__ int s_tok, s_slot;
-  DevState* st = B.st;
-  if (st->done || st->err) return;
-  reduce_head(B, red);
-  if (threadIdx.x == 0) {
-    s_tok = -1;
-    const int t = st->t;
-    if (t + 1 > D.max_seq) {
-      set_err(st, ERR_BOUNDS, 510);
-    } else {
-      const int y = red[0][0].i1;
-      if (y < 0 || y >= D.V) {
-        set_err(st, ERR_BOUNDS, 511);
-        s_tok = -1;
-      }
-      st->target_top1 = y;
-      st->v = t;
-      st->t = t + 1;
-      st->a = 1;
-      B.seq[t + 1] = y;
-      st->pushed = y;
-      st->cycles += 1;
-      if (st->v + 1 - st->P >= st->max_commit) st->done = 1;
-      if (y >= 0 && y < D.V) s_tok = y;
-      s_slot = (t + 1) % (D.n + 1);
-    }
-  }
-  __syncthreads();
-  if (s_tok >= 0) push_embedding<WT>(D, B, s_tok, s_slot);
+  ctl::control_ar<WT>(D, B, red, s_tok, s_slot, 256, 1);
 }
 
 template <typename WT>
@@ -178,7 +52,7 @@ __global__ void __launch_bounds__(256) prefill_finish_kernel(Dims D, Bufs B, int
   __shared__ Top2 red[256][2];
   __shared__ int s_tok;
   DevState* st = B.st;
-  reduce_head(B, red);
+  ctl::reduce_head(B, red, 256, 1);
   if (threadIdx.x == 0) {
     int x = red[0][0].i1;
     if (x < 0 || x >= D.V) {
@@ -195,7 +69,7 @@ __global__ void __launch_bounds__(256) prefill_finish_kernel(Dims D, Bufs B, int
     s_tok = x;
   }
   __syncthreads();
-  if (s_tok >= 0) push_embedding<WT>(D, B, s_tok, (P + 1) % (D.n + 1));
+  if (s_tok >= 0) push_embedding<WT>(D, B, s_tok, (P + 1) % (D.n + 1), blockDim.x);
 }
 
 template <typename WT>
@@ -210,7 +84,7 @@ __global__ void __launch_bounds__(256) rollback_kernel(Dims D, Bufs B, int keep,
     B.seq[keep + 1] = reseed;
     for (int l = 0; l < D.L; ++l) B.kvlen[l] = keep;
   }
-  push_embedding<WT>(D, B, reseed, (keep + 1) % (D.n + 1));
+  push_embedding<WT>(D, B, reseed, (keep + 1) % (D.n + 1), blockDim.x);
 }
 
 __global__ void begin_generate_kernel(Bufs B, int max_new) {

@@ -1,394 +1,27 @@
-// Grouped GEMV engine for the SPD cycle.
-//
-// One launch computes y_g = W_g x_g for up to kMaxGroups groups.  Each group has its own weights,
-// operator and epilogue, so one launch can carry the stage-diagonal step of the target (the token
-// at depth j runs layer j*S+s, SPD summary 方法步骤详情 step 1) together with the draft module's rows
-// (steps 3-4).
-//
-// Weight streaming: one producer warp issues 2-D TMA tensor copies (cp.async.bulk.tensor, boxes of
-// 128 bytes x 32 rows with the 128-byte swizzle, L2 evict-first) into a 4-deep ring of 32 KB stages
-// guarded by mbarriers; a stage holds 64 weight rows x 512 bytes (4 boxes wide, 2 boxes high).
-// Every weight matrix has its own tensor map, encoded once when the handle is created.  Copies of
-// 4 KB keep the per-copy cost of the copy engine below the HBM time of the bytes it moves.
-//
-// Work split: every CTA of the persistent grid (one per SM) takes a contiguous share of the
-// launch's weight bytes, cut at 32-row boundaries; tiles never straddle a group or a share.
-//
-// Two compute paths, eight consumer warps:
-//  * single input vector (target step, plain AR, heads): warp w owns weight rows w, w+8, ..., w+56
-//    of the stage, lane l the 16-byte column vector l of each 512-byte row slice (bf16: columns
-//    8l..8l+7); the activation slice (RMS-normalised when the operator has a norm) comes through
-//    L1 and is reused over the warp's 8 rows.  Partial sums stay in registers across stages; a row
-//    ends with one xor-tree warp reduction.  A row's arithmetic depends only on its column count,
-//    never on the other groups of the launch, so a token's results are bit-identical in plain AR
-//    and in the SPD step.
-//  * several input vectors sharing the weights (draft-module rows, prefill blocks; bf16 weights):
-//    m16n8k16 bf16 tensor-core MMAs with fp32 accumulation, the weight rows as the n8 operand
-//    (ldmatrix through the swizzle) and the vectors as the m16 operand.  The fp32 activations are
-//    split into bf16 high and low halves (x = hi + lo keeps ~16 significant bits) and both are
-//    multiplied into the accumulator.  Warp w takes the two 16-column k-steps 32w..32w+31 of every
-//    stage; the eight partial tiles are added in warp order at the end of a tile.
-//
-// Epilogues (per group):
-//   STORE   y = W x                                  (anchor FC, stand-alone operator)
-//   RESID   h += W x, anchor capture when the layer index + 1 = b_i   (o-proj, down)
-//   SWIGLU  u = silu(W_gate x) * (W_up x)            (gate/up; x = RMSNorm(h) * ffn_norm)
-//   QKV     x = RMSNorm(h) * attn_norm; q and k rotated by RoPE (rotate-half pairs i, i+hd/2: a tile
-//           holds 32 rows of a head and their 32 partners), q written for attention, k and v
-//           rounded to the cache dtype and appended to the layer's KV cache at position pos-1
-//   TOP2    logits of the vocab head; per-CTA top-2 (+ optional full logits for debugging)
+// Stand-alone launches of the grouped GEMV engine (spd_engine.cuh): the prefill blocks, the
+// per-operator path used when the step kernel is not, and the stand-alone operator
+// spd_grouped_gemv.  One CTA per SM; one producer warp streams the weights with 2-D TMA tensor
+// copies, eight consumer warps compute.
 #include <cudaTypedefs.h>
 
-#include "spd_internal.cuh"
+#include "spd_engine.cuh"
 
 namespace spd {
 
 namespace {
 
-constexpr int kBig = 1 << 30;
-constexpr int kNCW = 8;                        // consumer warps
-constexpr int kThreads = (kNCW + 1) * 32;      // + one producer warp
-constexpr int kBoxRows = 32;                   // rows of one tensor-map box (128 bytes wide)
-constexpr int kBoxBytes = kBoxRows * 128;
-constexpr int kSlots = 64;                     // weight rows per stage (2 boxes high)
-constexpr int kStageBytes = kSlots * 512;      // 4 boxes wide
-constexpr int kStages = 4;
-constexpr int kRedFloats = kNCW * 8 * 4 * 32;  // tensor-core partial tiles of one m-tile (32 KB)
-constexpr int kDynSmem = 1024 + kStages * kStageBytes + kRedFloats * 4;
-constexpr int kMaxMT = 2;                      // tensor-core path: up to 2 m-tiles of 16 vectors
+using namespace eng;
 
-enum Epi { EPI_STORE = 0, EPI_RESID = 1, EPI_SWIGLU = 2, EPI_QKV = 3, EPI_TOP2 = 4 };
-
-struct GG {
-  const CUtensorMap* m[3];     // tensor maps of the segments (QKV: wq | wk | wv); gate/up: gate, up
-  int seg1, seg2;              // first row of segment 1 and 2
-  int rows, cols;              // output rows (gate/up: rows of each weight), input columns
-  short nv, nw, epi, kind;     // vectors, weights per output row, epilogue, head kind
-  short mma, tr;               // tensor-core path; tile height in output rows (64 / nw)
-  const float* x; int xrow0, xring, xstride;
-  float* y; int yrow0, yring, ystride;
-  const float* normw;
-  float* anch; int astride;    // anchor capture (row (yrow0+v) % yring of the anchor ring)
-  void* kc; void* vc;          // QKV: K / V cache of this layer, [Hkv][max_seq][hd]
-  int pos0;                    // QKV: position of vector 0
-  int* kvlen;                  // QKV on the target stack: kvlen[layer]
-  long long cost0;             // weight elements of the launch before this group
-};
+constexpr int kGemvSmem = 1024 + kStages * kStageBytes + kMmaScratch;
 
 struct GemvParams {
+  EngineCfg cfg;
   int nparts;
   GemvPart part[2];
   int explicit_mode;
   int resolve_after_wait;      // the control block may have been written by the previous kernel
-  int debug_logits;
-  int has_mma;                 // bf16 weights (tensor-core path available)
-  float eps;
-  Dims D;
-  Bufs B;
   GemvExplicit ge;
 };
-
-__device__ __forceinline__ long long rowcost(const GG& g) { return (long long)g.cols * g.nw; }
-
-__device__ __forceinline__ int anchor_index(const Dims& D, int layer_done) {
-  for (int i = 0; i < D.m; ++i)
-    if (D.anchors[i] == layer_done) return i;
-  return -1;
-}
-
-__device__ __forceinline__ void gg_clear(GG& o) {
-  o.seg1 = o.seg2 = kBig;
-  o.nw = 1; o.epi = EPI_STORE; o.kind = 0; o.mma = 0; o.nv = 1;
-  o.normw = nullptr; o.anch = nullptr; o.astride = 0;
-  o.kc = o.vc = nullptr; o.pos0 = 0; o.kvlen = nullptr;
-  o.xrow0 = o.yrow0 = 0; o.xring = o.yring = kBig;
-}
-
-// Appends the groups of one launch part; returns the new group count.
-__device__ int add_part(const GemvParams& p, const GemvPart& pt, GG* gg, int ng) {
-  const Dims& D = p.D;
-  const Bufs& B = p.B;
-  const Launch& lc = pt.lc;
-  const Act& A = lc.act;
-  DevState* st = B.st;
-  if (pt.op == OP_HEAD) {
-    auto add = [&](const float* x, int xrow0, int xring, const CUtensorMap* W, const float* nw, int kind) {
-      GG& o = gg[ng++];
-      gg_clear(o);
-      o.m[0] = o.m[1] = o.m[2] = W;
-      o.rows = D.V; o.cols = D.d;
-      o.x = x; o.xrow0 = xrow0; o.xring = xring; o.xstride = D.d;
-      o.y = nullptr; o.normw = nw; o.epi = EPI_TOP2; o.kind = kind;
-    };
-    if (lc.kind == LK_DIAG) {
-      if (st->a == D.n) add(B.resid, (st->t - D.n + 1) % (D.n + 1), D.n + 1, B.tm_lm, B.final_norm, 0);
-      if (!(st->flags & SF_TARGET_ONLY)) {
-        const int R = st->t - st->pdm_len;
-        if (R < 1 || R > D.n + 1) set_err(st, ERR_PDM_ROWS, 200);
-        else add(A.qkv /* draft rows z */, R - 1, kBig, B.tm_pdm, B.pdm_norm, 1);
-      }
-    } else if (lc.kind == LK_AR) {
-      add(B.resid, st->t % (D.n + 1), D.n + 1, B.tm_lm, B.final_norm, 0);
-    } else if (lc.kind == LK_ROWS) {
-      add(A.resid, lc.cnt - 1, kBig, B.tm_lm, B.final_norm, 0);
-    }
-    return ng;
-  }
-  if (pt.op == OP_FC) {
-    // draft rows: depth by the staircase, f by the anchor table; equal f are contiguous runs
-    if (lc.kind == LK_ROWS) {
-      const int f = D.ftab[D.n];
-      GG& o = gg[ng++];
-      gg_clear(o);
-      o.m[0] = o.m[1] = o.m[2] = B.tm_fc[f];
-      o.rows = D.d; o.cols = (f + 1) * D.d; o.nv = lc.cnt;
-      o.x = A.anch; o.xstride = D.m * D.d;
-      o.y = A.resid; o.ystride = D.d;
-      return ng;
-    }
-    const int t = st->t, a = st->a, R = t - st->pdm_len;
-    if (R < 1 || R > D.n + 1) {
-      set_err(st, ERR_PDM_ROWS, 300);
-      return ng;
-    }
-    int prev_f = -1;
-    for (int r = 0; r < R; ++r) {
-      const int pos = st->pdm_len + 1 + r;
-      const int depth = (t - pos < a) ? (t - pos) : D.n;
-      const int f = D.ftab[depth];
-      if (f != prev_f) {
-        GG& o = gg[ng++];
-        gg_clear(o);
-        o.m[0] = o.m[1] = o.m[2] = B.tm_fc[f];
-        o.rows = D.d; o.cols = (f + 1) * D.d; o.nv = 0;
-        o.x = B.anch; o.xrow0 = pos % (D.n + 1); o.xring = D.n + 1; o.xstride = D.m * D.d;
-        o.y = A.resid; o.yrow0 = r; o.ystride = D.d;
-        prev_f = f;
-      }
-      gg[ng - 1].nv++;
-    }
-    return ng;
-  }
-  RowGroup rg[kMaxGroups];
-  const int nr = build_rows(lc, D, st, rg);
-  const LayerW* LW = lc.stack == 0 ? B.tl : B.pl;
-  const int hqd = D.hq * D.hd;
-  const int esz = D.dtype == SPD_DTYPE_BF16 ? 2 : 4;
-  const size_t layer_bytes = (size_t)D.hkv * D.max_seq * D.hd * esz;
-  for (int i = 0; i < nr; ++i) {
-    GG& o = gg[ng++];
-    gg_clear(o);
-    const LayerW& w = LW[rg[i].layer];
-    o.nv = rg[i].nv;
-    switch (pt.op) {
-      case OP_QKV:
-        o.m[0] = w.tq; o.m[1] = w.tk; o.m[2] = w.tv;
-        o.seg1 = hqd; o.seg2 = hqd + D.hkv * D.hd; o.rows = D.qkv_rows; o.cols = D.d;
-        o.x = A.resid; o.xrow0 = rg[i].rrow0; o.xring = A.resid_ring; o.xstride = D.d;
-        o.normw = (const float*)w.attn_norm;
-        o.y = A.qkv; o.yrow0 = rg[i].vid0; o.ystride = D.qkv_rows;
-        o.epi = EPI_QKV;
-        o.kc = (unsigned char*)(lc.stack == 0 ? B.kc : B.pkc) + (size_t)rg[i].layer * layer_bytes;
-        o.vc = (unsigned char*)(lc.stack == 0 ? B.vc : B.pvc) + (size_t)rg[i].layer * layer_bytes;
-        o.pos0 = rg[i].pos0;
-        o.kvlen = (lc.stack == 0 && B.kvlen) ? B.kvlen + rg[i].layer : nullptr;
-        break;
-      case OP_O:
-        o.m[0] = o.m[1] = o.m[2] = w.to;
-        o.rows = D.d; o.cols = hqd;
-        o.x = A.attn; o.xrow0 = rg[i].vid0; o.xstride = hqd;
-        o.y = A.resid; o.yrow0 = rg[i].rrow0; o.yring = A.resid_ring; o.ystride = D.d;
-        o.epi = EPI_RESID;
-        break;
-      case OP_GATEUP:
-        o.m[0] = w.tg; o.m[1] = w.tu; o.m[2] = w.tu; o.nw = 2;
-        o.rows = D.ffn; o.cols = D.d;
-        o.x = A.resid; o.xrow0 = rg[i].rrow0; o.xring = A.resid_ring; o.xstride = D.d;
-        o.normw = (const float*)w.ffn_norm;
-        o.y = A.u; o.yrow0 = rg[i].vid0; o.ystride = D.ffn;
-        o.epi = EPI_SWIGLU;
-        break;
-      default: {  // OP_DOWN
-        o.m[0] = o.m[1] = o.m[2] = w.td;
-        o.rows = D.d; o.cols = D.ffn;
-        o.x = A.u; o.xrow0 = rg[i].vid0; o.xstride = D.ffn;
-        o.y = A.resid; o.yrow0 = rg[i].rrow0; o.yring = A.resid_ring; o.ystride = D.d;
-        o.epi = EPI_RESID;
-        const int ai = (lc.stack == 0 && A.anch) ? anchor_index(D, rg[i].layer + 1) : -1;
-        if (ai >= 0) { o.anch = A.anch + (size_t)ai * D.d; o.astride = D.m * D.d; }
-      }
-    }
-  }
-  return ng;
-}
-
-// Resolves every group of the launch and fixes each group's path and tile height.  Groups with
-// several vectors that cannot take the tensor-core path are split into one group per vector.
-__device__ int resolve_groups(const GemvParams& p, GG* gg) {
-  int ng = 0;
-  if (p.explicit_mode) {
-    for (int g = 0; g < p.ge.G; ++g) {
-      GG& o = gg[ng++];
-      gg_clear(o);
-      o.m[0] = o.m[1] = o.m[2] = p.ge.tm[g];
-      o.rows = p.ge.rows; o.cols = p.ge.cols;
-      o.x = p.ge.x[g]; o.xstride = p.ge.cols;
-      o.y = p.ge.y[g]; o.ystride = p.ge.rows;
-      o.normw = p.ge.nw;
-    }
-  } else {
-    for (int i = 0; i < p.nparts; ++i) ng = add_part(p, p.part[i], gg, ng);
-  }
-  // paths; without tensor cores (fp32 weights) a multi-vector group becomes one group per vector
-  int out = ng;
-  for (int g = ng - 1; g >= 0; --g) {
-    GG& o = gg[g];
-    if (o.nv > 1 && !p.has_mma) {
-      const int nv = o.nv;
-      if (out + nv - 1 > kMaxGroups) { set_err(p.B.st, ERR_BOUNDS, 90); return 0; }
-      for (int k = out - 1; k > g; --k) gg[k + nv - 1] = gg[k];  // make room after g
-      for (int v = nv - 1; v >= 0; --v) {
-        GG& c = gg[g + v];
-        c = o;  // o is still intact at index g until v == 0
-        c.nv = 1;
-        c.xrow0 = o.xrow0 + v; c.yrow0 = o.yrow0 + v; c.pos0 = o.pos0 + v;
-      }
-      out += nv - 1;
-    }
-  }
-  ng = out;
-  long long cost = 0;
-  for (int g = 0; g < ng; ++g) {
-    GG& o = gg[g];
-    if (o.nv > 16 * kMaxMT) { set_err(p.B.st, ERR_BOUNDS, 91); return 0; }
-    o.mma = o.nv > 1;
-    o.tr = (short)(kSlots / o.nw);
-    o.cost0 = cost;
-    cost += (long long)o.rows * rowcost(o);
-  }
-  return ng;
-}
-
-// Row boundary of weight-cost position X: first row of the group holding X whose cost prefix is
-// >= X, rounded down to a 32-row box (to a whole 64-row tile in the rotary region of a QKV group,
-// whose tiles hold complete (i, i+hd/2) pairs).  Monotone in X, so neighbouring shares meet exactly.
-__device__ void locate(const GG* gg, int ng, long long X, int& g, int& r) {
-  g = 0;
-  while (g < ng && X >= gg[g].cost0 + (long long)gg[g].rows * rowcost(gg[g])) ++g;
-  if (g >= ng) { g = ng; r = 0; return; }
-  const long long rc = rowcost(gg[g]);
-  r = (int)((X - gg[g].cost0 + rc - 1) / rc);
-  const int gran = (gg[g].epi == EPI_QKV && r < gg[g].seg2) ? kSlots : kBoxRows;
-  r -= r % gran;
-  if (r >= gg[g].rows) { ++g; r = 0; }
-}
-
-__device__ __forceinline__ float warp_sum(float v) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-  return v;
-}
-
-// Physical weight row of virtual row `r` of a group.  In the rotary region of a QKV group a
-// 64-row tile holds rows i0..i0+31 of one head and their partners i0+hd/2..i0+hd/2+31.
-__device__ __forceinline__ int phys_row(const GG& G, int r, int hd) {
-  if (G.epi != EPI_QKV || r >= G.seg2) return r;
-  const int h = r / hd, vb = r % hd;
-  const int blk = vb / kSlots, j = vb % kSlots;
-  return h * hd + (j < kBoxRows ? blk * kBoxRows + j : hd / 2 + blk * kBoxRows + (j - kBoxRows));
-}
-
-__device__ __forceinline__ void tma_box(void* dst, const CUtensorMap* map, int x, int y, uint64_t* bar,
-                                        uint64_t pol) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
-      " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(smem_u32(dst)), "l"(map), "r"(x), "r"(y),
-      "r"(smem_u32(bar)), "l"(pol)
-      : "memory");
-}
-
-// Byte offset in a stage of the 16-byte chunk `j` (0..31 across the 512-byte row slice) of slot
-// `slot` (0..63): box (slot/32, j/8), row slot%32, 128-byte swizzle (chunk ^ row % 8).
-__device__ __forceinline__ uint32_t stage_off(int slot, int j) {
-  const int rb = slot >> 5, rr = slot & 31;
-  return (uint32_t)(((rb * 4 + (j >> 3)) * kBoxBytes) + rr * 128 + (((j & 7) ^ (rr & 7)) << 4));
-}
-
-__device__ __forceinline__ uint32_t pack_bf16x2(float lo_k, float hi_k) {
-  const __nv_bfloat162 v = __floats2bfloat162_rn(lo_k, hi_k);
-  return *reinterpret_cast<const uint32_t*>(&v);
-}
-
-__device__ __forceinline__ void ldmatrix_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
-                                            uint32_t& r3) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
-               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3) : "r"(addr));
-}
-
-__device__ __forceinline__ void mma_bf16(float* c, const uint32_t* a, uint32_t b0, uint32_t b1) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
-      "{%0,%1,%2,%3};"
-      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
-      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
-}
-
-template <typename WT>
-__device__ __forceinline__ void store_kv(void* base, int head, int pos, int e, const Dims& D, float v) {
-  WT* p = reinterpret_cast<WT*>(base) + ((size_t)head * D.max_seq + (pos - 1)) * D.hd + e;
-  *p = WTraits<WT>::from_f(v);
-}
-
-// Epilogue of one output row (or rotary pair) for vector v.  y0/y1: the two accumulations the
-// caller holds (gate/up: gate and up of row r; rotary: rows r and its partner; else y1 unused).
-template <typename WT>
-__device__ __forceinline__ void epilogue(const GemvParams& p, const GG& G, int v, int row, float y0,
-                                         float y1, bool pair, Top2* loc) {
-  const Dims& D = p.D;
-  if (G.epi == EPI_TOP2) {
-    top2_push(loc[G.kind], y0, row);
-    if (p.debug_logits) p.B.logits[(size_t)G.kind * D.V + row] = y0;
-    return;
-  }
-  const int yr = (G.yrow0 + v) % G.yring;
-  float* yrow = G.y + (size_t)yr * G.ystride;
-  switch (G.epi) {
-    case EPI_SWIGLU:
-      yrow[row] = (y0 / (1.0f + expf(-y0))) * y1;
-      break;
-    case EPI_RESID: {
-      const float hn = yrow[row] + y0;
-      yrow[row] = hn;
-      if (G.anch) G.anch[(size_t)yr * G.astride + row] = hn;
-      break;
-    }
-    case EPI_QKV: {
-      const int pos = G.pos0 + v;
-      const int hd = D.hd, half = hd / 2;
-      if (pair) {  // row = physical index of the first element of a rotary pair
-        const int h = row / hd, i = row % hd;
-        const float c = p.B.rope_cos[(size_t)(pos - 1) * half + i];
-        const float s = p.B.rope_sin[(size_t)(pos - 1) * half + i];
-        const float r1 = y0 * c - y1 * s;
-        const float r2 = y1 * c + y0 * s;
-        if (h < D.hq) {
-          yrow[h * hd + i] = r1;
-          yrow[h * hd + i + half] = r2;
-        } else {
-          store_kv<WT>(G.kc, h - D.hq, pos, i, D, r1);
-          store_kv<WT>(G.kc, h - D.hq, pos, i + half, D, r2);
-          if (G.kvlen && h == D.hq && i == 0) *G.kvlen = pos;
-        }
-      } else {  // value row
-        const int vr = row - G.seg2;
-        store_kv<WT>(G.vc, vr / hd, pos, vr % hd, D, y0);
-      }
-      break;
-    }
-    default:
-      yrow[row] = y0;
-  }
-}
 
 template <typename WT>
 __global__ void __launch_bounds__(kThreads, 1) gemv_engine(const __grid_constant__ GemvParams p) {
@@ -396,10 +29,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_engine(const __grid_constant
   // the 128-byte swizzle wants 1024-byte aligned boxes
   unsigned char* ring =
       reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
-  float* red = reinterpret_cast<float*>(ring + kStages * kStageBytes);
-  constexpr int VEC = WTraits<WT>::kVec;   // elements per 16-byte chunk
-  constexpr int CW = 512 / sizeof(WT);     // columns per stage
-  constexpr int BOXC = 128 / sizeof(WT);   // columns per box
+  unsigned char* scratch = ring + kStages * kStageBytes;
 
   __shared__ GG gg[kMaxGroups];
   __shared__ int s_ng, s_gb, s_rb, s_ge, s_re;
@@ -410,7 +40,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_engine(const __grid_constant
   __shared__ Top2 hred[kNCW * 8][2];
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  DevState* st = p.B.st;
+  DevState* st = p.cfg.B.st;
   if (p.resolve_after_wait) pdl_wait();
   if (tid == 0) {
     for (int i = 0; i < kStages; ++i) {
@@ -418,321 +48,31 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_engine(const __grid_constant
       mbar_init(&empty_bar[i], kNCW);
     }
     fence_mbar_init();
-    const bool skip = !p.explicit_mode && (st->done || st->err);
-    const int ng = skip ? 0 : resolve_groups(p, gg);
+    int ng = 0;
+    if (p.explicit_mode) ng = resolve_explicit(p.cfg, p.ge, gg);
+    else if (!(st->done || st->err)) ng = resolve_parts(p.cfg, p.part, p.nparts, gg, kMaxGroups);
     s_ng = ng;
-    const long long total = ng ? gg[ng - 1].cost0 + (long long)gg[ng - 1].rows * rowcost(gg[ng - 1]) : 0;
-    int gb = ng, rb = 0, ge = ng, re = 0;
-    if (ng) {
-      locate(gg, ng, total * blockIdx.x / gridDim.x, gb, rb);
-      locate(gg, ng, total * (blockIdx.x + 1) / gridDim.x, ge, re);
-    }
-    s_gb = gb; s_rb = rb; s_ge = ge; s_re = re;
+    span_of(gg, ng, blockIdx.x, gridDim.x, s_gb, s_rb, s_ge, s_re);
   }
   __syncthreads();
   const int ng = s_ng;
-  const int gbeg = s_gb, rbeg = s_rb, gend = s_ge, rend = s_re;
-  const int hd = p.D.hd;
+  Ring R{ring, full_bar, empty_bar, 0u, false};
 
-  if (warp == kNCW) {
-    // ------------------------------ producer warp ------------------------------
-    const uint64_t pol = l2_evict_first_policy();
-    uint32_t ctr = 0;
-    bool failed = false;
-    for (int g = gbeg, r = rbeg; (g < gend || (g == gend && r < rend)) && !failed;) {
-      const GG& G = gg[g];
-      const int last = (g == gend) ? rend : G.rows;
-      const int tr = min((int)G.tr, last - r);
-      const int nrb = G.nw == 2 ? 2 : (tr + kBoxRows - 1) / kBoxRows;  // row boxes per stage
-      // tensor map and first row of each row box
-      const CUtensorMap* m0;
-      const CUtensorMap* m1;
-      int y0, y1;
-      if (G.nw == 2) {
-        m0 = G.m[0]; m1 = G.m[1]; y0 = y1 = r;
-      } else {
-        const int p0 = phys_row(G, r, hd), p1 = phys_row(G, r + kBoxRows, hd);
-        const int s0 = p0 < G.seg1 ? 0 : (p0 < G.seg2 ? 1 : 2);
-        const int s1 = p1 < G.seg1 ? 0 : (p1 < G.seg2 ? 1 : 2);
-        m0 = G.m[s0]; m1 = G.m[s1];
-        y0 = p0 - (s0 == 0 ? 0 : (s0 == 1 ? G.seg1 : G.seg2));
-        y1 = p1 - (s1 == 0 ? 0 : (s1 == 1 ? G.seg1 : G.seg2));
-      }
-      for (int c0 = 0; c0 < G.cols; c0 += CW) {
-        const int s = ctr % kStages;
-        if (ctr >= (uint32_t)kStages &&
-            !mbar_wait_bounded(&empty_bar[s], ((ctr / kStages) - 1) & 1)) {
-          if (lane == 0) set_err(st, ERR_TIMEOUT, 40);
-          failed = true;
-          break;
-        }
-        if (lane == 0) mbar_arrive_expect_tx(&full_bar[s], (uint32_t)(nrb * 4 * kBoxBytes));
-        __syncwarp();
-        if (lane < nrb * 4) {
-          const int rb = lane >> 2, cb = lane & 3;
-          tma_box(ring + (size_t)s * kStageBytes + (size_t)(rb * 4 + cb) * kBoxBytes, rb ? m1 : m0,
-                  c0 + cb * BOXC, rb ? y1 : y0, &full_bar[s], pol);
-        }
-        ++ctr;
-      }
-      r += tr;
-      if (r >= last) { ++g; r = 0; }
-    }
-    if (failed && lane == 0) {  // let the copies in flight land before leaving
-      const uint32_t first = ctr > (uint32_t)kStages ? ctr - kStages : 0;
-      for (uint32_t c = first; c < ctr; ++c) mbar_wait_bounded(&full_bar[c % kStages], (c / kStages) & 1);
-    }
+  if (warp == kNCW) {  // producer warp
+    produce_span<WT>(gg, s_gb, s_rb, s_ge, s_re, p.cfg.D.hd, R, st, l2_evict_first_policy(), lane);
+    drain_ring(R, lane);
     return;
   }
-
-  // ------------------------------ consumer warps ------------------------------
   if (!p.resolve_after_wait) pdl_wait();   // activations of the previous kernel are visible now
   pdl_trigger();
-  constexpr int NCT = kNCW * 32;
-  uint32_t ctr = 0;
-  bool failed = false;
   Top2 loc[2];
   top2_init(loc[0]);
   top2_init(loc[1]);
-  const int gq = lane >> 2, tq = lane & 3;   // mma fragment coordinates
-  float rstd = 1.f;                          // single-vector path: 1/rms of the group's input
-  int last_g = -1;
-  for (int g = gbeg, r = rbeg; g < gend || (g == gend && r < rend);) {
-    const GG& G = gg[g];
-    const int last = (g == gend) ? rend : G.rows;
-    const int tr = min((int)G.tr, last - r);
-    if (g != last_g) {  // group entry: 1/rms of the input vector(s)
-      named_bar(1, NCT);
-      rstd = 1.f;
-      if (!G.mma) {
-        if (G.normw) {
-          const float* xr = G.x + (size_t)(G.xrow0 % G.xring) * G.xstride;
-          float sq = 0.f;
-          for (int c = tid * 4; c < G.cols; c += NCT * 4) {
-            const float4 q = *reinterpret_cast<const float4*>(xr + c);
-            sq += q.x * q.x; sq += q.y * q.y; sq += q.z * q.z; sq += q.w * q.w;
-          }
-          sq = warp_sum(sq);
-          if (lane == 0) wpart[warp] = sq;
-          named_bar(1, NCT);
-          float tot = 0.f;
-#pragma unroll
-          for (int w8 = 0; w8 < kNCW; ++w8) tot += wpart[w8];
-          rstd = 1.0f / sqrtf(tot / (float)G.cols + p.eps);
-        }
-      } else if (G.normw) {
-        for (int v = warp; v < G.nv; v += kNCW) {
-          const float* xr = G.x + (size_t)((G.xrow0 + v) % G.xring) * G.xstride;
-          float sq = 0.f;
-          for (int c = lane * 4; c < G.cols; c += 128) {
-            const float4 q = *reinterpret_cast<const float4*>(xr + c);
-            sq += q.x * q.x; sq += q.y * q.y; sq += q.z * q.z; sq += q.w * q.w;
-          }
-          sq = warp_sum(sq);
-          if (lane == 0) rstd_s[v] = 1.0f / sqrtf(sq / (float)G.cols + p.eps);
-        }
-      }
-      named_bar(1, NCT);
-      last_g = g;
-    }
-    if (!G.mma) {
-      // ---------------- single-vector path ----------------
-      const float* xr = G.x + (size_t)(G.xrow0 % G.xring) * G.xstride;
-      float acc[8];
-#pragma unroll
-      for (int i = 0; i < 8; ++i) acc[i] = 0.f;
-      for (int c0 = 0; c0 < G.cols; c0 += CW) {
-        const int s = ctr % kStages;
-        if (!failed && !mbar_wait_bounded(&full_bar[s], (ctr / kStages) & 1)) {
-          if (lane == 0) set_err(st, ERR_TIMEOUT, 50);
-          failed = true;
-        }
-        if (!failed) {
-          const int col = c0 + VEC * lane;
-          float xv[VEC];
-          if (col < G.cols) {
-#pragma unroll
-            for (int e = 0; e < VEC; e += 4) {
-              float4 q = *reinterpret_cast<const float4*>(xr + col + e);
-              if (G.normw) {
-                const float4 n4 = *reinterpret_cast<const float4*>(G.normw + col + e);
-                q.x = q.x * rstd * n4.x; q.y = q.y * rstd * n4.y;
-                q.z = q.z * rstd * n4.z; q.w = q.w * rstd * n4.w;
-              }
-              xv[e] = q.x; xv[e + 1] = q.y; xv[e + 2] = q.z; xv[e + 3] = q.w;
-            }
-          } else {
-#pragma unroll
-            for (int e = 0; e < VEC; ++e) xv[e] = 0.f;
-          }
-          const unsigned char* sb = ring + (size_t)s * kStageBytes;
-#pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            const int slot = warp + 8 * i;
-            const bool ok = G.nw == 2 ? ((slot & 31) < tr) : (slot < tr);
-            if (ok) {
-              float wf[VEC];
-              WTraits<WT>::unpack(*reinterpret_cast<const uint4*>(sb + stage_off(slot, lane)), wf);
-#pragma unroll
-              for (int e = 0; e < VEC; ++e) acc[i] = fmaf(wf[e], xv[e], acc[i]);
-            }
-          }
-        }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&empty_bar[s]);
-        ++ctr;
-      }
-      float sums[8];
-#pragma unroll
-      for (int i = 0; i < 8; ++i) sums[i] = warp_sum(acc[i]);
-      if (!failed && lane < 8) {  // lane i finishes slot warp + 8i (and its partner slot + 32)
-        float y0 = 0.f, y1 = 0.f;
-#pragma unroll
-        for (int k = 0; k < 8; ++k) {
-          if (k == lane) y0 = sums[k];
-          if (k == lane + 4) y1 = sums[k];
-        }
-        const int slot = warp + 8 * lane;
-        if (G.nw == 2) {
-          if (lane < 4 && slot < tr) epilogue<WT>(p, G, 0, r + slot, y0, y1, false, loc);
-        } else if (G.epi == EPI_QKV && r < G.seg2) {
-          if (lane < 4) epilogue<WT>(p, G, 0, phys_row(G, r + slot, hd), y0, y1, true, loc);
-        } else if (slot < tr) {
-          epilogue<WT>(p, G, 0, r + slot, y0, 0.f, false, loc);
-        }
-      }
-    } else {
-      // ---------------- tensor-core path (bf16 weights, several vectors) ----------------
-      const int nv = G.nv;
-      const int MT = (nv + 15) / 16;
-      float acc[kMaxMT][8][4];
-#pragma unroll
-      for (int i = 0; i < kMaxMT; ++i)
-#pragma unroll
-        for (int j = 0; j < 8; ++j)
-#pragma unroll
-          for (int e = 0; e < 4; ++e) acc[i][j][e] = 0.f;
-      // activation pair (k, k+1) of vector v, normalised, 0 outside the matrix
-      auto ldx = [&](int v, int k) -> float2 {
-        float2 q = make_float2(0.f, 0.f);
-        if (v < nv && k < G.cols) {
-          q = *reinterpret_cast<const float2*>(G.x + (size_t)((G.xrow0 + v) % G.xring) * G.xstride + k);
-          if (G.normw) {
-            const float2 n2 = *reinterpret_cast<const float2*>(G.normw + k);
-            const float rs = rstd_s[v];
-            q.x = q.x * rs * n2.x; q.y = q.y * rs * n2.y;
-          }
-        }
-        return q;
-      };
-      const int kb = warp * 32;                 // this warp's 32 columns of each stage
-      const int jb = (kb >> 3) + (lane >> 3);   // its ldmatrix chunk (0..31)
-      for (int c0 = 0; c0 < G.cols; c0 += CW) {
-        const int s = ctr % kStages;
-        if (!failed && !mbar_wait_bounded(&full_bar[s], (ctr / kStages) & 1)) {
-          if (lane == 0) set_err(st, ERR_TIMEOUT, 60);
-          failed = true;
-        }
-        if (!failed) {
-          uint32_t ah[kMaxMT][2][4], al[kMaxMT][2][4];
-#pragma unroll
-          for (int mt = 0; mt < kMaxMT; ++mt) {
-            if (mt < MT) {
-#pragma unroll
-              for (int ks = 0; ks < 2; ++ks) {
-                const int k = c0 + kb + 16 * ks + 2 * tq;
-                const int v0 = mt * 16 + gq;
-                const float2 q[4] = {ldx(v0, k), ldx(v0 + 8, k), ldx(v0, k + 8), ldx(v0 + 8, k + 8)};
-#pragma unroll
-                for (int f = 0; f < 4; ++f) {
-                  const __nv_bfloat16 hx = __float2bfloat16_rn(q[f].x), hy = __float2bfloat16_rn(q[f].y);
-                  const float fx = __bfloat162float(hx), fy = __bfloat162float(hy);
-                  ah[mt][ks][f] = pack_bf16x2(fx, fy);
-                  al[mt][ks][f] = pack_bf16x2(q[f].x - fx, q[f].y - fy);
-                }
-              }
-            }
-          }
-          const uint32_t sb = smem_u32(ring + (size_t)s * kStageBytes);
-#pragma unroll
-          for (int nt = 0; nt < 8; ++nt) {
-            const bool ok = G.nw == 2 ? (((nt * 8) & 31) < tr) : (nt * 8 < tr);
-            if (ok) {
-              uint32_t b0, b1, b2, b3;
-              ldmatrix_x4(sb + stage_off(nt * 8 + (lane & 7), jb), b0, b1, b2, b3);
-#pragma unroll
-              for (int mt = 0; mt < kMaxMT; ++mt) {
-                if (mt < MT) {
-                  mma_bf16(acc[mt][nt], ah[mt][0], b0, b1);
-                  mma_bf16(acc[mt][nt], al[mt][0], b0, b1);
-                  mma_bf16(acc[mt][nt], ah[mt][1], b2, b3);
-                  mma_bf16(acc[mt][nt], al[mt][1], b2, b3);
-                }
-              }
-            }
-          }
-        }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&empty_bar[s]);
-        ++ctr;
-      }
-      // per m-tile: the 8 warps' partial tiles -> shared memory, added in warp order
-#pragma unroll
-      for (int mt = 0; mt < kMaxMT; ++mt) {
-        if (mt < MT) {
-#pragma unroll
-          for (int nt = 0; nt < 8; ++nt)
-#pragma unroll
-            for (int e = 0; e < 4; ++e) red[((warp * 8 + nt) * 4 + e) * 32 + lane] = acc[mt][nt][e];
-          named_bar(1, NCT);
-          auto tot = [&](int slot, int vv) {
-            const int nt = slot >> 3, n = slot & 7;
-            const int ln = (vv & 7) * 4 + (n >> 1);
-            const int e = (vv >= 8 ? 2 : 0) + (n & 1);
-            float sum = 0.f;
-#pragma unroll
-            for (int w8 = 0; w8 < kNCW; ++w8) sum += red[((w8 * 8 + nt) * 4 + e) * 32 + ln];
-            return sum;
-          };
-          if (!failed) {
-            if (G.nw == 2 || (G.epi == EPI_QKV && r < G.seg2)) {  // gate/up, or rotary pairs
-              const bool pair = G.nw != 2;
-              for (int idx = tid; idx < 32 * 16; idx += NCT) {
-                const int m = idx >> 4, vv = idx & 15, v = mt * 16 + vv;
-                if (v < nv && m < tr)
-                  epilogue<WT>(p, G, v, pair ? phys_row(G, r + m, hd) : r + m, tot(m, vv), tot(m + 32, vv),
-                               pair, loc);
-              }
-            } else {
-              for (int idx = tid; idx < 64 * 16; idx += NCT) {
-                const int m = idx >> 4, vv = idx & 15, v = mt * 16 + vv;
-                if (v < nv && m < tr) epilogue<WT>(p, G, v, r + m, tot(m, vv), 0.f, false, loc);
-              }
-            }
-          }
-          named_bar(1, NCT);  // `red` is rewritten next
-        }
-      }
-    }
-    r += tr;
-    if (r >= last) { ++g; r = 0; }
-  }
-  // head: per-CTA top-2 of each kind (the order of the merge does not change a top-2)
+  consume_span<WT>(p.cfg, gg, s_gb, s_rb, s_ge, s_re, R, scratch, rstd_s, wpart, loc);
   bool head = false;
   for (int i = 0; i < ng; ++i) head |= gg[i].epi == EPI_TOP2;
-  if (head || (ng == 0 && p.nparts > 0 && p.part[0].op == OP_HEAD)) {
-    if (lane < 8) { hred[warp * 8 + lane][0] = loc[0]; hred[warp * 8 + lane][1] = loc[1]; }
-    named_bar(1, NCT);
-    if (tid == 0) {
-      float* hp = p.B.head_part + (size_t)blockIdx.x * 8;
-      for (int k = 0; k < 2; ++k) {
-        Top2 m = hred[0][k];
-        for (int i = 1; i < kNCW * 8; ++i) top2_merge(m, hred[i][k]);
-        hp[k * 4 + 0] = m.v1; hp[k * 4 + 1] = __int_as_float(m.i1);
-        hp[k * 4 + 2] = m.v2; hp[k * 4 + 3] = __int_as_float(m.i2);
-      }
-    }
-  }
+  if (head || (ng == 0 && p.nparts > 0 && p.part[0].op == OP_HEAD))
+    write_head_partial(loc, hred, p.cfg.B.head_part + (size_t)blockIdx.x * 8);
 }
 
 template <typename WT>
@@ -741,7 +81,7 @@ cudaError_t launch_engine(const GemvParams& p, bool pdl, cudaStream_t s) {
   memset(&cfg, 0, sizeof(cfg));
   cfg.gridDim = dim3(num_sms());
   cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = kDynSmem;
+  cfg.dynamicSmemBytes = kGemvSmem;
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -771,10 +111,10 @@ int gemv_head_grid(int dtype) {
 
 cudaError_t gemv_setup_attributes() {
   cudaError_t e = cudaFuncSetAttribute(gemv_engine<float>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       kDynSmem);
+                                       kGemvSmem);
   if (e != cudaSuccess) return e;
   return cudaFuncSetAttribute(gemv_engine<__nv_bfloat16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              kDynSmem);
+                              kGemvSmem);
 }
 
 cudaError_t launch_gemv(const GemvPart* parts, int nparts, const Dims& D, const Bufs& B,
@@ -785,19 +125,19 @@ cudaError_t launch_gemv(const GemvPart* parts, int nparts, const Dims& D, const 
   for (int i = 0; i < nparts && i < 2; ++i) p.part[i] = parts[i];
   p.explicit_mode = 0;
   p.resolve_after_wait = resolve_after_wait ? 1 : 0;
-  p.debug_logits = cfg.debug_logits;
-  p.has_mma = D.dtype == SPD_DTYPE_BF16;
-  p.eps = D.eps;
-  p.D = D; p.B = B;
+  p.cfg.debug_logits = cfg.debug_logits;
+  p.cfg.has_mma = D.dtype == SPD_DTYPE_BF16;
+  p.cfg.eps = D.eps;
+  p.cfg.D = D; p.cfg.B = B;
   return D.dtype == SPD_DTYPE_BF16 ? launch_engine<__nv_bfloat16>(p, pdl, s) : launch_engine<float>(p, pdl, s);
 }
 
 cudaError_t launch_gemv_explicit(const GemvExplicit& ge, int dtype, float eps, cudaStream_t s) {
   GemvParams p;
   memset(&p, 0, sizeof(p));
-  p.explicit_mode = 1; p.resolve_after_wait = 1; p.eps = eps; p.ge = ge;
-  p.has_mma = 0;
-  p.D.dtype = dtype; p.D.eps = eps;
+  p.explicit_mode = 1; p.resolve_after_wait = 1; p.ge = ge;
+  p.cfg.eps = eps; p.cfg.has_mma = 0;
+  p.cfg.D.dtype = dtype; p.cfg.D.eps = eps;
   return dtype == SPD_DTYPE_BF16 ? launch_engine<__nv_bfloat16>(p, false, s) : launch_engine<float>(p, false, s);
 }
 

@@ -299,6 +299,25 @@ struct GemvPart {
   Launch lc;
 };
 
+// ---- persistent step kernel: one cooperative launch runs a program of phases ----
+enum PhaseType { PH_GEMV = 0, PH_ATTN = 1, PH_CTRL_CYCLE = 2, PH_CTRL_AR = 3 };
+struct Phase {
+  int type;        // PhaseType
+  int kind;        // kernel kind charged with the phase's time (KK_*, +9 for draft-only phases)
+  int nparts;      // GEMV / attention parts (target rows, draft rows)
+  GemvPart part[2];
+};
+constexpr int kStepChunk = 64;   // attention keys per split inside the step kernel
+
+// Dynamic shared memory the step kernel needs for this model (0: it does not fit on one SM).
+size_t step_smem_bytes(const Dims& D);
+cudaError_t step_setup_attributes(size_t smem);
+// One cooperative launch (one CTA per SM) running `prog[0..nphases)`.  `bar` = 2 words of grid
+// barrier state (zero-initialised), `phase_ns` = per-phase accumulated nanoseconds (or null).
+cudaError_t launch_step(const Dims& D, const Bufs& B, const LaunchCfg& cfg, const Phase* prog,
+                        int nphases, unsigned* bar, unsigned long long* phase_ns, size_t smem,
+                        cudaStream_t s);
+
 // pdl: launch with programmatic stream serialisation (the kernel may start before its predecessor
 // ends; it waits with griddepcontrol.wait before touching activations).  resolve_after_wait: the
 // predecessor may have written the control block, so the rows are resolved after that wait.
@@ -308,7 +327,7 @@ cudaError_t launch_gemv_explicit(const GemvExplicit& ge, int dtype, float eps, c
 cudaError_t launch_attn(const Dims& D, const Bufs& B, const Launch& lc, const LaunchCfg& cfg,
                         bool pdl, cudaStream_t s);
 size_t attn_smem_bytes(const Dims& D, bool multi);
-size_t attn_part_floats(int rows, int hq, int hd, int max_seq);
+size_t attn_part_floats(int rows, int hq, int hd, int max_seq, int ck = kAttnChunk);
 cudaError_t gemv_setup_attributes();
 // Encodes the tensor map the GEMV engine streams a row-major [rows, cols] weight matrix with
 // (boxes of 128 bytes x 32 rows, 128-byte swizzle).  Host call; returns a CUDA error code.
