@@ -31,7 +31,7 @@ struct Tile {
 
 // Appends the tiles of one part (a launch descriptor; rows of up to `qt` queries per tile).
 static __device__ int add_tiles(const Dims& D, const Bufs& B, const Launch& lc, int qt, int ck, Tile* tiles,
-                         int nt, int* items) {
+                         int nt, int* items, int cap = kMaxTiles) {
   DevState* st = B.st;
   RowGroup rg[kMaxGroups];
   int nr;
@@ -48,7 +48,7 @@ static __device__ int add_tiles(const Dims& D, const Bufs& B, const Launch& lc, 
   int rec = 0, local = 0;
   for (int i = 0; i < nr; ++i) {
     for (int r0 = 0; r0 < rg[i].nv; r0 += qt) {
-      if (nt >= kMaxTiles) { set_err(st, ERR_BOUNDS, 400); return -1; }
+      if (nt >= cap) { set_err(st, ERR_BOUNDS, 400); return -1; }
       Tile& T = tiles[nt++];
       T.layer = rg[i].layer;
       T.nq = min(qt, rg[i].nv - r0);
@@ -81,51 +81,187 @@ __host__ __device__ inline size_t smem_bytes(int hd, int gq, int esz, int qt, in
   return (size_t)2 * ck * hd * esz + (size_t)qh * hd * 4 + (size_t)qh * ck * 4 + (size_t)2 * qh * 4;
 }
 
-// Runs items item0, item0 + step, ... of the tiles on the 256 calling threads (threadIdx.x < 256).
-// `sm` (smem_bytes) and `kv_bar` (an initialised mbarrier, parity `phase`) belong to the caller;
-// `fail` is a shared flag.  Returns false if a bounded wait gave up.
+// Geometry of work item `item`: tile T, kv head kh, key chunk c of `ck` keys (nk of them).
+struct Item {
+  int T, kh, c, nk;
+};
+__device__ __forceinline__ Item item_of(const Tile* tiles, int nt, int item, int ck) {
+  Item it;
+  it.T = 0;
+  while (it.T + 1 < nt && tiles[it.T + 1].item_off <= item) ++it.T;
+  const Tile& Ti = tiles[it.T];
+  const int rem = item - Ti.item_off;
+  it.kh = rem / Ti.nch;
+  it.c = rem % Ti.nch;
+  const int pos_last = Ti.pos0 + Ti.nq - 1;
+  it.nk = min(ck, pos_last - it.c * ck);
+  return it;
+}
+
+// True if chunk c of tile Ti holds a key the QKV step of this cycle appended (key pos0-1 onward).
+__device__ __forceinline__ bool chunk_is_new(const Tile& Ti, int c, int ck) { return c >= (Ti.pos0 - 1) / ck; }
+
+// One item on the 256 calling threads, its K and V chunks already in shared memory (ks, vs:
+// [nk][hd] in the cache dtype): queries -> qs, scores, per-chunk softmax, unnormalised partial
+// (o, m, l) to global scratch, and -- for the last item of its (tile, kv head) to finish, by an
+// atomic ticket -- the merge of the partials in chunk order.  Named barrier 2.
 template <typename WT, int CK>
-static __device__ bool run_items(const Dims& D, DevState* st, const Tile* tiles, int nt, int n_items, int item0,
-                          int step, int qh_max, unsigned char* sm, uint64_t* kv_bar, uint32_t& phase,
-                          int* fail, int* last_flag) {
-  constexpr int ESZ = sizeof(WT);
+__device__ void item_compute(const Dims& D, const Tile& Ti, const Item& it, const WT* ks, const WT* vs, float* qs,
+                             float* sc, float* m_s, float* l_s, int* last_flag) {
   const int hd = D.hd, GQ = D.gq;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const float scale = 1.0f / sqrtf((float)hd);
+  const int qkv_rows = D.qkv_rows;
+  const int hqd = D.hq * hd;
+  const int LPK = hd / 16;  // lanes per key
+  const int KPW = 32 / LPK;
+  const int kh = it.kh, c = it.c, nk = it.nk;
+  const int QH = Ti.nq * GQ;
+  const int key0 = c * CK;
+  // queries (already rotated) -> shared memory
+  for (int idx = tid; idx < QH * hd; idx += kThreads) {
+    const int qh = idx / hd, e = idx % hd;
+    const int r = qh / GQ, hg = qh % GQ;
+    qs[idx] = Ti.q[(size_t)(Ti.vid0 + r) * qkv_rows + (kh * GQ + hg) * hd + e];
+  }
+  named_bar(2, kThreads);
+  // scores
+  {
+    const int kl = lane / LPK, sub = lane % LPK;
+    for (int kb = warp * KPW; kb < CK; kb += 8 * KPW) {
+      const int kk = kb + kl;
+      float kf[16];
+      if (kk < nk) {
+        const WT* kr = ks + (size_t)kk * hd + sub * 16;
+#pragma unroll
+        for (int e = 0; e < 16; e += 16 / (int)sizeof(WT)) {
+          const uint4 q4 = *reinterpret_cast<const uint4*>(kr + e);
+          WTraits<WT>::unpack(q4, kf + e);
+        }
+      } else {
+#pragma unroll
+        for (int e = 0; e < 16; ++e) kf[e] = 0.f;
+      }
+      for (int qh = 0; qh < QH; ++qh) {
+        const float* qv = qs + (size_t)qh * hd + sub * 16;
+        float dot = 0.f;
+#pragma unroll
+        for (int e = 0; e < 16; e += 4) {
+          const float4 q4 = *reinterpret_cast<const float4*>(qv + e);
+          dot = fmaf(kf[e], q4.x, dot);
+          dot = fmaf(kf[e + 1], q4.y, dot);
+          dot = fmaf(kf[e + 2], q4.z, dot);
+          dot = fmaf(kf[e + 3], q4.w, dot);
+        }
+        for (int o = LPK / 2; o > 0; o >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, o);
+        if (sub == 0 && kk < nk) {
+          const int pos_q = Ti.pos0 + qh / GQ;
+          sc[(size_t)qh * CK + kk] = (key0 + kk < pos_q) ? dot * scale : -INFINITY;
+        }
+      }
+    }
+  }
+  named_bar(2, kThreads);
+  // per-chunk softmax statistics, one warp per query head
+  for (int qh = warp; qh < QH; qh += 8) {
+    float* srow = sc + (size_t)qh * CK;
+    float m = -INFINITY;
+    for (int k = lane; k < nk; k += 32) m = fmaxf(m, srow[k]);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+    float l = 0.f;
+    for (int k = lane; k < nk; k += 32) {
+      const float pk = (m == -INFINITY) ? 0.f : expf(srow[k] - m);
+      srow[k] = pk;
+      l += pk;
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) l += __shfl_xor_sync(0xffffffffu, l, o);
+    if (lane == 0) { m_s[qh] = m; l_s[qh] = l; }
+  }
+  named_bar(2, kThreads);
+  // unnormalised chunk output -> partial record (o[hd], m, l).  With at most 128 outputs the
+  // keys are split between the two thread halves (lower half first, then added in that order).
+  const int nout = QH * hd;
+  const bool split = 2 * nout <= kThreads;
+  float* oh = qs;  // the queries are dead once the scores exist: scratch for the upper half
+  for (int idx = tid; idx < (split ? 2 * nout : nout); idx += kThreads) {
+    const int half = split ? idx / nout : 0;
+    const int o_i = split ? idx % nout : idx;
+    const int qh = o_i / hd, e = o_i % hd;
+    const float* prow = sc + (size_t)qh * CK;
+    const int k0 = split ? (half ? nk / 2 : 0) : 0;
+    const int k1 = split ? (half ? nk : nk / 2) : nk;
+    float o = 0.f;
+    for (int k = k0; k < k1; ++k) o = fmaf(prow[k], WTraits<WT>::to_f(vs[(size_t)k * hd + e]), o);
+    if (split && half) oh[o_i] = o;
+    if (split) named_bar(3, kThreads);  // every thread reaches it once (2 * nout <= kThreads)
+    if (!(split && half)) {
+      if (split) o += oh[o_i];
+      float* rec = Ti.part + ((size_t)Ti.rec_off + ((size_t)kh * Ti.nch + c) * QH + qh) * (hd + 2);
+      rec[e] = o;
+      if (e == 0) { rec[hd] = m_s[qh]; rec[hd + 1] = l_s[qh]; }
+    }
+  }
+  if (split && tid >= 2 * nout) named_bar(3, kThreads);  // threads without an output item
+  __threadfence();
+  named_bar(2, kThreads);
+  if (tid == 0) {
+    const int old = atomicAdd(&Ti.tick[Ti.tick_off + kh], 1);
+    *last_flag = (old == Ti.nch - 1);
+  }
+  named_bar(2, kThreads);
+  if (*last_flag) {
+    __threadfence();
+    // merge this (tile, kv head): each query over its own chunks, in chunk order
+    for (int idx = tid; idx < QH * hd; idx += kThreads) {
+      const int qh = idx / hd, e = idx % hd;
+      const int r = qh / GQ, hg = qh % GQ;
+      const int nc = (Ti.pos0 + r + CK - 1) / CK;
+      const float* base = Ti.part + ((size_t)Ti.rec_off + (size_t)kh * Ti.nch * QH + qh) * (hd + 2);
+      const size_t cstride = (size_t)QH * (hd + 2);
+      float M = -INFINITY;
+      for (int cc = 0; cc < nc; ++cc) M = fmaxf(M, __ldcg(base + cc * cstride + hd));
+      float Ls = 0.f, O = 0.f;
+      for (int cc = 0; cc < nc; ++cc) {
+        const float* rc = base + cc * cstride;
+        const float w = expf(__ldcg(rc + hd) - M);
+        Ls = fmaf(__ldcg(rc + hd + 1), w, Ls);
+        O = fmaf(__ldcg(rc + e), w, O);
+      }
+      Ti.out[(size_t)(Ti.vid0 + r) * hqd + (kh * GQ + hg) * hd + e] = O / Ls;
+    }
+    if (tid == 0) Ti.tick[Ti.tick_off + kh] = 0;
+  }
+  named_bar(2, kThreads);  // shared buffers are reused by the next item
+}
+
+// Runs items item0, item0 + step, ... of the tiles on the 256 calling threads (threadIdx.x < 256),
+// loading each item's K/V chunk itself.  `sm` (smem_bytes) and `kv_bar` (an initialised mbarrier,
+// parity `phase`) belong to the caller; `fail` is a shared flag.  False if a bounded wait gave up.
+template <typename WT, int CK>
+static __device__ bool run_items(const Dims& D, DevState* st, const Tile* tiles, int nt, int n_items, int item0,
+                                 int step, int qh_max, unsigned char* sm, uint64_t* kv_bar, uint32_t& phase,
+                                 int* fail, int* last_flag) {
+  constexpr int ESZ = sizeof(WT);
+  const int hd = D.hd;
+  const int tid = threadIdx.x;
   WT* ks = reinterpret_cast<WT*>(sm);
   WT* vs = reinterpret_cast<WT*>(sm + (size_t)CK * hd * ESZ);
   float* qs = reinterpret_cast<float*>(sm + (size_t)2 * CK * hd * ESZ);
   float* sc = qs + (size_t)qh_max * hd;
   float* m_s = sc + (size_t)qh_max * CK;
   float* l_s = m_s + qh_max;
-  const float scale = 1.0f / sqrtf((float)hd);
-  const int qkv_rows = D.qkv_rows;
-  const int hqd = D.hq * hd;
-  const int LPK = hd / 16;  // lanes per key
-  const int KPW = 32 / LPK;
   for (int item = item0; item < n_items; item += step) {
-    int T = 0;
-    while (T + 1 < nt && tiles[T + 1].item_off <= item) ++T;
-    const Tile& Ti = tiles[T];
-    const int rem = item - Ti.item_off;
-    const int kh = rem / Ti.nch, c = rem % Ti.nch;
-    const int QH = Ti.nq * GQ;
-    const int pos_last = Ti.pos0 + Ti.nq - 1;
-    const int key0 = c * CK;
-    const int nk = min(CK, pos_last - key0);
-    // K/V chunk -> shared memory (one bulk copy each)
-    if (tid == 0) {
-      const uint32_t bytes = (uint32_t)nk * hd * ESZ;
-      const size_t off = ((size_t)kh * D.max_seq + key0) * hd * ESZ;
+    const Item it = item_of(tiles, nt, item, CK);
+    const Tile& Ti = tiles[it.T];
+    if (tid == 0) {  // K/V chunk -> shared memory (one bulk copy each)
+      const uint32_t bytes = (uint32_t)it.nk * hd * ESZ;
+      const size_t off = ((size_t)it.kh * D.max_seq + it.c * CK) * hd * ESZ;
       mbar_arrive_expect_tx(kv_bar, 2 * bytes);
       const uint64_t pol = l2_evict_first_policy();
       bulk_g2s(ks, Ti.kc + off, bytes, kv_bar, pol);
       bulk_g2s(vs, Ti.vc + off, bytes, kv_bar, pol);
-    }
-    // queries (already rotated) -> shared memory
-    for (int idx = tid; idx < QH * hd; idx += kThreads) {
-      const int qh = idx / hd, e = idx % hd;
-      const int r = qh / GQ, hg = qh % GQ;
-      qs[idx] = Ti.q[(size_t)(Ti.vid0 + r) * qkv_rows + (kh * GQ + hg) * hd + e];
     }
     if (!mbar_wait_bounded(kv_bar, phase)) *fail = 1;
     phase ^= 1;
@@ -137,115 +273,7 @@ static __device__ bool run_items(const Dims& D, DevState* st, const Tile* tiles,
       }
       return false;
     }
-    // scores
-    {
-      const int kl = lane / LPK, sub = lane % LPK;
-      for (int kb = warp * KPW; kb < CK; kb += 8 * KPW) {
-        const int kk = kb + kl;
-        float kf[16];
-        if (kk < nk) {
-          const WT* kr = ks + (size_t)kk * hd + sub * 16;
-#pragma unroll
-          for (int e = 0; e < 16; e += 16 / ESZ) {
-            const uint4 q4 = *reinterpret_cast<const uint4*>(kr + e);
-            WTraits<WT>::unpack(q4, kf + e);
-          }
-        } else {
-#pragma unroll
-          for (int e = 0; e < 16; ++e) kf[e] = 0.f;
-        }
-        for (int qh = 0; qh < QH; ++qh) {
-          const float* qv = qs + (size_t)qh * hd + sub * 16;
-          float dot = 0.f;
-#pragma unroll
-          for (int e = 0; e < 16; e += 4) {
-            const float4 q4 = *reinterpret_cast<const float4*>(qv + e);
-            dot = fmaf(kf[e], q4.x, dot);
-            dot = fmaf(kf[e + 1], q4.y, dot);
-            dot = fmaf(kf[e + 2], q4.z, dot);
-            dot = fmaf(kf[e + 3], q4.w, dot);
-          }
-          for (int o = LPK / 2; o > 0; o >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, o);
-          if (sub == 0 && kk < nk) {
-            const int pos_q = Ti.pos0 + qh / GQ;
-            sc[(size_t)qh * CK + kk] = (key0 + kk < pos_q) ? dot * scale : -INFINITY;
-          }
-        }
-      }
-    }
-    named_bar(2, kThreads);
-    // per-chunk softmax statistics, one warp per query head
-    for (int qh = warp; qh < QH; qh += 8) {
-      float* srow = sc + (size_t)qh * CK;
-      float m = -INFINITY;
-      for (int k = lane; k < nk; k += 32) m = fmaxf(m, srow[k]);
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-      float l = 0.f;
-      for (int k = lane; k < nk; k += 32) {
-        const float pk = (m == -INFINITY) ? 0.f : expf(srow[k] - m);
-        srow[k] = pk;
-        l += pk;
-      }
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) l += __shfl_xor_sync(0xffffffffu, l, o);
-      if (lane == 0) { m_s[qh] = m; l_s[qh] = l; }
-    }
-    named_bar(2, kThreads);
-    // unnormalised chunk output -> partial record (o[hd], m, l).  With at most 128 outputs the
-    // keys are split between the two thread halves (lower half first, then added in that order).
-    const int nout = QH * hd;
-    const bool split = 2 * nout <= kThreads;
-    float* oh = qs;  // the queries are dead once the scores exist: scratch for the upper half
-    for (int idx = tid; idx < (split ? 2 * nout : nout); idx += kThreads) {
-      const int half = split ? idx / nout : 0;
-      const int o_i = split ? idx % nout : idx;
-      const int qh = o_i / hd, e = o_i % hd;
-      const float* prow = sc + (size_t)qh * CK;
-      const int k0 = split ? (half ? nk / 2 : 0) : 0;
-      const int k1 = split ? (half ? nk : nk / 2) : nk;
-      float o = 0.f;
-      for (int k = k0; k < k1; ++k) o = fmaf(prow[k], WTraits<WT>::to_f(vs[(size_t)k * hd + e]), o);
-      if (split && half) oh[o_i] = o;
-      if (split) named_bar(3, kThreads);  // every thread reaches it once (2 * nout <= kThreads)
-      if (!(split && half)) {
-        if (split) o += oh[o_i];
-        float* rec = Ti.part + ((size_t)Ti.rec_off + ((size_t)kh * Ti.nch + c) * QH + qh) * (hd + 2);
-        rec[e] = o;
-        if (e == 0) { rec[hd] = m_s[qh]; rec[hd + 1] = l_s[qh]; }
-      }
-    }
-    if (split && tid >= 2 * nout) named_bar(3, kThreads);  // threads without an output item
-    __threadfence();
-    named_bar(2, kThreads);
-    if (tid == 0) {
-      const int old = atomicAdd(&Ti.tick[Ti.tick_off + kh], 1);
-      *last_flag = (old == Ti.nch - 1);
-    }
-    named_bar(2, kThreads);
-    if (*last_flag) {
-      __threadfence();
-      // merge this (tile, kv head): each query over its own chunks, in chunk order
-      for (int idx = tid; idx < QH * hd; idx += kThreads) {
-        const int qh = idx / hd, e = idx % hd;
-        const int r = qh / GQ, hg = qh % GQ;
-        const int nc = (Ti.pos0 + r + CK - 1) / CK;
-        const float* base = Ti.part + ((size_t)Ti.rec_off + (size_t)kh * Ti.nch * QH + qh) * (hd + 2);
-        const size_t cstride = (size_t)QH * (hd + 2);
-        float M = -INFINITY;
-        for (int cc = 0; cc < nc; ++cc) M = fmaxf(M, __ldcg(base + cc * cstride + hd));
-        float Ls = 0.f, O = 0.f;
-        for (int cc = 0; cc < nc; ++cc) {
-          const float* rc = base + cc * cstride;
-          const float w = expf(__ldcg(rc + hd) - M);
-          Ls = fmaf(__ldcg(rc + hd + 1), w, Ls);
-          O = fmaf(__ldcg(rc + e), w, O);
-        }
-        Ti.out[(size_t)(Ti.vid0 + r) * hqd + (kh * GQ + hg) * hd + e] = O / Ls;
-      }
-      if (tid == 0) Ti.tick[Ti.tick_off + kh] = 0;
-    }
-    named_bar(2, kThreads);  // shared buffers are reused by the next item
+    item_compute<WT, CK>(D, Ti, it, ks, vs, qs, sc, m_s, l_s, last_flag);
   }
   return true;
 }

@@ -2,7 +2,9 @@
 //
 // One CTA per SM runs a program of phases (SPD summary 方法步骤详情 steps 1-5 for a cycle):
 //   GEMV   the grouped GEMV engine over this CTA's share of the phase's weight bytes
-//   ATTN   decode attention items (tile, kv head, 64-key chunk), CTA-strided
+//   ATTN   decode attention items (tile, kv head, 64-key chunk), CTA-strided; the producer streams
+//          their K/V chunks through the same ring (chunks of earlier cycles before the QKV phase's
+//          barrier, the chunks holding this cycle's keys after it)
 //   CTRL   verify / accept / rollback / reseed on CTA 0 (the last phase)
 // Consecutive phases are separated by a grid barrier of the consumer warps.  The producer warp
 // does not take part in the barriers: the weights of every GEMV phase are known when the cycle
@@ -25,6 +27,8 @@ namespace {
 using namespace eng;
 
 constexpr int kStepGroups = 36;   // groups of one phase: n target + n+1 draft rows (n <= 16)
+constexpr int kStepTiles = 24;    // attention tiles of one phase: n target tiles + draft-row tiles
+constexpr int kKVHalf = kStageBytes / 2;  // an attention item's ring stage: K chunk | V chunk
 
 struct StepParams {
   EngineCfg cfg;
@@ -92,11 +96,11 @@ __global__ void __launch_bounds__(kThreads, 1) step_kernel(const __grid_constant
   unsigned char* uni = ring + kStages * kStageBytes;
   GG* gg_c = reinterpret_cast<GG*>(uni + p.union_bytes);  // consumers: 2 tables (this / next phase)
   GG* gg_p = gg_c + 2 * kStepGroups;                       // producer
-  att::Tile* tiles = reinterpret_cast<att::Tile*>(gg_p + kStepGroups);
+  att::Tile* tiles = reinterpret_cast<att::Tile*>(gg_p + kStepGroups);  // consumers
+  att::Tile* tiles_p = tiles + kStepTiles;                                 // producer
 
   __shared__ __align__(8) uint64_t full_bar[kStages];
   __shared__ __align__(8) uint64_t empty_bar[kStages];
-  __shared__ __align__(8) uint64_t kv_bar;
   __shared__ int s_ng[2], s_gb[2], s_rb[2], s_ge[2], s_re[2];
   __shared__ int s_skip, s_nt, s_items, s_fail, s_last, s_tok, s_slot, s_ok;
   __shared__ float rstd_s[16 * kMaxMT];
@@ -112,7 +116,6 @@ __global__ void __launch_bounds__(kThreads, 1) step_kernel(const __grid_constant
       mbar_init(&full_bar[i], 1);
       mbar_init(&empty_bar[i], kNCW);
     }
-    mbar_init(&kv_bar, 1);
     fence_mbar_init();
     s_skip = (st->done || st->err) ? 1 : 0;
   }
@@ -123,19 +126,72 @@ __global__ void __launch_bounds__(kThreads, 1) step_kernel(const __grid_constant
   if (warp == kNCW) {
     // ------------------------------ producer warp ------------------------------
     const uint64_t pol = l2_evict_first_policy();
+    // grid barriers completed before phase ph = ph; the generation word counts them
+    const unsigned g_start = __shfl_sync(0xffffffffu, lane == 0 ? ld_acquire(p.bar + 1) : 0u, 0);
+    constexpr int ESZ = sizeof(WT);
     for (int ph = 0; ph < p.nphases && !R.failed; ++ph) {
       const Phase& P = p.prog[ph];
-      if (P.type != PH_GEMV) continue;
-      int gb = 0, rb = 0, ge = 0, re = 0;
-      if (lane == 0) {
-        const int ng = resolve_parts(cfg, P.part, P.nparts, gg_p, kStepGroups);
-        span_of(gg_p, ng, blockIdx.x, gridDim.x, gb, rb, ge, re);
+      if (P.type == PH_GEMV) {
+        int gb = 0, rb = 0, ge = 0, re = 0;
+        if (lane == 0) {
+          const int ng = resolve_parts(cfg, P.part, P.nparts, gg_p, kStepGroups);
+          span_of(gg_p, ng, blockIdx.x, gridDim.x, gb, rb, ge, re);
+        }
+        __syncwarp();
+        gb = __shfl_sync(0xffffffffu, gb, 0); rb = __shfl_sync(0xffffffffu, rb, 0);
+        ge = __shfl_sync(0xffffffffu, ge, 0); re = __shfl_sync(0xffffffffu, re, 0);
+        produce_span<WT>(gg_p, gb, rb, ge, re, D.hd, R, st, pol, lane);
+        __syncwarp();  // gg_p is rewritten by the next phase
+      } else if (P.type == PH_ATTN) {
+        // this CTA's items: chunks written in earlier cycles first, then -- once the QKV phase's
+        // grid barrier has passed -- the chunks holding this cycle's keys
+        int nt = 0, items = 0;
+        if (lane == 0) {
+          for (int i = 0; i < P.nparts && nt >= 0; ++i)
+            nt = att::add_tiles(D, cfg.B, P.part[i].lc, qt_of(P.part[i].lc), kStepChunk, tiles_p, nt, &items,
+                                kStepTiles);
+        }
+        __syncwarp();
+        nt = __shfl_sync(0xffffffffu, nt, 0);
+        items = __shfl_sync(0xffffffffu, items, 0);
+        if (nt <= 0) continue;
+        for (int pass = 0; pass < 2 && !R.failed; ++pass) {
+          if (pass == 1) {
+            int ok = 1;
+            if (lane == 0) {
+              const uint64_t t0 = globaltimer_ns();
+              for (uint32_t it = 0; (ld_acquire(p.bar + 1) - g_start) < (unsigned)ph; ++it)
+                if ((it & 63u) == 63u && globaltimer_ns() - t0 > 2000000000ull) {
+                  set_err(st, ERR_TIMEOUT, 41);
+                  ok = 0;
+                  break;
+                }
+            }
+            if (!__shfl_sync(0xffffffffu, ok, 0)) { R.failed = true; break; }
+          }
+          for (int item = blockIdx.x; item < items && !R.failed; item += gridDim.x) {
+            const att::Item it = att::item_of(tiles_p, nt, item, kStepChunk);
+            const att::Tile& Ti = tiles_p[it.T];
+            if (att::chunk_is_new(Ti, it.c, kStepChunk) != (pass == 1)) continue;
+            const int s = R.ctr % kStages;
+            if (R.ctr >= (uint32_t)kStages && !mbar_wait_bounded(&R.empty[s], ((R.ctr / kStages) - 1) & 1)) {
+              if (lane == 0) set_err(st, ERR_TIMEOUT, 42);
+              R.failed = true;
+              break;
+            }
+            if (lane == 0) {
+              const uint32_t bytes = (uint32_t)it.nk * D.hd * ESZ;
+              const size_t off = ((size_t)it.kh * D.max_seq + (size_t)it.c * kStepChunk) * D.hd * ESZ;
+              unsigned char* dst = R.base + (size_t)s * kStageBytes;
+              mbar_arrive_expect_tx(&R.full[s], 2 * bytes);
+              bulk_g2s(dst, Ti.kc + off, bytes, &R.full[s], pol);
+              bulk_g2s(dst + kKVHalf, Ti.vc + off, bytes, &R.full[s], pol);
+            }
+            __syncwarp();
+            ++R.ctr;
+          }
+        }
       }
-      __syncwarp();
-      gb = __shfl_sync(0xffffffffu, gb, 0); rb = __shfl_sync(0xffffffffu, rb, 0);
-      ge = __shfl_sync(0xffffffffu, ge, 0); re = __shfl_sync(0xffffffffu, re, 0);
-      produce_span<WT>(gg_p, gb, rb, ge, re, D.hd, R, st, pol, lane);
-      __syncwarp();  // gg_p is rewritten by the next phase
     }
     drain_ring(R, lane);
     return;
@@ -143,7 +199,6 @@ __global__ void __launch_bounds__(kThreads, 1) step_kernel(const __grid_constant
 
   // ------------------------------ consumer warps ------------------------------
   constexpr int NCT = kNCW * 32;
-  uint32_t kv_phase = 0;
   uint64_t t_prev = (blockIdx.x == 0 && tid == 0) ? globaltimer_ns() : 0;
   // groups (table ph & 1) or attention tiles of phase ph; they depend on the control block only,
   // so phase ph+1 is prepared before the grid barrier that ends phase ph
@@ -156,7 +211,8 @@ __global__ void __launch_bounds__(kThreads, 1) step_kernel(const __grid_constant
     } else if (P.type == PH_ATTN) {
       int nt = 0, items = 0;
       for (int i = 0; i < P.nparts && nt >= 0; ++i)
-        nt = att::add_tiles(D, cfg.B, P.part[i].lc, qt_of(P.part[i].lc), kStepChunk, tiles, nt, &items);
+        nt = att::add_tiles(D, cfg.B, P.part[i].lc, qt_of(P.part[i].lc), kStepChunk, tiles, nt, &items,
+                            kStepTiles);
       s_nt = nt > 0 ? nt : 0;
       s_items = nt > 0 ? items : 0;
       s_fail = 0;
@@ -176,9 +232,32 @@ __global__ void __launch_bounds__(kThreads, 1) step_kernel(const __grid_constant
       if (P.nparts > 0 && P.part[0].op == OP_HEAD)
         write_head_partial(loc, hred, cfg.B.head_part + (size_t)blockIdx.x * 8);
     } else if (P.type == PH_ATTN) {
-      if (s_items > 0)
-        att::run_items<WT, kStepChunk>(D, st, tiles, s_nt, s_items, blockIdx.x, gridDim.x, p.attn_qh_max, uni,
-                                       &kv_bar, kv_phase, &s_fail, &s_last);
+      // items from the ring, in the producer's order (older chunks, then this cycle's)
+      float* qs = reinterpret_cast<float*>(uni);
+      float* sc = qs + (size_t)p.attn_qh_max * D.hd;
+      float* m_s = sc + (size_t)p.attn_qh_max * kStepChunk;
+      float* l_s = m_s + p.attn_qh_max;
+      for (int pass = 0; pass < 2 && s_items > 0; ++pass) {
+        for (int item = blockIdx.x; item < s_items; item += gridDim.x) {
+          const att::Item it = att::item_of(tiles, s_nt, item, kStepChunk);
+          if (att::chunk_is_new(tiles[it.T], it.c, kStepChunk) != (pass == 1)) continue;
+          const int s = R.ctr % kStages;
+          if (!R.failed && !mbar_wait_bounded(&R.full[s], (R.ctr / kStages) & 1)) {
+            set_err(st, ERR_TIMEOUT, 31);
+            s_fail = 1;
+          }
+          named_bar(1, NCT);  // uniform decision
+          if (s_fail) R.failed = true;
+          if (!R.failed) {
+            const WT* kst = reinterpret_cast<const WT*>(R.base + (size_t)s * kStageBytes);
+            const WT* vst = reinterpret_cast<const WT*>(R.base + (size_t)s * kStageBytes + kKVHalf);
+            att::item_compute<WT, kStepChunk>(D, tiles[it.T], it, kst, vst, qs, sc, m_s, l_s, &s_last);
+          }
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&R.empty[s]);
+          ++R.ctr;
+        }
+      }
     } else if (blockIdx.x == 0) {  // control: the last phase
       Top2 (*red)[2] = reinterpret_cast<Top2(*)[2]>(uni);
       if (P.type == PH_CTRL_CYCLE) ctl::control_cycle<WT>(D, cfg.B, red, s_tok, s_slot, NCT, 1);
@@ -206,12 +285,13 @@ __global__ void __launch_bounds__(kThreads, 1) step_kernel(const __grid_constant
 
 size_t step_smem_bytes(const Dims& D) {
   const int esz = D.dtype == SPD_DTYPE_BF16 ? 2 : 4;
-  size_t uni = att::smem_bytes(D.hd, D.gq, esz, kAttnQT, kStepChunk);
+  if ((size_t)kStepChunk * D.hd * esz > (size_t)kKVHalf) return 0;  // a K or V chunk fills half a stage
+  size_t uni = att::smem_bytes(D.hd, D.gq, esz, kAttnQT, kStepChunk) - (size_t)2 * kStepChunk * D.hd * esz;
   if (uni < (size_t)kMmaScratch) uni = (size_t)kMmaScratch;
   if (uni < (size_t)kNCW * 32 * 2 * sizeof(Top2)) uni = (size_t)kNCW * 32 * 2 * sizeof(Top2);
   uni = (uni + 127) & ~(size_t)127;
   const size_t total = 1024 + (size_t)kStages * kStageBytes + uni + 3 * kStepGroups * sizeof(GG) +
-                       (size_t)kMaxTiles * sizeof(att::Tile);
+                       (size_t)2 * kStepTiles * sizeof(att::Tile);
   const size_t static_bytes = 8 * 1024;  // barriers, per-vector 1/rms, head merge scratch
   return total + static_bytes <= 227 * 1024 ? total : 0;
 }
@@ -236,7 +316,7 @@ cudaError_t launch_step(const Dims& D, const Bufs& B, const LaunchCfg& lcfg, con
   p.bar = bar;
   p.phase_ns = phase_ns;
   const int esz = D.dtype == SPD_DTYPE_BF16 ? 2 : 4;
-  size_t uni = att::smem_bytes(D.hd, D.gq, esz, kAttnQT, kStepChunk);
+  size_t uni = att::smem_bytes(D.hd, D.gq, esz, kAttnQT, kStepChunk) - (size_t)2 * kStepChunk * D.hd * esz;
   if (uni < (size_t)kMmaScratch) uni = (size_t)kMmaScratch;
   if (uni < (size_t)kNCW * 32 * 2 * sizeof(Top2)) uni = (size_t)kNCW * 32 * 2 * sizeof(Top2);
   p.union_bytes = (int)((uni + 127) & ~(size_t)127);
