@@ -9,6 +9,7 @@ no flush is needed between steps.  Prints ONE JSON line on rank 0.
 
   python bench.py [--gpus N --steps K --warmup W --workload NAME --alpha A]
   python bench.py --impl reference      # the CPU oracle timed on the host cores
+  python bench.py --profile-cycles K    # K eager SPD cycles, for ncu launch lists and captures
 """
 from __future__ import annotations
 
@@ -38,6 +39,9 @@ def parse():
     ap.add_argument("--alpha", type=float, default=None)
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--profile-cycles", type=int, default=0,
+                    help="profiling case: prefill, then this many SPD cycles as plain (non-graph) "
+                         "launches of the step kernel, one per cycle; prints one summary line")
     return ap.parse_args()
 
 
@@ -404,8 +408,47 @@ def main_spd(args):
     return 0
 
 
+def main_profile(args):
+    """Prefill, G plain AR steps (the reference stream for the draft overrides), then K SPD cycles,
+    all launched one by one without graphs.  Under a profiler the launch sequence is fixed: set-up
+    and prefill kernels, G step-kernel launches (AR), then exactly one step-kernel launch per cycle,
+    so `-k regex:step_kernel -s <G + warm-up cycles>` selects steady-state cycles."""
+    import torch
+    import spd_inputs as si
+    import speculative_pipeline_decoding_gb300 as spd
+    from speculative_pipeline_decoding_gb300 import binding as B
+    from speculative_pipeline_decoding_gb300 import build_ext
+
+    build_ext.build()
+    w = si.WORKLOADS[args.workload]
+    alpha = args.alpha if args.alpha is not None else w.alphas[0]
+    P, G = w.prompt_len, w.gen_len
+    params = si.generate_weights(w, device="cuda")
+    prompt = si.prompt_tokens(w).tolist()
+    torch.cuda.synchronize()
+    eng = spd.Engine(spd.Config.from_workload(w), params)
+    eng.set_options(B.OPT_DEFAULT & ~B.OPT_GRAPHS)
+    first = eng.prefill(prompt)
+    ar, _ = eng.generate_ar(G)  # G step-kernel launches, one per token: the reference stream
+    eng.rollback(P, first)
+    modes = si.override_modes(w.coin_seed, alpha, P + 2, P + G)
+    eng.set_draft_override(P + 2, ar.tolist()[1:], modes)
+    t0 = time.time()
+    exits = 0
+    for _ in range(args.profile_cycles):
+        exits += eng.cycle()["exited"]
+    torch.cuda.synchronize()
+    print(json.dumps({"profile_cycles": args.profile_cycles, "ar_steps_before": G, "exits": exits,
+                      "workload": w.name,
+                      "wall_s": time.time() - t0}))
+    eng.close()
+    return 0
+
+
 def main():
     args = parse()
+    if args.profile_cycles > 0:
+        return main_profile(args)
     if args.impl == "reference":
         return main_reference(args)
     return main_spd(args)

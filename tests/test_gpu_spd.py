@@ -238,3 +238,38 @@ def test_dense_full_size_sampled_tokens_match_oracle(dense_setup):
 def test_dense_full_size_first_cycles_parity(dense_setup):
     worst = per_cycle_parity(dense_setup, 0.8, 12, 2e-2)
     print("dense1.5b bf16 worst relative errors", worst)
+
+
+# ------------------------------------------------------------------------------------------------
+# execution options: the persistent step kernel vs per-operator launches, draft module co-scheduled
+# vs serialised, graphs vs eager launches -- every combination computes the same streams
+# ------------------------------------------------------------------------------------------------
+def _option_sets():
+    from speculative_pipeline_decoding_gb300 import binding as B
+    return {
+        "step_serial_graphs": B.OPT_STEP | B.OPT_PDL | B.OPT_GRAPHS,
+        "step_cosched_eager": B.OPT_STEP | B.OPT_PDL | B.OPT_COSCHED,
+        "ops_cosched_graphs": B.OPT_GRAPHS | B.OPT_PDL | B.OPT_COSCHED,
+        "ops_serial_eager": 0,
+    }
+
+
+@pytest.mark.parametrize("name", ["step_serial_graphs", "step_cosched_eager", "ops_cosched_graphs",
+                                  "ops_serial_eager"])
+@pytest.mark.parametrize("setup", ["tiny_setup", "small_setup"])
+def test_execution_options_give_identical_streams(request, setup, name):
+    from speculative_pipeline_decoding_gb300 import binding as B
+    S = request.getfixturevalue(setup)
+    alpha = S.w.alphas[0]
+    toks0, stats0, trace0 = S.spd_run(alpha)
+    S.eng.set_options(_option_sets()[name])
+    try:
+        toks, stats, trace = S.spd_run(alpha)
+        S.eng.rollback(S.P, S.first)
+        ar, _ = S.eng.generate_ar(S.G)
+    finally:
+        S.eng.set_options(B.OPT_DEFAULT)
+    assert toks == toks0 == S.ar
+    assert ar.tolist() == S.ar
+    assert np.array_equal(trace, trace0)
+    assert stats["cycles"] == stats0["cycles"] and stats["rejects"] == stats0["rejects"]
