@@ -36,7 +36,7 @@ __global__ void __launch_bounds__(kAttnThreads) attn_kernel(const __grid_constan
   if (threadIdx.x == 0) {
     const bool skip = p.lc.kind != LK_EXPLICIT && (st->done || st->err);
     int items = 0;
-    const int nt = skip ? 0 : att::add_tiles(p.D, p.B, p.lc, p.qt, kAttnChunk, tiles, 0, &items);
+    const int nt = skip ? 0 : att::add_tiles(p.D, p.B, p.lc, p.qt, kAttnChunk, tiles, 0, &items, kMaxTiles, p.B.st);
     s_nt = nt > 0 ? nt : 0;
     s_items = nt > 0 ? items : 0;
     s_fail = 0;

@@ -21,6 +21,8 @@ constexpr int kThreads = 256;   // threads taking part (named barrier 2)
 
 struct Tile {
   int layer, nq, pos0, vid0, nch, rec_off, item_off, tick_off;
+  int co, old_off, new_off;  // step kernel: chunks written before this cycle; item offsets of the
+                             // tile in the lists of such chunks and of the chunks holding new keys
   const unsigned char* kc;  // base of this layer's K cache (head 0, position 1)
   const unsigned char* vc;
   const float* q;           // query rows [row][qkv_rows] (rotated q at the front)
@@ -31,7 +33,7 @@ struct Tile {
 
 // Appends the tiles of one part (a launch descriptor; rows of up to `qt` queries per tile).
 static __device__ int add_tiles(const Dims& D, const Bufs& B, const Launch& lc, int qt, int ck, Tile* tiles,
-                         int nt, int* items, int cap = kMaxTiles) {
+                         int nt, int* items, int cap, const DevState* sv) {
   DevState* st = B.st;
   RowGroup rg[kMaxGroups];
   int nr;
@@ -41,7 +43,7 @@ static __device__ int add_tiles(const Dims& D, const Bufs& B, const Launch& lc, 
       rg[r].layer = 0; rg[r].nv = 1; rg[r].pos0 = lc.act.pos_arr[r]; rg[r].vid0 = r; rg[r].rrow0 = 0;
     }
   } else {
-    nr = build_rows(lc, D, st, rg);
+    nr = build_rows(lc, D, sv, st, rg);
   }
   const int esz = D.dtype == SPD_DTYPE_BF16 ? 2 : 4;
   const size_t layer_elems = (size_t)D.hkv * D.max_seq * D.hd;
@@ -276,6 +278,218 @@ static __device__ bool run_items(const Dims& D, DevState* st, const Tile* tiles,
     item_compute<WT, CK>(D, Ti, it, ks, vs, qs, sc, m_s, l_s, last_flag);
   }
   return true;
+}
+
+// ------------------------------------------------------------------------------------------------
+// One warp per work item (persistent step kernel).  Item = (tile, kv head, chunk of CK = 32 keys);
+// its K and V chunks sit in a ring stage ([nk][hd] each, cache dtype).  Per query head of the tile:
+// lane k scores key k (a dot product over hd, reading the K row from a rotated chunk so that the
+// lanes of a quarter-warp hit distinct banks), the chunk's softmax statistics come from xor-shuffle
+// reductions, and lane l accumulates output dims [l*hd/32, (l+1)*hd/32) over the chunk's keys.
+// The partial (o, m, l) goes to global scratch.  A warp batches the tickets of its items (one
+// fence, then one atomic per (tile, kv head) it touched); the warp that takes the last ticket of a
+// (tile, kv head) merges the partials of every query head in chunk order.  No block barrier.
+// ------------------------------------------------------------------------------------------------
+constexpr int kWarpCK = 32;
+
+// Chunks of earlier cycles and chunks holding this cycle's keys, per tile (`ck` keys per chunk):
+// fills co / old_off / new_off and returns the totals.
+__device__ __forceinline__ void split_items(const Dims& D, Tile* tiles, int nt, int ck, int* n_old, int* n_new) {
+  int o = 0, w = 0;
+  for (int i = 0; i < nt; ++i) {
+    Tile& T = tiles[i];
+    T.co = min(T.nch, (T.pos0 - 1) / ck);
+    T.old_off = o;
+    T.new_off = w;
+    o += D.hkv * T.co;
+    w += D.hkv * (T.nch - T.co);
+  }
+  *n_old = o;
+  *n_new = w;
+}
+
+// Item `g` of the list of old (pass 0) or new (pass 1) chunks.
+__device__ __forceinline__ Item item_of_pass(const Tile* tiles, int nt, int pass, int g, int ck) {
+  Item it;
+  it.T = 0;
+  if (pass == 0) {
+    while (it.T + 1 < nt && tiles[it.T + 1].old_off <= g) ++it.T;
+    const Tile& T = tiles[it.T];
+    const int rem = g - T.old_off;
+    it.kh = rem / T.co;
+    it.c = rem % T.co;
+  } else {
+    while (it.T + 1 < nt && tiles[it.T + 1].new_off <= g) ++it.T;
+    const Tile& T = tiles[it.T];
+    const int nn = T.nch - T.co;
+    const int rem = g - T.new_off;
+    it.kh = rem / nn;
+    it.c = T.co + rem % nn;
+  }
+  const Tile& T = tiles[it.T];
+  it.nk = min(ck, T.pos0 + T.nq - 1 - it.c * ck);
+  return it;
+}
+
+// DPL consecutive elements of a K/V row in shared memory -> fp32 (DPL * sizeof(WT) bytes, aligned).
+template <typename WT, int DPL>
+__device__ __forceinline__ void load_row(const WT* p, float* f) {
+  if constexpr (sizeof(WT) == 2 && DPL == 2) {
+    const uint32_t u = *reinterpret_cast<const uint32_t*>(p);
+    f[0] = bf16_lo(u); f[1] = bf16_hi(u);
+  } else if constexpr (sizeof(WT) == 2 && DPL == 4) {
+    const uint2 u = *reinterpret_cast<const uint2*>(p);
+    f[0] = bf16_lo(u.x); f[1] = bf16_hi(u.x); f[2] = bf16_lo(u.y); f[3] = bf16_hi(u.y);
+  } else if constexpr (sizeof(WT) == 2 && DPL == 8) {
+    WTraits<WT>::unpack(*reinterpret_cast<const uint4*>(p), f);
+  } else if constexpr (DPL == 2) {
+    const float2 v = *reinterpret_cast<const float2*>(p);
+    f[0] = v.x; f[1] = v.y;
+  } else {
+#pragma unroll
+    for (int e = 0; e < DPL; e += 4) {
+      const float4 v = *reinterpret_cast<const float4*>(p + e);
+      f[e] = v.x; f[e + 1] = v.y; f[e + 2] = v.z; f[e + 3] = v.w;
+    }
+  }
+}
+
+// Query head qh of tile T for kv head kh -> lane's DPL dims (rotated q, written by the QKV phase).
+template <int DPL>
+__device__ __forceinline__ void load_q(const Dims& D, const Tile& T, int kh, int qh, float* qv) {
+  const int lane = threadIdx.x & 31;
+  const int r = qh / D.gq, hg = qh % D.gq;
+  const float* src = T.q + (size_t)(T.vid0 + r) * D.qkv_rows + (kh * D.gq + hg) * D.hd + lane * DPL;
+  if constexpr (DPL % 4 == 0) {
+#pragma unroll
+    for (int e = 0; e < DPL; e += 4) {
+      const float4 v = __ldcg(reinterpret_cast<const float4*>(src + e));
+      qv[e] = v.x; qv[e + 1] = v.y; qv[e + 2] = v.z; qv[e + 3] = v.w;
+    }
+  } else {
+#pragma unroll
+    for (int e = 0; e < DPL; e += 2) {
+      const float2 v = __ldcg(reinterpret_cast<const float2*>(src + e));
+      qv[e] = v.x; qv[e + 1] = v.y;
+    }
+  }
+}
+
+// Query heads qh0, qh0 + qstep, ... of item `it` on the calling warp; q0 holds query head qh0
+// (loaded ahead by the caller).  ks / vs: the chunk's K and V rows in shared memory; qb: hd floats
+// of per-warp scratch.  Writes one partial (o, m, l) per query head; no ticket.
+template <typename WT, int DPL>
+__device__ void warp_item(const Dims& D, const Tile& T, const Item& it, const WT* ks, const WT* vs, float* qb,
+                          int qh0, int qstep, const float* q0) {
+  constexpr int CK = kWarpCK;
+  constexpr int VEC = WTraits<WT>::kVec;  // elements per 16-byte chunk of a K row
+  const int lane = threadIdx.x & 31;
+  const int hd = D.hd;
+  const int nchk = hd / VEC;               // 16-byte chunks per K row
+  const float scale = 1.0f / sqrtf((float)hd);
+  const int QH = T.nq * D.gq;
+  const int kh = it.kh, c = it.c, nk = it.nk;
+  const int key0 = c * CK;
+  float qc[DPL];
+#pragma unroll
+  for (int e = 0; e < DPL; ++e) qc[e] = q0[e];
+  for (int qh = qh0; qh < QH; qh += qstep) {
+    const int pos_q = T.pos0 + qh / D.gq;
+    const bool more = qh + qstep < QH;
+    float qn[DPL];
+    if (more) load_q<DPL>(D, T, kh, qh + qstep, qn);  // next query head in flight
+#pragma unroll
+    for (int e = 0; e < DPL; ++e) qb[lane * DPL + e] = qc[e];
+    __syncwarp();
+    // score of key `lane`: four partial sums (element e % 4), added at the end
+    float d4[4] = {0.f, 0.f, 0.f, 0.f};
+    if (lane < nk) {
+      const WT* kr = ks + (size_t)lane * hd;
+#pragma unroll 4
+      for (int j = 0; j < nchk; ++j) {
+        const int jj = (j + lane) % nchk;
+        float kf[VEC];
+        WTraits<WT>::unpack(*reinterpret_cast<const uint4*>(kr + jj * VEC), kf);
+        const float* qv = qb + jj * VEC;
+#pragma unroll
+        for (int e = 0; e < VEC; e += 4) {
+          const float4 q4 = *reinterpret_cast<const float4*>(qv + e);
+          d4[0] = fmaf(kf[e], q4.x, d4[0]);
+          d4[1] = fmaf(kf[e + 1], q4.y, d4[1]);
+          d4[2] = fmaf(kf[e + 2], q4.z, d4[2]);
+          d4[3] = fmaf(kf[e + 3], q4.w, d4[3]);
+        }
+      }
+    }
+    const float dot = (d4[0] + d4[1]) + (d4[2] + d4[3]);
+    const float sk = (lane < nk && key0 + lane < pos_q) ? dot * scale : -INFINITY;
+    float m = sk;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+    const float pk = (m == -INFINITY) ? 0.f : expf(sk - m);
+    float l = pk;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) l += __shfl_xor_sync(0xffffffffu, l, o);
+    // unnormalised chunk output, dims lane*DPL ..
+    float acc[DPL];
+#pragma unroll
+    for (int e = 0; e < DPL; ++e) acc[e] = 0.f;
+#pragma unroll 8
+    for (int k = 0; k < nk; ++k) {
+      const float pj = __shfl_sync(0xffffffffu, pk, k);
+      float vf[DPL];
+      load_row<WT, DPL>(vs + (size_t)k * hd + lane * DPL, vf);
+#pragma unroll
+      for (int e = 0; e < DPL; ++e) acc[e] = fmaf(pj, vf[e], acc[e]);
+    }
+    float* rec = T.part + ((size_t)T.rec_off + ((size_t)kh * T.nch + c) * QH + qh) * (hd + 2);
+#pragma unroll
+    for (int e = 0; e < DPL; ++e) rec[lane * DPL + e] = acc[e];
+    if (lane == 0) { rec[hd] = m; rec[hd + 1] = l; }
+    __syncwarp();  // qb is rewritten by the next query head
+    if (more) {
+#pragma unroll
+      for (int e = 0; e < DPL; ++e) qc[e] = qn[e];
+    }
+  }
+}
+
+// Merge of (tile T, kv head kh) on the calling warp, after its last ticket: each query head over
+// its own chunks, in chunk order; resets the ticket.
+template <int DPL>
+__device__ void warp_merge(const Dims& D, const Tile& T, int kh) {
+  constexpr int CK = kWarpCK;
+  const int lane = threadIdx.x & 31;
+  const int hd = D.hd, GQ = D.gq;
+  const int hqd = D.hq * hd;
+  const int QH = T.nq * GQ;
+  for (int qh = 0; qh < QH; ++qh) {
+    const int r = qh / GQ, hg = qh % GQ;
+    const int nc = (T.pos0 + r + CK - 1) / CK;
+    const float* base = T.part + ((size_t)T.rec_off + (size_t)kh * T.nch * QH + qh) * (hd + 2);
+    const size_t cstride = (size_t)QH * (hd + 2);
+    float M = -INFINITY;
+    for (int cc = lane; cc < nc; cc += 32) M = fmaxf(M, __ldcg(base + cc * cstride + hd));
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+    // the sums run over the chunks in order; four chunks' loads are issued together
+    float Ls = 0.f, O[DPL];
+#pragma unroll
+    for (int e = 0; e < DPL; ++e) O[e] = 0.f;
+#pragma unroll 4
+    for (int cc = 0; cc < nc; ++cc) {
+      const float* rc = base + cc * cstride;
+      const float w = expf(__ldcg(rc + hd) - M);
+      Ls = fmaf(__ldcg(rc + hd + 1), w, Ls);
+#pragma unroll
+      for (int e = 0; e < DPL; ++e) O[e] = fmaf(__ldcg(rc + lane * DPL + e), w, O[e]);
+    }
+    float* out = T.out + (size_t)(T.vid0 + r) * hqd + (kh * GQ + hg) * hd + lane * DPL;
+#pragma unroll
+    for (int e = 0; e < DPL; ++e) out[e] = O[e] / Ls;
+  }
+  __syncwarp();
+  if (lane == 0) T.tick[T.tick_off + kh] = 0;
 }
 
 }  // namespace att

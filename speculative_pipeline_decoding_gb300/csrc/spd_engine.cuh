@@ -106,7 +106,7 @@ __device__ __forceinline__ void gg_clear(GG& o) {
 }
 
 // Appends the groups of one launch part; returns the new group count.
-static __device__ int add_part(const EngineCfg& p, const GemvPart& pt, GG* gg, int ng, int cap) {
+static __device__ int add_part(const EngineCfg& p, const GemvPart& pt, GG* gg, int ng, int cap, const View& vw) {
   const Dims& D = p.D;
   const Bufs& B = p.B;
   const Launch& lc = pt.lc;
@@ -115,7 +115,8 @@ static __device__ int add_part(const EngineCfg& p, const GemvPart& pt, GG* gg, i
     return ng;
   }
   const Act& A = lc.act;
-  DevState* st = B.st;
+  DevState* st = B.st;         // error flags
+  const DevState* sv = vw.sv;  // control block (read)
   if (pt.op == OP_HEAD) {
     auto add = [&](const float* x, int xrow0, int xring, const CUtensorMap* W, const float* nw, int kind) {
       GG& o = gg[ng++];
@@ -126,14 +127,14 @@ static __device__ int add_part(const EngineCfg& p, const GemvPart& pt, GG* gg, i
       o.y = nullptr; o.normw = nw; o.epi = EPI_TOP2; o.kind = kind;
     };
     if (lc.kind == LK_DIAG) {
-      if (st->a == D.n) add(B.resid, (st->t - D.n + 1) % (D.n + 1), D.n + 1, B.tm_lm, B.final_norm, 0);
-      if (!(st->flags & SF_TARGET_ONLY)) {
-        const int R = st->t - st->pdm_len;
+      if (sv->a == D.n) add(B.resid, (sv->t - D.n + 1) % (D.n + 1), D.n + 1, B.tm_lm, B.final_norm, 0);
+      if (!(sv->flags & SF_TARGET_ONLY)) {
+        const int R = sv->t - sv->pdm_len;
         if (R < 1 || R > D.n + 1) set_err(st, ERR_PDM_ROWS, 200);
         else add(A.qkv /* draft rows z */, R - 1, kBig, B.tm_pdm, B.pdm_norm, 1);
       }
     } else if (lc.kind == LK_AR) {
-      add(B.resid, st->t % (D.n + 1), D.n + 1, B.tm_lm, B.final_norm, 0);
+      add(B.resid, sv->t % (D.n + 1), D.n + 1, B.tm_lm, B.final_norm, 0);
     } else if (lc.kind == LK_ROWS) {
       add(A.resid, lc.cnt - 1, kBig, B.tm_lm, B.final_norm, 0);
     }
@@ -151,14 +152,14 @@ static __device__ int add_part(const EngineCfg& p, const GemvPart& pt, GG* gg, i
       o.y = A.resid; o.ystride = D.d;
       return ng;
     }
-    const int t = st->t, a = st->a, R = t - st->pdm_len;
+    const int t = sv->t, a = sv->a, R = t - sv->pdm_len;
     if (R < 1 || R > D.n + 1) {
       set_err(st, ERR_PDM_ROWS, 300);
       return ng;
     }
     int prev_f = -1;
     for (int r = 0; r < R; ++r) {
-      const int pos = st->pdm_len + 1 + r;
+      const int pos = sv->pdm_len + 1 + r;
       const int depth = (t - pos < a) ? (t - pos) : D.n;
       const int f = D.ftab[depth];
       if (f != prev_f) {
@@ -175,8 +176,8 @@ static __device__ int add_part(const EngineCfg& p, const GemvPart& pt, GG* gg, i
     return ng;
   }
   RowGroup rg[kMaxGroups];
-  const int nr = build_rows(lc, D, st, rg);
-  const LayerW* LW = lc.stack == 0 ? B.tl : B.pl;
+  const int nr = build_rows(lc, D, sv, st, rg);
+  const LayerW* LW = lc.stack == 0 ? vw.tl : vw.pl;
   const int hqd = D.hq * D.hd;
   const int esz = D.dtype == SPD_DTYPE_BF16 ? 2 : 4;
   const size_t layer_bytes = (size_t)D.hkv * D.max_seq * D.hd * esz;
@@ -259,9 +260,10 @@ static __device__ int finish_groups(const EngineCfg& p, GG* gg, int ng, int cap)
   return ng;
 }
 
-static __device__ int resolve_parts(const EngineCfg& p, const GemvPart* parts, int nparts, GG* gg, int cap) {
+static __device__ int resolve_parts(const EngineCfg& p, const GemvPart* parts, int nparts, GG* gg, int cap,
+                                    const View& vw) {
   int ng = 0;
-  for (int i = 0; i < nparts; ++i) ng = add_part(p, parts[i], gg, ng, cap);
+  for (int i = 0; i < nparts; ++i) ng = add_part(p, parts[i], gg, ng, cap, vw);
   return finish_groups(p, gg, ng, cap);
 }
 
@@ -358,9 +360,11 @@ __device__ __forceinline__ void store_kv(void* base, int head, int pos, int e, c
 
 // Epilogue of one output row (or rotary pair) for vector v.  y0/y1: the two accumulations the
 // caller holds (gate/up: gate and up of row r; rotary: rows r and its partner; else y1 unused).
+// `pre` (or null): the inputs the epilogue reads, loaded by the caller ahead of time -- the residual
+// value of the row (RESID) or the rotary cos and sin of the pair (QKV).
 template <typename WT>
 __device__ __forceinline__ void epilogue(const EngineCfg& p, const GG& G, int v, int row, float y0,
-                                         float y1, bool pair, Top2* loc) {
+                                         float y1, bool pair, Top2* loc, const float* pre = nullptr) {
   const Dims& D = p.D;
   if (G.epi == EPI_TOP2) {
     top2_push(loc[G.kind], y0, row);
@@ -374,7 +378,7 @@ __device__ __forceinline__ void epilogue(const EngineCfg& p, const GG& G, int v,
       yrow[row] = (y0 / (1.0f + expf(-y0))) * y1;
       break;
     case EPI_RESID: {
-      const float hn = yrow[row] + y0;
+      const float hn = (pre ? pre[0] : yrow[row]) + y0;
       yrow[row] = hn;
       if (G.anch) G.anch[(size_t)yr * G.astride + row] = hn;
       break;
@@ -384,8 +388,8 @@ __device__ __forceinline__ void epilogue(const EngineCfg& p, const GG& G, int v,
       const int hd = D.hd, half = hd / 2;
       if (pair) {  // row = physical index of the first element of a rotary pair
         const int h = row / hd, i = row % hd;
-        const float c = p.B.rope_cos[(size_t)(pos - 1) * half + i];
-        const float s = p.B.rope_sin[(size_t)(pos - 1) * half + i];
+        const float c = pre ? pre[0] : p.B.rope_cos[(size_t)(pos - 1) * half + i];
+        const float s = pre ? pre[1] : p.B.rope_sin[(size_t)(pos - 1) * half + i];
         const float r1 = y0 * c - y1 * s;
         const float r2 = y1 * c + y0 * s;
         if (h < D.hq) {
@@ -657,6 +661,8 @@ static __device__ void consume_span(const EngineCfg& p, const GG* gg, int gb, in
   const int hd = p.D.hd;
   DevState* st = p.B.st;
   float rstd = 1.f;
+  bool xs_on = false;  // single-vector group: its (normalised) input vector is staged in `scratch`
+  float* xs = reinterpret_cast<float*>(scratch);
   int last_g = -1;
   for (int g = gb, r = rb; g < ge || (g == ge && r < re);) {
     const GG& G = gg[g];
@@ -665,9 +671,10 @@ static __device__ void consume_span(const EngineCfg& p, const GG* gg, int gb, in
     if (g != last_g) {  // group entry: 1/rms of the input vector(s)
       named_bar(1, NCT);
       rstd = 1.f;
+      xs_on = false;
       if (!G.mma) {
+        const float* xr = G.x + (size_t)(G.xrow0 % G.xring) * G.xstride;
         if (G.normw) {
-          const float* xr = G.x + (size_t)(G.xrow0 % G.xring) * G.xstride;
           float sq = 0.f;
 #pragma unroll 4
           for (int c = tid * 4; c < G.cols; c += NCT * 4) {
@@ -681,6 +688,20 @@ static __device__ void consume_span(const EngineCfg& p, const GG* gg, int gb, in
 #pragma unroll
           for (int w8 = 0; w8 < kNCW; ++w8) tot += wpart[w8];
           rstd = 1.0f / sqrtf(tot / (float)G.cols + p.eps);
+        }
+        // the whole input vector once into shared memory (x * rstd * norm weight when normalised,
+        // the product formed in the same order as on the streaming path): no per-stage loads
+        if (G.cols * (int)sizeof(float) <= kMmaScratch) {
+          xs_on = true;
+          for (int c = tid * 4; c < G.cols; c += NCT * 4) {
+            float4 q = *reinterpret_cast<const float4*>(xr + c);
+            if (G.normw) {
+              const float4 n4 = *reinterpret_cast<const float4*>(G.normw + c);
+              q.x = q.x * rstd * n4.x; q.y = q.y * rstd * n4.y;
+              q.z = q.z * rstd * n4.z; q.w = q.w * rstd * n4.w;
+            }
+            *reinterpret_cast<float4*>(xs + c) = q;
+          }
         }
       } else if (G.normw) {
         for (int v = warp; v < G.nv; v += kNCW) {
@@ -701,6 +722,22 @@ static __device__ void consume_span(const EngineCfg& p, const GG* gg, int gb, in
     if (!G.mma) {
       // ---------------- single-vector path ----------------
       const float* xr = G.x + (size_t)(G.xrow0 % G.xring) * G.xstride;
+      // the epilogue inputs of this lane's output row, loaded now: they are in registers when the
+      // tile ends (the residual value, or the rotary cos / sin of the pair)
+      float pre[2] = {0.f, 0.f};
+      if (lane < 8 && G.nw != 2) {
+        const int slot = warp + 8 * lane;
+        if (G.epi == EPI_QKV && r < G.seg2) {
+          if (lane < 4) {
+            const int i = phys_row(G, r + slot, hd) % hd;
+            const size_t at = (size_t)(G.pos0 - 1) * (hd / 2) + i;
+            pre[0] = __ldg(p.B.rope_cos + at);
+            pre[1] = __ldg(p.B.rope_sin + at);
+          }
+        } else if (G.epi == EPI_RESID && slot < tr) {
+          pre[0] = __ldcg(G.y + (size_t)(G.yrow0 % G.yring) * G.ystride + r + slot);
+        }
+      }
       float acc[8];
 #pragma unroll
       for (int i = 0; i < 8; ++i) acc[i] = 0.f;
@@ -721,7 +758,13 @@ static __device__ void consume_span(const EngineCfg& p, const GG* gg, int gb, in
           }
           const int col = c0 + VEC * lane;
           float xv[VEC];
-          if (col < G.cols) {
+          if (col < G.cols && xs_on) {
+#pragma unroll
+            for (int e = 0; e < VEC; e += 4) {
+              const float4 q = *reinterpret_cast<const float4*>(xs + col + e);
+              xv[e] = q.x; xv[e + 1] = q.y; xv[e + 2] = q.z; xv[e + 3] = q.w;
+            }
+          } else if (col < G.cols) {
 #pragma unroll
             for (int e = 0; e < VEC; e += 4) {
               float4 q = *reinterpret_cast<const float4*>(xr + col + e);
@@ -762,9 +805,9 @@ static __device__ void consume_span(const EngineCfg& p, const GG* gg, int gb, in
         if (G.nw == 2) {
           if (lane < 4 && slot < tr) epilogue<WT>(p, G, 0, r + slot, y0, y1, false, loc);
         } else if (G.epi == EPI_QKV && r < G.seg2) {
-          if (lane < 4) epilogue<WT>(p, G, 0, phys_row(G, r + slot, hd), y0, y1, true, loc);
+          if (lane < 4) epilogue<WT>(p, G, 0, phys_row(G, r + slot, hd), y0, y1, true, loc, pre);
         } else if (slot < tr) {
-          epilogue<WT>(p, G, 0, r + slot, y0, 0.f, false, loc);
+          epilogue<WT>(p, G, 0, r + slot, y0, 0.f, false, loc, G.epi == EPI_RESID ? pre : nullptr);
         }
       }
     } else if (G.nv <= 16) {

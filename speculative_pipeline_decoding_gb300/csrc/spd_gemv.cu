@@ -50,7 +50,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_engine(const __grid_constant
     fence_mbar_init();
     int ng = 0;
     if (p.explicit_mode) ng = resolve_explicit(p.cfg, p.ge, gg);
-    else if (!(st->done || st->err)) ng = resolve_parts(p.cfg, p.part, p.nparts, gg, kMaxGroups);
+    else if (!(st->done || st->err)) ng = resolve_parts(p.cfg, p.part, p.nparts, gg, kMaxGroups, View{st, p.cfg.B.tl, p.cfg.B.pl});
     s_ng = ng;
     span_of(gg, ng, blockIdx.x, gridDim.x, s_gb, s_rb, s_ge, s_re);
   }

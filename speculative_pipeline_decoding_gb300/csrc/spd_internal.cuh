@@ -235,13 +235,22 @@ struct RowGroup {
   int layer, nv, pos0, vid0, rrow0;
 };
 
-// Fill `g` from the launch kind and the control block; returns the group count (0 if none).
-// Executed by one thread.  Sets an error flag for an out-of-step draft cache.
-__device__ __forceinline__ int build_rows(const Launch& lc, const Dims& D, DevState* st,
+// Where row and group resolution reads the control block and the per-layer tables: global memory
+// in the stand-alone kernels; shared-memory snapshots taken at the start of the step kernel (the
+// control block changes only in its last phase), so that resolving a phase costs no global loads.
+struct View {
+  const DevState* sv;
+  const LayerW* tl;
+  const LayerW* pl;
+};
+
+// Fill `g` from the launch kind and the control block `sv`; returns the group count (0 if none).
+// Executed by one thread.  Sets an error flag in `st` for an out-of-step draft cache.
+__device__ __forceinline__ int build_rows(const Launch& lc, const Dims& D, const DevState* sv, DevState* st,
                                           RowGroup* g) {
   switch (lc.kind) {
     case LK_DIAG: {
-      const int a = st->a, t = st->t;
+      const int a = sv->a, t = sv->t;
       for (int j = 0; j < a; ++j) {
         g[j].layer = j * D.S + lc.sub; g[j].nv = 1; g[j].pos0 = t - j; g[j].vid0 = j;
         g[j].rrow0 = (t - j) % (D.n + 1);
@@ -249,20 +258,20 @@ __device__ __forceinline__ int build_rows(const Launch& lc, const Dims& D, DevSt
       return a;
     }
     case LK_PDMROWS: {
-      const int R = st->t - st->pdm_len;
+      const int R = sv->t - sv->pdm_len;
       if (R < 1 || R > D.n + 1) {
         set_err(st, ERR_PDM_ROWS, 100 + lc.sub);
         return 0;
       }
-      g[0].layer = lc.sub; g[0].nv = R; g[0].pos0 = st->pdm_len + 1; g[0].vid0 = 0; g[0].rrow0 = 0;
+      g[0].layer = lc.sub; g[0].nv = R; g[0].pos0 = sv->pdm_len + 1; g[0].vid0 = 0; g[0].rrow0 = 0;
       return 1;
     }
     case LK_ROWS:
       g[0].layer = lc.sub; g[0].nv = lc.cnt; g[0].pos0 = lc.pos0; g[0].vid0 = 0; g[0].rrow0 = 0;
       return 1;
     case LK_AR:
-      g[0].layer = lc.sub; g[0].nv = 1; g[0].pos0 = st->t; g[0].vid0 = 0;
-      g[0].rrow0 = st->t % (D.n + 1);
+      g[0].layer = lc.sub; g[0].nv = 1; g[0].pos0 = sv->t; g[0].vid0 = 0;
+      g[0].rrow0 = sv->t % (D.n + 1);
       return 1;
     default:
       return 0;
@@ -307,7 +316,7 @@ struct Phase {
   int nparts;      // GEMV / attention parts (target rows, draft rows)
   GemvPart part[2];
 };
-constexpr int kStepChunk = 64;   // attention keys per split inside the step kernel
+constexpr int kStepChunk = 32;   // attention keys per split inside the step kernel (one warp item)
 
 // Dynamic shared memory the step kernel needs for this model (0: it does not fit on one SM).
 size_t step_smem_bytes(const Dims& D);

@@ -28,7 +28,11 @@ using namespace eng;
 
 constexpr int kStepGroups = 36;   // groups of one phase: n target + n+1 draft rows (n <= 16)
 constexpr int kStepTiles = 24;    // attention tiles of one phase: n target tiles + draft-row tiles
-constexpr int kKVHalf = kStageBytes / 2;  // an attention item's ring stage: K chunk | V chunk
+constexpr int kProdWarp = kNCW;       // warp 8: producer (weights and K/V chunks into the ring)
+constexpr int kPlanWarp = kNCW + 1;   // warp 9: planner (resolves the next phase)
+constexpr int kStepThreads = (kNCW + 2) * 32;
+constexpr int kNCT = kNCW * 32;       // consumer threads
+constexpr int kStepQT = 4;            // query rows per attention tile of the draft module's rows
 
 struct StepParams {
   EngineCfg cfg;
@@ -36,8 +40,7 @@ struct StepParams {
   int nphases;
   unsigned* bar;                  // [0] count, [1] generation
   unsigned long long* phase_ns;   // accumulated per-phase time (CTA 0), or null
-  int union_bytes;                // attention items / tensor-core partials / control scratch
-  int attn_qh_max;
+  int union_bytes;                // tensor-core partials / attention query vectors / control scratch
 };
 
 __device__ __forceinline__ unsigned ld_acquire(const unsigned* p) {
@@ -46,36 +49,23 @@ __device__ __forceinline__ unsigned ld_acquire(const unsigned* p) {
   return v;
 }
 
-__device__ __forceinline__ unsigned atom_add_acq_rel(unsigned* p, unsigned v) {
-  unsigned old;
-  asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
-  return old;
-}
-
 __device__ __forceinline__ void red_add_release(unsigned* p, unsigned v) {
   asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
 
-// Grid barrier of the 256 consumer threads of every CTA, in two halves so that thread 0 can
-// prepare the next phase between its arrival and its wait.  Writes before grid_arrive are visible
-// to every CTA after grid_wait.
-__device__ __forceinline__ unsigned grid_arrive(unsigned* bar) {  // thread 0 only
-  unsigned* count = bar;
-  unsigned* gen = bar + 1;
-  const unsigned g0 = ld_acquire(gen);
-  const unsigned old = atom_add_acq_rel(count, 1u);
-  if (old == gridDim.x - 1) {
-    atomicExch(count, 0u);
-    red_add_release(gen, 1u);
-  }
-  return g0;
-}
+// Grid barrier of the 256 consumer threads of every CTA.  One monotonic arrival counter: every
+// CTA adds 1 (a release reduction, no round trip) when it arrives; barrier k of a launch is passed
+// once the counter reaches (g0 + k + 1) * gridDim.x, where g0 = barriers completed before the
+// launch (the counter is zeroed with the control block at prefill and rollback).  Arrival and wait
+// are separate so that the next phase can be prepared in between.  Writes before grid_arrive are
+// visible to every CTA after grid_wait.
+__device__ __forceinline__ void grid_arrive(unsigned* bar) { red_add_release(bar, 1u); }  // thread 0
 
-// Thread 0: bounded wait for the generation to move past g0.  False if it gave up.
-__device__ __forceinline__ bool grid_wait(unsigned* bar, unsigned g0, DevState* st) {
-  const unsigned* gen = bar + 1;
+// Thread 0: bounded wait for the counter to reach `target`.  False if it gave up.
+__device__ __forceinline__ bool grid_wait(const unsigned* bar, unsigned target, DevState* st) {
+  if ((int)(ld_acquire(bar) - target) >= 0) return true;
   const uint64_t t0 = globaltimer_ns();
-  for (uint32_t it = 0; ld_acquire(gen) == g0; ++it) {
+  for (uint32_t it = 0; (int)(ld_acquire(bar) - target) < 0; ++it) {
     if ((it & 63u) == 63u && globaltimer_ns() - t0 > 2000000000ull) {
       set_err(st, ERR_TIMEOUT, 70);
       return false;
@@ -85,24 +75,159 @@ __device__ __forceinline__ bool grid_wait(unsigned* bar, unsigned g0, DevState* 
 }
 
 __device__ __forceinline__ int qt_of(const Launch& lc) {
-  return (lc.kind == LK_PDMROWS || lc.kind == LK_ROWS) ? kAttnQT : 1;
+  return (lc.kind == LK_PDMROWS || lc.kind == LK_ROWS) ? kStepQT : 1;
+}
+
+__device__ __forceinline__ void st_release_cta(int* p, int v) {
+  asm volatile("st.release.cta.shared.s32 [%0], %1;" ::"r"(smem_u32(p)), "r"(v) : "memory");
+}
+__device__ __forceinline__ int ld_acquire_cta(const int* p) {
+  int v;
+  asm volatile("ld.acquire.cta.shared.s32 %0, [%1];" : "=r"(v) : "r"(smem_u32(p)) : "memory");
+  return v;
+}
+// Bounded wait (lane 0 of a warp) for a shared progress counter to reach `v`.
+__device__ __forceinline__ bool wait_progress(const int* p, int v) {
+  if (ld_acquire_cta(p) >= v) return true;
+  const uint64_t t0 = globaltimer_ns();
+  for (uint32_t it = 0; ld_acquire_cta(p) < v; ++it)
+    if ((it & 63u) == 63u && globaltimer_ns() - t0 > 2000000000ull) return false;
+  return true;
+}
+
+__device__ __forceinline__ void mbar_arrive_cnt(uint64_t* bar, uint32_t n) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(n) : "memory");
+}
+
+// Cooperative 16-byte copy global -> shared by threads [t0, t0 + nthr) of the caller's set.
+__device__ __forceinline__ void copy16(void* dst, const void* src, int bytes, int t, int nthr) {
+  const uint4* s4 = reinterpret_cast<const uint4*>(src);
+  uint4* d4 = reinterpret_cast<uint4*>(dst);
+  for (int i = t; i < bytes / 16; i += nthr) d4[i] = s4[i];
+}
+
+// Items of one attention phase for this CTA: pass 0 = chunks written in earlier cycles, pass 1 =
+// chunks holding this cycle's keys; each list is dealt to the CTAs round robin, each pass padded to
+// whole ring stages of `ips` items.
+struct AttnPlan {
+  int n0, n1;      // this CTA's items of pass 0 and 1
+  int q0, q1;      // the same, padded to multiples of ips
+  __device__ __forceinline__ int stages(int ips) const { return (q0 + q1) / ips; }
+};
+__device__ __forceinline__ AttnPlan attn_plan(int n_old, int n_new, int ips) {
+  AttnPlan a;
+  const int b = blockIdx.x, G = gridDim.x;
+  a.n0 = n_old > b ? (n_old - b + G - 1) / G : 0;
+  a.n1 = n_new > b ? (n_new - b + G - 1) / G : 0;
+  a.q0 = (a.n0 + ips - 1) / ips * ips;
+  a.q1 = (a.n1 + ips - 1) / ips * ips;
+  return a;
+}
+// Item at padded position q of this CTA's sequence: pass and index in that pass's list (-1: padding).
+__device__ __forceinline__ int attn_item_at(const AttnPlan& a, int q, int& pass) {
+  pass = q < a.q0 ? 0 : 1;
+  const int k = pass ? q - a.q0 : q;
+  if (k >= (pass ? a.n1 : a.n0)) return -1;
+  return blockIdx.x + k * gridDim.x;
+}
+
+// Consumer warps of an attention phase.  Warp w takes padded positions q = w / wpi + j * (8 / wpi)
+// of this CTA's item sequence (ring stage q / ips, slot q % ips); wpi warps share an item (each takes
+// every wpi-th query head) and the two warps of a stage release it with 4 arrivals each.  The next
+// item's first query is loaded while the current one is computed; tickets are batched per warp
+// (one lane per (tile, kv head) touched) and flushed at the end.
+template <typename WT, int DPL>
+__device__ void attn_consume(const Dims& D, const att::Tile* tb, int nt, const AttnPlan& A, int nst, int ips,
+                             int item_bytes, Ring& R, float* qb, int* s_fail, DevState* st) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int wpi = 2 / ips;
+  const int qh0 = warp % wpi;
+  const int qend = nst * ips, qstride = kNCW / wpi;
+  int pT = 0, pkh = 0, pc = 0, npend = 0;  // pending tickets: lane i holds entry i
+  auto flush = [&]() {
+    __threadfence();  // this warp's partials before its tickets
+    __syncwarp();
+    int last = 0;
+    if (lane < npend) {
+      const att::Tile& T = tb[pT];
+      const int old = atomicAdd(&T.tick[T.tick_off + pkh], pc);
+      last = old + pc == T.nch * wpi;
+    }
+    unsigned mask = __ballot_sync(0xffffffffu, last);
+    if (mask) __threadfence();  // the other warps' partials of the (tile, kv head) are visible
+    while (mask) {
+      const int b = __ffs(mask) - 1;
+      mask &= mask - 1;
+      const int T_ = __shfl_sync(0xffffffffu, pT, b), kh_ = __shfl_sync(0xffffffffu, pkh, b);
+      att::warp_merge<DPL>(D, tb[T_], kh_);
+    }
+    npend = 0;
+  };
+  att::Item it{0, 0, 0, 0};
+  int g = -1;
+  float qv[DPL];
+  auto fetch = [&](int qpos) {  // identity of the item at qpos and its first query head
+    int pass = 0;
+    g = qpos < qend ? attn_item_at(A, qpos, pass) : -1;
+    if (g >= 0) {
+      it = att::item_of_pass(tb, nt, pass, g, att::kWarpCK);
+      if (qh0 < tb[it.T].nq * D.gq) att::load_q<DPL>(D, tb[it.T], it.kh, qh0, qv);
+    }
+  };
+  fetch(warp / wpi);
+  for (int q = warp / wpi; q < qend; q += qstride) {
+    const att::Item cur = it;
+    const int gcur = g;
+    float qc[DPL];
+#pragma unroll
+    for (int e = 0; e < DPL; ++e) qc[e] = qv[e];
+    fetch(q + qstride);
+    const uint32_t ctr = R.ctr + (uint32_t)(q / ips);
+    const int s = ctr % kStages;
+    bool ok = !(R.failed || *(volatile int*)s_fail);
+    if (ok && !mbar_wait_bounded(&R.full[s], (ctr / kStages) & 1)) {
+      if (lane == 0) set_err(st, ERR_TIMEOUT, 31);
+      *(volatile int*)s_fail = 1;
+      ok = false;
+    }
+    if (ok && gcur >= 0) {
+      const unsigned char* slot = R.base + (size_t)s * kStageBytes + (size_t)(q % ips) * item_bytes;
+      att::warp_item<WT, DPL>(D, tb[cur.T], cur, reinterpret_cast<const WT*>(slot),
+                              reinterpret_cast<const WT*>(slot + item_bytes / 2), qb, qh0, wpi, qc);
+      const unsigned hit = __ballot_sync(0xffffffffu, lane < npend && pT == cur.T && pkh == cur.kh);
+      if (hit) {
+        if (lane == __ffs(hit) - 1) ++pc;
+      } else {
+        if (lane == npend) { pT = cur.T; pkh = cur.kh; pc = 1; }
+        ++npend;
+      }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive_cnt(&R.empty[s], kNCW / 2);
+    if (npend == 32) flush();
+  }
+  if (npend > 0 && !*(volatile int*)s_fail) flush();
 }
 
 template <typename WT>
-__global__ void __launch_bounds__(kThreads, 1) step_kernel(const __grid_constant__ StepParams p) {
+__global__ void __launch_bounds__(kStepThreads, 1) step_kernel(const __grid_constant__ StepParams p) {
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   unsigned char* ring =
       reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
   unsigned char* uni = ring + kStages * kStageBytes;
-  GG* gg_c = reinterpret_cast<GG*>(uni + p.union_bytes);  // consumers: 2 tables (this / next phase)
-  GG* gg_p = gg_c + 2 * kStepGroups;                       // producer
-  att::Tile* tiles = reinterpret_cast<att::Tile*>(gg_p + kStepGroups);  // consumers
-  att::Tile* tiles_p = tiles + kStepTiles;                                 // producer
+  GG* gg = reinterpret_cast<GG*>(uni + p.union_bytes);                // 2 tables (phase parity)
+  att::Tile* tiles = reinterpret_cast<att::Tile*>(gg + 2 * kStepGroups);  // 2 tables (phase parity)
+  LayerW* lw = reinterpret_cast<LayerW*>(  // target layers, then draft layers (16-byte aligned)
+      (reinterpret_cast<uintptr_t>(tiles + 2 * kStepTiles) + 15) & ~(uintptr_t)15);
 
   __shared__ __align__(8) uint64_t full_bar[kStages];
   __shared__ __align__(8) uint64_t empty_bar[kStages];
-  __shared__ int s_ng[2], s_gb[2], s_rb[2], s_ge[2], s_re[2];
-  __shared__ int s_skip, s_nt, s_items, s_fail, s_last, s_tok, s_slot, s_ok;
+  __shared__ int s_planned, s_produced;         // last phase resolved (planner) / streamed (producer)
+  __shared__ __align__(16) DevState s_sv;        // control block as the cycle starts
+  __shared__ __align__(16) Phase s_ph[2];        // descriptors of the phases by parity
+  __shared__ int s_ng[2], s_gb[2], s_rb[2], s_ge[2], s_re[2];  // GEMV: groups, this CTA's share
+  __shared__ int s_nt[2], s_nold[2], s_nnew[2];                // attention: tiles, item counts
+  __shared__ int s_fail, s_abort, s_tok, s_slot;
   __shared__ float rstd_s[16 * kMaxMT];
   __shared__ float wpart[kNCW];
   __shared__ Top2 hred[kNCW * 8][2];
@@ -111,56 +236,107 @@ __global__ void __launch_bounds__(kThreads, 1) step_kernel(const __grid_constant
   const EngineCfg& cfg = p.cfg;
   const Dims& D = cfg.D;
   DevState* st = cfg.B.st;
+  constexpr int ESZ = sizeof(WT);
+  // one attention item = K and V chunks of kWarpCK keys; ips items per ring stage (at most 2)
+  const int item_bytes = 2 * att::kWarpCK * D.hd * ESZ;
+  const int ips = kStageBytes / item_bytes >= 2 ? 2 : 1;
+  // snapshots: control block, per-layer tables
+  copy16(&s_sv, st, sizeof(DevState), tid, kStepThreads);
+  copy16(lw, cfg.B.tl, D.L * (int)sizeof(LayerW), tid, kStepThreads);
+  if (D.Ls > 0) copy16(lw + D.L, cfg.B.pl, D.Ls * (int)sizeof(LayerW), tid, kStepThreads);
   if (tid == 0) {
     for (int i = 0; i < kStages; ++i) {
       mbar_init(&full_bar[i], 1);
       mbar_init(&empty_bar[i], kNCW);
     }
     fence_mbar_init();
-    s_skip = (st->done || st->err) ? 1 : 0;
+    s_planned = -1;
+    s_produced = -1;
+    s_fail = 0;
+    s_abort = 0;
   }
   __syncthreads();
-  if (s_skip) return;  // every CTA reads the same control block: a uniform decision
+  if (s_sv.done || s_sv.err) return;  // every CTA reads the same control block: a uniform decision
+  const View vw{&s_sv, lw, lw + D.L};
   Ring R{ring, full_bar, empty_bar, 0u, false};
 
-  if (warp == kNCW) {
+  if (warp == kPlanWarp) {
+    // ------------------------------ planner warp ------------------------------
+    // Resolves phase ph+1 (descriptor, groups and this CTA's share, or attention tiles) while the
+    // consumers run phase ph; named barrier 4 with the consumers at every phase boundary.  Tables
+    // alternate by phase parity: those of phase ph are rewritten for ph+2 once the consumers have
+    // finished ph (barrier 4) and the producer has streamed it (s_produced).
+    auto plan = [&](int ph) {
+      const int b = ph & 1;
+      int ok = 1;
+      if (lane == 0 && ph >= 2 && !wait_progress(&s_produced, ph - 2)) {
+        set_err(st, ERR_TIMEOUT, 44);
+        ok = 0;
+      }
+      if (!__shfl_sync(0xffffffffu, ok, 0)) {  // the producer is gone: the consumers stop waiting
+        if (lane == 0) { s_abort = 1; st_release_cta(&s_planned, ph); }
+        __syncwarp();
+        return;
+      }
+      copy16(&s_ph[b], p.prog + ph, sizeof(Phase), lane, 32);
+      __syncwarp();
+      if (lane == 0) {
+        const Phase& P = s_ph[b];
+        if (P.type == PH_GEMV) {
+          s_ng[b] = resolve_parts(cfg, P.part, P.nparts, gg + b * kStepGroups, kStepGroups, vw);
+          span_of(gg + b * kStepGroups, s_ng[b], blockIdx.x, gridDim.x, s_gb[b], s_rb[b], s_ge[b], s_re[b]);
+        } else if (P.type == PH_ATTN) {
+          att::Tile* tb = tiles + b * kStepTiles;
+          int nt = 0, items = 0;
+          for (int i = 0; i < P.nparts && nt >= 0; ++i)
+            nt = att::add_tiles(D, cfg.B, P.part[i].lc, qt_of(P.part[i].lc), att::kWarpCK, tb, nt, &items,
+                                kStepTiles, &s_sv);
+          if (nt < 0) nt = 0;
+          s_nt[b] = nt;
+          att::split_items(D, tb, nt, att::kWarpCK, &s_nold[b], &s_nnew[b]);
+        }
+        st_release_cta(&s_planned, ph);  // releases the tables to the producer
+      }
+      __syncwarp();
+    };
+    plan(0);
+    named_bar(4, kNCT + 32);
+    for (int ph = 0; ph + 1 < p.nphases; ++ph) {
+      plan(ph + 1);
+      named_bar(4, kNCT + 32);
+    }
+    return;
+  }
+
+  if (warp == kProdWarp) {
     // ------------------------------ producer warp ------------------------------
     const uint64_t pol = l2_evict_first_policy();
-    // grid barriers completed before phase ph = ph; the generation word counts them
-    const unsigned g_start = __shfl_sync(0xffffffffu, lane == 0 ? ld_acquire(p.bar + 1) : 0u, 0);
-    constexpr int ESZ = sizeof(WT);
+    // arrivals before this launch; phase ph starts once the counter reaches base + ph * gridDim.x
+    const unsigned base = __shfl_sync(0xffffffffu, lane == 0 ? ld_acquire(p.bar) / gridDim.x : 0u, 0) * gridDim.x;
     for (int ph = 0; ph < p.nphases && !R.failed; ++ph) {
-      const Phase& P = p.prog[ph];
+      const int b = ph & 1;
+      int ok = 1;
+      if (lane == 0 && !wait_progress(&s_planned, ph)) {
+        set_err(st, ERR_TIMEOUT, 43);
+        ok = 0;
+      }
+      if (!__shfl_sync(0xffffffffu, ok, 0)) { R.failed = true; break; }
+      const Phase& P = s_ph[b];
       if (P.type == PH_GEMV) {
-        int gb = 0, rb = 0, ge = 0, re = 0;
-        if (lane == 0) {
-          const int ng = resolve_parts(cfg, P.part, P.nparts, gg_p, kStepGroups);
-          span_of(gg_p, ng, blockIdx.x, gridDim.x, gb, rb, ge, re);
-        }
-        __syncwarp();
-        gb = __shfl_sync(0xffffffffu, gb, 0); rb = __shfl_sync(0xffffffffu, rb, 0);
-        ge = __shfl_sync(0xffffffffu, ge, 0); re = __shfl_sync(0xffffffffu, re, 0);
-        produce_span<WT>(gg_p, gb, rb, ge, re, D.hd, R, st, pol, lane);
-        __syncwarp();  // gg_p is rewritten by the next phase
+        produce_span<WT>(gg + b * kStepGroups, s_gb[b], s_rb[b], s_ge[b], s_re[b], D.hd, R, st, pol, lane);
       } else if (P.type == PH_ATTN) {
-        // this CTA's items: chunks written in earlier cycles first, then -- once the QKV phase's
-        // grid barrier has passed -- the chunks holding this cycle's keys
-        int nt = 0, items = 0;
-        if (lane == 0) {
-          for (int i = 0; i < P.nparts && nt >= 0; ++i)
-            nt = att::add_tiles(D, cfg.B, P.part[i].lc, qt_of(P.part[i].lc), kStepChunk, tiles_p, nt, &items,
-                                kStepTiles);
-        }
-        __syncwarp();
-        nt = __shfl_sync(0xffffffffu, nt, 0);
-        items = __shfl_sync(0xffffffffu, items, 0);
-        if (nt <= 0) continue;
-        for (int pass = 0; pass < 2 && !R.failed; ++pass) {
-          if (pass == 1) {
+        const att::Tile* tb = tiles + b * kStepTiles;
+        const int nt = s_nt[b];
+        const AttnPlan A = attn_plan(s_nold[b], s_nnew[b], ips);
+        const int nst = nt > 0 ? A.stages(ips) : 0;
+        for (int k = 0; k < nst && !R.failed; ++k) {
+          if (k * ips == A.q0 && A.q1 > 0) {
+            // chunks holding this cycle's keys: wait for the QKV phase's grid barrier
             int ok = 1;
             if (lane == 0) {
               const uint64_t t0 = globaltimer_ns();
-              for (uint32_t it = 0; (ld_acquire(p.bar + 1) - g_start) < (unsigned)ph; ++it)
+              const unsigned target = base + (unsigned)ph * gridDim.x;
+              for (uint32_t it = 0; (int)(ld_acquire(p.bar) - target) < 0; ++it)
                 if ((it & 63u) == 63u && globaltimer_ns() - t0 > 2000000000ull) {
                   set_err(st, ERR_TIMEOUT, 41);
                   ok = 0;
@@ -169,109 +345,87 @@ __global__ void __launch_bounds__(kThreads, 1) step_kernel(const __grid_constant
             }
             if (!__shfl_sync(0xffffffffu, ok, 0)) { R.failed = true; break; }
           }
-          for (int item = blockIdx.x; item < items && !R.failed; item += gridDim.x) {
-            const att::Item it = att::item_of(tiles_p, nt, item, kStepChunk);
-            const att::Tile& Ti = tiles_p[it.T];
-            if (att::chunk_is_new(Ti, it.c, kStepChunk) != (pass == 1)) continue;
-            const int s = R.ctr % kStages;
-            if (R.ctr >= (uint32_t)kStages && !mbar_wait_bounded(&R.empty[s], ((R.ctr / kStages) - 1) & 1)) {
-              if (lane == 0) set_err(st, ERR_TIMEOUT, 42);
-              R.failed = true;
-              break;
-            }
-            if (lane == 0) {
-              const uint32_t bytes = (uint32_t)it.nk * D.hd * ESZ;
-              const size_t off = ((size_t)it.kh * D.max_seq + (size_t)it.c * kStepChunk) * D.hd * ESZ;
-              unsigned char* dst = R.base + (size_t)s * kStageBytes;
-              mbar_arrive_expect_tx(&R.full[s], 2 * bytes);
-              bulk_g2s(dst, Ti.kc + off, bytes, &R.full[s], pol);
-              bulk_g2s(dst + kKVHalf, Ti.vc + off, bytes, &R.full[s], pol);
-            }
-            __syncwarp();
-            ++R.ctr;
+          const int s = R.ctr % kStages;
+          if (R.ctr >= (uint32_t)kStages && !mbar_wait_bounded(&R.empty[s], ((R.ctr / kStages) - 1) & 1)) {
+            if (lane == 0) set_err(st, ERR_TIMEOUT, 42);
+            R.failed = true;
+            break;
           }
+          if (lane == 0) {
+            att::Item its[2];
+            int idx[2];
+            uint32_t tot = 0;
+            for (int h = 0; h < ips; ++h) {
+              int pass;
+              idx[h] = attn_item_at(A, k * ips + h, pass);
+              if (idx[h] >= 0) {
+                its[h] = att::item_of_pass(tb, nt, pass, idx[h], att::kWarpCK);
+                tot += 2u * (uint32_t)its[h].nk * D.hd * ESZ;
+              }
+            }
+            mbar_arrive_expect_tx(&R.full[s], tot);
+            for (int h = 0; h < ips; ++h) {
+              if (idx[h] < 0) continue;
+              const att::Tile& Ti = tb[its[h].T];
+              const uint32_t bytes = (uint32_t)its[h].nk * D.hd * ESZ;
+              const size_t off = ((size_t)its[h].kh * D.max_seq + (size_t)its[h].c * att::kWarpCK) * D.hd * ESZ;
+              unsigned char* dst = R.base + (size_t)s * kStageBytes + (size_t)h * item_bytes;
+              bulk_g2s(dst, Ti.kc + off, bytes, &R.full[s], pol);
+              bulk_g2s(dst + item_bytes / 2, Ti.vc + off, bytes, &R.full[s], pol);
+            }
+          }
+          __syncwarp();
+          ++R.ctr;
         }
       }
+      __syncwarp();
+      if (lane == 0) st_release_cta(&s_produced, ph);  // the tables of phase ph are no longer read
     }
+    if (lane == 0) st_release_cta(&s_produced, 1 << 30);  // leaving (done or failed)
     drain_ring(R, lane);
     return;
   }
 
   // ------------------------------ consumer warps ------------------------------
-  constexpr int NCT = kNCW * 32;
   uint64_t t_prev = (blockIdx.x == 0 && tid == 0) ? globaltimer_ns() : 0;
-  // groups (table ph & 1) or attention tiles of phase ph; they depend on the control block only,
-  // so phase ph+1 is prepared before the grid barrier that ends phase ph
-  auto prepare = [&](int ph) {
-    const Phase& P = p.prog[ph];
-    const int b = ph & 1;
-    if (P.type == PH_GEMV) {
-      s_ng[b] = resolve_parts(cfg, P.part, P.nparts, gg_c + b * kStepGroups, kStepGroups);
-      span_of(gg_c + b * kStepGroups, s_ng[b], blockIdx.x, gridDim.x, s_gb[b], s_rb[b], s_ge[b], s_re[b]);
-    } else if (P.type == PH_ATTN) {
-      int nt = 0, items = 0;
-      for (int i = 0; i < P.nparts && nt >= 0; ++i)
-        nt = att::add_tiles(D, cfg.B, P.part[i].lc, qt_of(P.part[i].lc), kStepChunk, tiles, nt, &items,
-                            kStepTiles);
-      s_nt = nt > 0 ? nt : 0;
-      s_items = nt > 0 ? items : 0;
-      s_fail = 0;
-    }
-  };
-  if (tid == 0) prepare(0);
-  named_bar(1, NCT);
+  // arrivals before this launch (fewer than gridDim.x of this launch can have been added yet)
+  const unsigned bar_base = tid == 0 ? (ld_acquire(p.bar) / gridDim.x) * gridDim.x : 0u;
+  named_bar(4, kNCT + 32);  // phase 0 resolved
   for (int ph = 0; ph < p.nphases; ++ph) {
-    const Phase& P = p.prog[ph];
     const int b = ph & 1;
+    const Phase& P = s_ph[b];
+    if (s_abort) R.failed = true;
     if (P.type == PH_GEMV) {
       Top2 loc[2];
       top2_init(loc[0]);
       top2_init(loc[1]);
-      consume_span<WT>(cfg, gg_c + b * kStepGroups, s_gb[b], s_rb[b], s_ge[b], s_re[b], R, uni, rstd_s, wpart,
+      consume_span<WT>(cfg, gg + b * kStepGroups, s_gb[b], s_rb[b], s_ge[b], s_re[b], R, uni, rstd_s, wpart,
                        loc);
       if (P.nparts > 0 && P.part[0].op == OP_HEAD)
         write_head_partial(loc, hred, cfg.B.head_part + (size_t)blockIdx.x * 8);
     } else if (P.type == PH_ATTN) {
-      // items from the ring, in the producer's order (older chunks, then this cycle's)
-      float* qs = reinterpret_cast<float*>(uni);
-      float* sc = qs + (size_t)p.attn_qh_max * D.hd;
-      float* m_s = sc + (size_t)p.attn_qh_max * kStepChunk;
-      float* l_s = m_s + p.attn_qh_max;
-      for (int pass = 0; pass < 2 && s_items > 0; ++pass) {
-        for (int item = blockIdx.x; item < s_items; item += gridDim.x) {
-          const att::Item it = att::item_of(tiles, s_nt, item, kStepChunk);
-          if (att::chunk_is_new(tiles[it.T], it.c, kStepChunk) != (pass == 1)) continue;
-          const int s = R.ctr % kStages;
-          if (!R.failed && !mbar_wait_bounded(&R.full[s], (R.ctr / kStages) & 1)) {
-            set_err(st, ERR_TIMEOUT, 31);
-            s_fail = 1;
-          }
-          named_bar(1, NCT);  // uniform decision
-          if (s_fail) R.failed = true;
-          if (!R.failed) {
-            const WT* kst = reinterpret_cast<const WT*>(R.base + (size_t)s * kStageBytes);
-            const WT* vst = reinterpret_cast<const WT*>(R.base + (size_t)s * kStageBytes + kKVHalf);
-            att::item_compute<WT, kStepChunk>(D, tiles[it.T], it, kst, vst, qs, sc, m_s, l_s, &s_last);
-          }
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&R.empty[s]);
-          ++R.ctr;
-        }
-      }
-    } else if (blockIdx.x == 0) {  // control: the last phase
+      const att::Tile* tb = tiles + b * kStepTiles;
+      const int nt = s_nt[b];
+      const AttnPlan A = attn_plan(s_nold[b], s_nnew[b], ips);
+      const int nst = nt > 0 ? A.stages(ips) : 0;
+      float* qb = reinterpret_cast<float*>(uni) + (size_t)warp * D.hd;
+      if (D.hd == 64) attn_consume<WT, 2>(D, tb, nt, A, nst, ips, item_bytes, R, qb, &s_fail, st);
+      else attn_consume<WT, 4>(D, tb, nt, A, nst, ips, item_bytes, R, qb, &s_fail, st);
+      R.ctr += (uint32_t)nst;
+      named_bar(1, kNCT);
+      if (s_fail) R.failed = true;
+    } else if (blockIdx.x == 0 && !R.failed) {  // control: the last phase
       Top2 (*red)[2] = reinterpret_cast<Top2(*)[2]>(uni);
-      if (P.type == PH_CTRL_CYCLE) ctl::control_cycle<WT>(D, cfg.B, red, s_tok, s_slot, NCT, 1);
-      else ctl::control_ar<WT>(D, cfg.B, red, s_tok, s_slot, NCT, 1);
+      if (P.type == PH_CTRL_CYCLE) ctl::control_cycle<WT>(D, cfg.B, red, s_tok, s_slot, kNCT, 1);
+      else ctl::control_ar<WT>(D, cfg.B, red, s_tok, s_slot, kNCT, 1);
     }
     if (ph + 1 < p.nphases) {
-      named_bar(1, NCT);  // this phase's writes are done; its tables / tiles are no longer read
-      if (tid == 0) {
-        const unsigned g0 = grid_arrive(p.bar);
-        prepare(ph + 1);
-        s_ok = grid_wait(p.bar, g0, st) ? 1 : 0;
+      named_bar(1, kNCT);  // this phase's writes are done
+      if (tid == 0 && !s_abort) {
+        grid_arrive(p.bar);
+        if (!grid_wait(p.bar, bar_base + (unsigned)(ph + 1) * gridDim.x, st)) s_abort = 1;
       }
-      named_bar(1, NCT);
-      if (!s_ok) break;
+      named_bar(4, kNCT + 32);  // with the planner: phase ph+1 resolved; s_abort visible
     }
     if (p.phase_ns && blockIdx.x == 0 && tid == 0) {
       const uint64_t t = globaltimer_ns();
@@ -281,18 +435,30 @@ __global__ void __launch_bounds__(kThreads, 1) step_kernel(const __grid_constant
   }
 }
 
+static_assert(sizeof(Phase) % 16 == 0, "phase descriptors are copied in 16-byte pieces");
+static_assert(sizeof(DevState) % 16 == 0 && sizeof(LayerW) % 16 == 0, "16-byte snapshots");
+
 }  // namespace
+
+// Union scratch: tensor-core partial tiles (GEMV), per-warp query vectors (attention), top-2 merge
+// (control).
+static size_t step_union_bytes(const Dims& D) {
+  size_t uni = (size_t)kMmaScratch;
+  const size_t q = (size_t)kNCW * D.hd * sizeof(float);
+  if (uni < q) uni = q;
+  if (uni < (size_t)kNCW * 32 * 2 * sizeof(Top2)) uni = (size_t)kNCW * 32 * 2 * sizeof(Top2);
+  return (uni + 127) & ~(size_t)127;
+}
 
 size_t step_smem_bytes(const Dims& D) {
   const int esz = D.dtype == SPD_DTYPE_BF16 ? 2 : 4;
-  if ((size_t)kStepChunk * D.hd * esz > (size_t)kKVHalf) return 0;  // a K or V chunk fills half a stage
-  size_t uni = att::smem_bytes(D.hd, D.gq, esz, kAttnQT, kStepChunk) - (size_t)2 * kStepChunk * D.hd * esz;
-  if (uni < (size_t)kMmaScratch) uni = (size_t)kMmaScratch;
-  if (uni < (size_t)kNCW * 32 * 2 * sizeof(Top2)) uni = (size_t)kNCW * 32 * 2 * sizeof(Top2);
-  uni = (uni + 127) & ~(size_t)127;
-  const size_t total = 1024 + (size_t)kStages * kStageBytes + uni + 3 * kStepGroups * sizeof(GG) +
-                       (size_t)2 * kStepTiles * sizeof(att::Tile);
-  const size_t static_bytes = 8 * 1024;  // barriers, per-vector 1/rms, head merge scratch
+  // an attention item (K and V chunks of kWarpCK keys) must fit one ring stage; hd 64 or 128 (other
+  // head sizes run on the per-operator launches)
+  if ((size_t)2 * att::kWarpCK * D.hd * esz > (size_t)kStageBytes) return 0;
+  if (D.hd != 64 && D.hd != 128) return 0;
+  const size_t total = 1024 + (size_t)kStages * kStageBytes + step_union_bytes(D) + 2 * kStepGroups * sizeof(GG) +
+                       (size_t)2 * kStepTiles * sizeof(att::Tile) + 16 + (size_t)(D.L + D.Ls) * sizeof(LayerW);
+  const size_t static_bytes = 8 * 1024;  // barriers, snapshots, per-vector 1/rms, head merge scratch
   return total + static_bytes <= 227 * 1024 ? total : 0;
 }
 
@@ -315,16 +481,11 @@ cudaError_t launch_step(const Dims& D, const Bufs& B, const LaunchCfg& lcfg, con
   p.nphases = nphases;
   p.bar = bar;
   p.phase_ns = phase_ns;
-  const int esz = D.dtype == SPD_DTYPE_BF16 ? 2 : 4;
-  size_t uni = att::smem_bytes(D.hd, D.gq, esz, kAttnQT, kStepChunk) - (size_t)2 * kStepChunk * D.hd * esz;
-  if (uni < (size_t)kMmaScratch) uni = (size_t)kMmaScratch;
-  if (uni < (size_t)kNCW * 32 * 2 * sizeof(Top2)) uni = (size_t)kNCW * 32 * 2 * sizeof(Top2);
-  p.union_bytes = (int)((uni + 127) & ~(size_t)127);
-  p.attn_qh_max = kAttnQT * D.gq;
+  p.union_bytes = (int)step_union_bytes(D);
   cudaLaunchConfig_t cfg;
   memset(&cfg, 0, sizeof(cfg));
   cfg.gridDim = dim3(num_sms());
-  cfg.blockDim = dim3(kThreads);
+  cfg.blockDim = dim3(kStepThreads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
