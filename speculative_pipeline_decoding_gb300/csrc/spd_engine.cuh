@@ -563,6 +563,25 @@ __device__ void mma_tile(const EngineCfg& p, const GG& G, int r, int tr, Ring& R
     }
   };
   load_raw(0);
+  // epilogue inputs of this thread's output items of m-tile 0 (the residual values, or the rotary
+  // cos / sin of the pairs), loaded now so that the tile end waits for no global load
+  const bool pairs = G.nw != 2 && G.epi == EPI_QKV && r < G.seg2;
+  const int nitem = (G.nw == 2 || pairs) ? 32 * 16 : 64 * 16;
+  float pre[4][2];
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    pre[k][0] = pre[k][1] = 0.f;
+    const int idx = tid + k * NCT, m = idx >> 4, v = idx & 15;
+    if (MT == 1 && idx < nitem && v < nv && m < tr) {
+      if (G.epi == EPI_RESID) {
+        pre[k][0] = __ldcg(G.y + (size_t)((G.yrow0 + v) % G.yring) * G.ystride + r + m);
+      } else if (pairs) {
+        const size_t at = (size_t)(G.pos0 + v - 1) * (hd / 2) + phys_row(G, r + m, hd) % hd;
+        pre[k][0] = __ldg(p.B.rope_cos + at);
+        pre[k][1] = __ldg(p.B.rope_sin + at);
+      }
+    }
+  }
   const int jb = 4 * warp + (lane >> 3);  // ldmatrix chunk of this lane (two k-steps x two halves)
   for (int c0 = 0; c0 < gcols; c0 += CW) {
     uint32_t ah[MT][2][4], al[MT][2][4];
@@ -627,23 +646,131 @@ __device__ void mma_tile(const EngineCfg& p, const GG& G, int r, int tr, Ring& R
       return sum;
     };
     if (!R.failed) {
-      if (G.nw == 2 || (G.epi == EPI_QKV && r < G.seg2)) {  // gate/up, or rotary pairs
-        const bool pair = G.nw != 2;
-        for (int idx = tid; idx < 32 * 16; idx += NCT) {
+      if (G.nw == 2 || pairs) {  // gate/up, or rotary pairs
+#pragma unroll
+        for (int k = 0; k < 2; ++k) {
+          const int idx = tid + k * NCT;
           const int m = idx >> 4, vv = idx & 15, v = mt * 16 + vv;
           if (v < nv && m < tr)
-            epilogue<WT>(p, G, v, pair ? phys_row(G, r + m, hd) : r + m, tot(m, vv), tot(m + 32, vv), pair,
-                         loc);
+            epilogue<WT>(p, G, v, pairs ? phys_row(G, r + m, hd) : r + m, tot(m, vv), tot(m + 32, vv), pairs,
+                         loc, (MT == 1 && pairs) ? pre[k] : nullptr);
         }
       } else {
-        for (int idx = tid; idx < 64 * 16; idx += NCT) {
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const int idx = tid + k * NCT;
           const int m = idx >> 4, vv = idx & 15, v = mt * 16 + vv;
-          if (v < nv && m < tr) epilogue<WT>(p, G, v, r + m, tot(m, vv), 0.f, false, loc);
+          if (v < nv && m < tr)
+            epilogue<WT>(p, G, v, r + m, tot(m, vv), 0.f, false, loc,
+                         (MT == 1 && G.epi == EPI_RESID) ? pre[k] : nullptr);
         }
       }
     }
   }
   named_bar(1, NCT);  // `red` is rewritten by the next tile
+}
+
+// Single-vector tile: output rows r..r+tr-1 of G, its column-chunk stages from the ring, then the
+// epilogue.  The input vector comes from `xs` (staged in shared memory, already normalised) or,
+// when null, from G.x through L1 (times rstd and the norm weight when the group has a norm).
+template <typename WT>
+__device__ void sv_tile(const EngineCfg& p, const GG& G, int r, int tr, Ring& R, const float* xs, float rstd,
+                        Top2* loc) {
+  constexpr int VEC = WTraits<WT>::kVec;
+  constexpr int CW = 512 / sizeof(WT);
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int hd = p.D.hd;
+  DevState* st = p.B.st;
+  // ---------------- single-vector path ----------------
+  const float* xr = G.x + (size_t)(G.xrow0 % G.xring) * G.xstride;
+  // the epilogue inputs of this lane's output row, loaded now: they are in registers when the
+  // tile ends (the residual value, or the rotary cos / sin of the pair)
+  float pre[2] = {0.f, 0.f};
+  if (lane < 8 && G.nw != 2) {
+    const int slot = warp + 8 * lane;
+    if (G.epi == EPI_QKV && r < G.seg2) {
+      if (lane < 4) {
+        const int i = phys_row(G, r + slot, hd) % hd;
+        const size_t at = (size_t)(G.pos0 - 1) * (hd / 2) + i;
+        pre[0] = __ldg(p.B.rope_cos + at);
+        pre[1] = __ldg(p.B.rope_sin + at);
+      }
+    } else if (G.epi == EPI_RESID && slot < tr) {
+      pre[0] = __ldcg(G.y + (size_t)(G.yrow0 % G.yring) * G.ystride + r + slot);
+    }
+  }
+  float acc[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) acc[i] = 0.f;
+  for (int c0 = 0; c0 < G.cols; c0 += CW) {
+    const int s = R.ctr % kStages;
+    if (!R.failed && !mbar_wait_bounded(&R.full[s], (R.ctr / kStages) & 1)) {
+      if (lane == 0) set_err(st, ERR_TIMEOUT, 50);
+      R.failed = true;
+    }
+    if (!R.failed) {
+      const unsigned char* sb = R.base + (size_t)s * kStageBytes;
+      uint4 wq[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {  // all eight weight chunks first (independent loads)
+        const int slot = warp + 8 * i;
+        const bool ok = G.nw == 2 ? ((slot & 31) < tr) : (slot < tr);
+        wq[i] = ok ? *reinterpret_cast<const uint4*>(sb + stage_off(slot, lane)) : make_uint4(0, 0, 0, 0);
+      }
+      const int col = c0 + VEC * lane;
+      float xv[VEC];
+      if (col < G.cols && xs) {
+#pragma unroll
+        for (int e = 0; e < VEC; e += 4) {
+          const float4 q = *reinterpret_cast<const float4*>(xs + col + e);
+          xv[e] = q.x; xv[e + 1] = q.y; xv[e + 2] = q.z; xv[e + 3] = q.w;
+        }
+      } else if (col < G.cols) {
+#pragma unroll
+        for (int e = 0; e < VEC; e += 4) {
+          float4 q = *reinterpret_cast<const float4*>(xr + col + e);
+          if (G.normw) {
+            const float4 n4 = *reinterpret_cast<const float4*>(G.normw + col + e);
+            q.x = q.x * rstd * n4.x; q.y = q.y * rstd * n4.y;
+            q.z = q.z * rstd * n4.z; q.w = q.w * rstd * n4.w;
+          }
+          xv[e] = q.x; xv[e + 1] = q.y; xv[e + 2] = q.z; xv[e + 3] = q.w;
+        }
+      } else {
+#pragma unroll
+        for (int e = 0; e < VEC; ++e) xv[e] = 0.f;
+      }
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        float wf[VEC];
+        WTraits<WT>::unpack(wq[i], wf);
+#pragma unroll
+        for (int e = 0; e < VEC; ++e) acc[i] = fmaf(wf[e], xv[e], acc[i]);
+      }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&R.empty[s]);
+    ++R.ctr;
+  }
+  float sums[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) sums[i] = warp_sum(acc[i]);
+  if (!R.failed && lane < 8) {  // lane i finishes slot warp + 8i (and its partner slot + 32)
+    float y0 = 0.f, y1 = 0.f;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      if (k == lane) y0 = sums[k];
+      if (k == lane + 4) y1 = sums[k];
+    }
+    const int slot = warp + 8 * lane;
+    if (G.nw == 2) {
+      if (lane < 4 && slot < tr) epilogue<WT>(p, G, 0, r + slot, y0, y1, false, loc);
+    } else if (G.epi == EPI_QKV && r < G.seg2) {
+      if (lane < 4) epilogue<WT>(p, G, 0, phys_row(G, r + slot, hd), y0, y1, true, loc, pre);
+    } else if (slot < tr) {
+      epilogue<WT>(p, G, 0, r + slot, y0, 0.f, false, loc, G.epi == EPI_RESID ? pre : nullptr);
+    }
+  }
 }
 
 // Consumer warps (named barrier 1, 256 threads): consume every stage of the span and run the
@@ -720,96 +847,7 @@ static __device__ void consume_span(const EngineCfg& p, const GG* gg, int gb, in
       last_g = g;
     }
     if (!G.mma) {
-      // ---------------- single-vector path ----------------
-      const float* xr = G.x + (size_t)(G.xrow0 % G.xring) * G.xstride;
-      // the epilogue inputs of this lane's output row, loaded now: they are in registers when the
-      // tile ends (the residual value, or the rotary cos / sin of the pair)
-      float pre[2] = {0.f, 0.f};
-      if (lane < 8 && G.nw != 2) {
-        const int slot = warp + 8 * lane;
-        if (G.epi == EPI_QKV && r < G.seg2) {
-          if (lane < 4) {
-            const int i = phys_row(G, r + slot, hd) % hd;
-            const size_t at = (size_t)(G.pos0 - 1) * (hd / 2) + i;
-            pre[0] = __ldg(p.B.rope_cos + at);
-            pre[1] = __ldg(p.B.rope_sin + at);
-          }
-        } else if (G.epi == EPI_RESID && slot < tr) {
-          pre[0] = __ldcg(G.y + (size_t)(G.yrow0 % G.yring) * G.ystride + r + slot);
-        }
-      }
-      float acc[8];
-#pragma unroll
-      for (int i = 0; i < 8; ++i) acc[i] = 0.f;
-      for (int c0 = 0; c0 < G.cols; c0 += CW) {
-        const int s = R.ctr % kStages;
-        if (!R.failed && !mbar_wait_bounded(&R.full[s], (R.ctr / kStages) & 1)) {
-          if (lane == 0) set_err(st, ERR_TIMEOUT, 50);
-          R.failed = true;
-        }
-        if (!R.failed) {
-          const unsigned char* sb = R.base + (size_t)s * kStageBytes;
-          uint4 wq[8];
-#pragma unroll
-          for (int i = 0; i < 8; ++i) {  // all eight weight chunks first (independent loads)
-            const int slot = warp + 8 * i;
-            const bool ok = G.nw == 2 ? ((slot & 31) < tr) : (slot < tr);
-            wq[i] = ok ? *reinterpret_cast<const uint4*>(sb + stage_off(slot, lane)) : make_uint4(0, 0, 0, 0);
-          }
-          const int col = c0 + VEC * lane;
-          float xv[VEC];
-          if (col < G.cols && xs_on) {
-#pragma unroll
-            for (int e = 0; e < VEC; e += 4) {
-              const float4 q = *reinterpret_cast<const float4*>(xs + col + e);
-              xv[e] = q.x; xv[e + 1] = q.y; xv[e + 2] = q.z; xv[e + 3] = q.w;
-            }
-          } else if (col < G.cols) {
-#pragma unroll
-            for (int e = 0; e < VEC; e += 4) {
-              float4 q = *reinterpret_cast<const float4*>(xr + col + e);
-              if (G.normw) {
-                const float4 n4 = *reinterpret_cast<const float4*>(G.normw + col + e);
-                q.x = q.x * rstd * n4.x; q.y = q.y * rstd * n4.y;
-                q.z = q.z * rstd * n4.z; q.w = q.w * rstd * n4.w;
-              }
-              xv[e] = q.x; xv[e + 1] = q.y; xv[e + 2] = q.z; xv[e + 3] = q.w;
-            }
-          } else {
-#pragma unroll
-            for (int e = 0; e < VEC; ++e) xv[e] = 0.f;
-          }
-#pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            float wf[VEC];
-            WTraits<WT>::unpack(wq[i], wf);
-#pragma unroll
-            for (int e = 0; e < VEC; ++e) acc[i] = fmaf(wf[e], xv[e], acc[i]);
-          }
-        }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&R.empty[s]);
-        ++R.ctr;
-      }
-      float sums[8];
-#pragma unroll
-      for (int i = 0; i < 8; ++i) sums[i] = warp_sum(acc[i]);
-      if (!R.failed && lane < 8) {  // lane i finishes slot warp + 8i (and its partner slot + 32)
-        float y0 = 0.f, y1 = 0.f;
-#pragma unroll
-        for (int k = 0; k < 8; ++k) {
-          if (k == lane) y0 = sums[k];
-          if (k == lane + 4) y1 = sums[k];
-        }
-        const int slot = warp + 8 * lane;
-        if (G.nw == 2) {
-          if (lane < 4 && slot < tr) epilogue<WT>(p, G, 0, r + slot, y0, y1, false, loc);
-        } else if (G.epi == EPI_QKV && r < G.seg2) {
-          if (lane < 4) epilogue<WT>(p, G, 0, phys_row(G, r + slot, hd), y0, y1, true, loc, pre);
-        } else if (slot < tr) {
-          epilogue<WT>(p, G, 0, r + slot, y0, 0.f, false, loc, G.epi == EPI_RESID ? pre : nullptr);
-        }
-      }
+      sv_tile<WT>(p, G, r, tr, R, xs_on ? xs : nullptr, rstd, loc);
     } else if (G.nv <= 16) {
       mma_tile<WT, 1>(p, G, r, tr, R, scratch, rstd_s, loc);
     } else {
