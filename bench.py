@@ -45,6 +45,28 @@ def parse():
     return ap.parse_args()
 
 
+def step_kernel_traffic_ratio():
+    """DRAM bytes / algorithmic bytes of one ncu-captured step-kernel launch, from the committed profile
+    summary -- only while the CUDA sources are the ones that were profiled (else None)."""
+    import hashlib
+    src = os.path.join(ROOT, "speculative_pipeline_decoding_gb300", "csrc")
+    prof = os.path.join(ROOT, "profiles", "step_kernel_dense1.5b_n8_sections.md")
+    try:
+        h = hashlib.sha1()
+        for f in sorted(os.listdir(src)):
+            if f.endswith((".cu", ".cuh")):
+                with open(os.path.join(src, f), "rb") as fh:
+                    h.update(fh.read())
+        with open(prof) as fh:
+            for line in fh:
+                parts = line.split()
+                if len(parts) == 4 and parts[0] == "traffic_ratio:" and parts[2] == "sources_sha1:":
+                    return float(parts[1]) if parts[3] == h.hexdigest() else None
+    except OSError:
+        return None
+    return None
+
+
 def measured_peaks():
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as fh:
@@ -349,6 +371,7 @@ def main_spd(args):
     # the cycle's algorithmic bytes, its duration the CUDA-event cycle time of the timed region
     peak, peak_src = measured_peaks()
     achieved = step_bytes / cycles / (t_cycle / 1e3) / 1e9
+    traffic_ratio = step_kernel_traffic_ratio()
 
     # --- end to end through the public API with host buffers ---
     prompt_np = __import__("numpy").asarray(prompt, dtype="int32")
@@ -387,8 +410,12 @@ def main_spd(args):
                    "parallelism": f"replicas x{world}"},
         "roofline": {"bound": "hbm", "kernel": "step_kernel (one SPD cycle per launch)",
                      "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
-                     "peak_source": peak_src, "traffic": None, "launches": args.steps * cycles,
-                     "bytes_per_launch": step_bytes / cycles},
+                     "peak_source": peak_src,
+                     "traffic": None if traffic_ratio is None else traffic_ratio * step_bytes / cycles,
+                     "traffic_source": "ncu dram bytes / algorithmic bytes of one captured launch "
+                                       "(profiles/step_kernel_dense1.5b_n8_sections.md) x bytes_per_launch"
+                                       if traffic_ratio is not None else "no capture of the current sources",
+                     "launches": args.steps * cycles, "bytes_per_launch": step_bytes / cycles},
         "cpu_baseline": cpu,
         "e2e": {"value": e2e_val, "unit": "tokens/s", "h2d_bytes_per_step": 4 * P + 5 * (G - 1),
                 "d2h_bytes_per_step": 4 * G, "includes": "prefill + decode per step"},
@@ -435,12 +462,19 @@ def main_profile(args):
     eng.set_draft_override(P + 2, ar.tolist()[1:], modes)
     t0 = time.time()
     exits = 0
+    st = eng.state()
+    t_prev, a_prev = st["t"], st["a"]
+    per_cycle = []  # (t, fill) before the cycle, exited, algorithmic bytes
     for _ in range(args.profile_cycles):
-        exits += eng.cycle()["exited"]
+        info = eng.cycle()
+        exits += info["exited"]
+        nbytes = sum(eng.cycle_bytes(t_prev, a_prev, bool(info["exited"]), True).values())
+        per_cycle.append([t_prev, a_prev, info["exited"], nbytes])
+        t_prev, a_prev = info["t"], info["a"]
     torch.cuda.synchronize()
     print(json.dumps({"profile_cycles": args.profile_cycles, "ar_steps_before": G, "exits": exits,
-                      "workload": w.name,
-                      "wall_s": time.time() - t0}))
+                      "workload": w.name, "wall_s": time.time() - t0,
+                      "cycles_t_fill_exited_bytes": per_cycle}))
     eng.close()
     return 0
 
