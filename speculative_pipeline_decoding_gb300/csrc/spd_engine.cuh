@@ -289,7 +289,9 @@ static __device__ void locate(const GG* gg, int ng, long long X, int& g, int& r)
   if (g >= ng) { g = ng; r = 0; return; }
   const long long rc = rowcost(gg[g]);
   const long long exact = (X - gg[g].cost0) / rc;
-  const int gran = (gg[g].epi == EPI_QKV && exact < gg[g].seg2) ? kSlots : kBoxRows;
+  // whole 64-row tiles in the rotary region and for tensor-core groups (a tile's stages cost the
+  // same however many of its rows are used); 32-row boxes elsewhere
+  const int gran = ((gg[g].epi == EPI_QKV && exact < gg[g].seg2) || gg[g].mma) ? (int)gg[g].tr : kBoxRows;
   r = (int)(((X - gg[g].cost0) + rc * gran / 2) / (rc * gran)) * gran;
   if (gg[g].epi == EPI_QKV && r > gg[g].seg2 && exact < gg[g].seg2) r = gg[g].seg2;
   if (r >= gg[g].rows) { ++g; r = 0; }
@@ -344,8 +346,9 @@ __device__ __forceinline__ void ldmatrix_x4(uint32_t addr, uint32_t& r0, uint32_
                : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3) : "r"(addr));
 }
 
+// no side effects beyond its outputs: not volatile, so that independent MMAs can be interleaved
 __device__ __forceinline__ void mma_bf16(float* c, const uint32_t* a, uint32_t b0, uint32_t b1) {
-  asm volatile(
+  asm(
       "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
       "{%0,%1,%2,%3};"
       : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
@@ -443,9 +446,16 @@ __device__ __forceinline__ int tile_rows(const GG& G, int r, int last) {
 }
 
 // Producer warp: one stage = the 64 weight slots of tile row `r` (tr output rows) at column c0.
+// A single-vector tile of at most 32 rows (one weight per row, outside the rotary region) streams
+// "wide": a stage holds its 32 rows x 1024 bytes (8 boxes across) instead of 64 rows x 512 bytes, so
+// every stage carries 32 KB.  A lane still meets its column chunks in the same order.
+__device__ __forceinline__ bool wide_tile(const GG& G, int r, int tr) {
+  return !G.mma && G.nw == 1 && tr <= kBoxRows && !(G.epi == EPI_QKV && r < G.seg2);
+}
+
 template <typename WT>
 __device__ __forceinline__ void issue_stage(const GG& G, int r, int tr, int c0, int hd, Ring& R, DevState* st,
-                                            uint64_t pol, int lane) {
+                                            uint64_t pol, int lane, bool wide = false) {
   constexpr int BOXC = 128 / sizeof(WT);   // columns per box
   const int nrb = G.nw == 2 ? 2 : (tr + kBoxRows - 1) / kBoxRows;  // row boxes
   const CUtensorMap* m0;
@@ -467,9 +477,12 @@ __device__ __forceinline__ void issue_stage(const GG& G, int r, int tr, int c0, 
     R.failed = true;
     return;
   }
-  if (lane == 0) mbar_arrive_expect_tx(&R.full[s], (uint32_t)(nrb * 4 * kBoxBytes));
+  if (lane == 0) mbar_arrive_expect_tx(&R.full[s], (uint32_t)((wide ? 8 : nrb * 4) * kBoxBytes));
   __syncwarp();
-  if (lane < nrb * 4) {
+  if (wide) {
+    if (lane < 8)
+      tma_box(R.base + (size_t)s * kStageBytes + (size_t)lane * kBoxBytes, m0, c0 + lane * BOXC, y0, &R.full[s], pol);
+  } else if (lane < nrb * 4) {
     const int rbx = lane >> 2, cb = lane & 3;
     tma_box(R.base + (size_t)s * kStageBytes + (size_t)(rbx * 4 + cb) * kBoxBytes, rbx ? m1 : m0,
             c0 + cb * BOXC, rbx ? y1 : y0, &R.full[s], pol);
@@ -489,9 +502,10 @@ __device__ void produce_span(const GG* gg, int gb, int rb, int ge, int re, int h
     const int tr = tile_rows(G, r, last);
     const int srows = kSlots / G.nw;                       // output rows per 64-slot stage
     const int nsl = G.mma ? (tr + srows - 1) / srows : 1;  // slices of the tile
-    for (int c0 = 0; c0 < G.cols && !R.failed; c0 += CW)
+    const bool wide = wide_tile(G, r, tr);
+    for (int c0 = 0; c0 < G.cols && !R.failed; c0 += wide ? 2 * CW : CW)
       for (int j = 0; j < nsl && !R.failed; ++j)
-        issue_stage<WT>(G, r + j * srows, min(srows, tr - j * srows), c0, hd, R, st, pol, lane);
+        issue_stage<WT>(G, r + j * srows, min(srows, tr - j * srows), c0, hd, R, st, pol, lane, wide);
     r += tr;
     if (r >= last) { ++g; r = 0; }
   }
@@ -607,18 +621,29 @@ __device__ void mma_tile(const EngineCfg& p, const GG& G, int r, int tr, Ring& R
     }
     if (!R.failed) {
       const uint32_t sb = smem_u32(R.base + (size_t)s * kStageBytes);
+      // weight fragments four n-tiles at a time, then the MMAs interleaved over those four
+      // independent accumulators (each accumulator still takes hi/lo x k-step in the same order)
 #pragma unroll
-      for (int nt = 0; nt < 8; ++nt) {
-        const bool ok = G.nw == 2 ? (((nt * 8) & 31) < tr) : (nt * 8 < tr);
-        if (ok) {
-          uint32_t b0, b1, b2, b3;
-          ldmatrix_x4(sb + stage_off(nt * 8 + (lane & 7), jb), b0, b1, b2, b3);
+      for (int nh = 0; nh < 8; nh += 4) {
+        uint32_t bq[4][4];
 #pragma unroll
-          for (int mt = 0; mt < MT; ++mt) {
-            mma_bf16(acc[nt][mt], ah[mt][0], b0, b1);
-            mma_bf16(acc[nt][mt], al[mt][0], b0, b1);
-            mma_bf16(acc[nt][mt], ah[mt][1], b2, b3);
-            mma_bf16(acc[nt][mt], al[mt][1], b2, b3);
+        for (int u = 0; u < 4; ++u) {
+          const int nt = nh + u;
+          const bool ok = G.nw == 2 ? (((nt * 8) & 31) < tr) : (nt * 8 < tr);
+          if (ok) ldmatrix_x4(sb + stage_off(nt * 8 + (lane & 7), jb), bq[u][0], bq[u][1], bq[u][2], bq[u][3]);
+          else bq[u][0] = bq[u][1] = bq[u][2] = bq[u][3] = 0u;
+        }
+#pragma unroll
+        for (int mt = 0; mt < MT; ++mt) {
+#pragma unroll
+          for (int step = 0; step < 4; ++step) {
+            const uint32_t* fa = (step & 1) ? al[mt][step >> 1] : ah[mt][step >> 1];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+              const int nt = nh + u;
+              const bool ok = G.nw == 2 ? (((nt * 8) & 31) < tr) : (nt * 8 < tr);
+              if (ok) mma_bf16(acc[nt][mt], fa, bq[u][(step >> 1) * 2], bq[u][(step >> 1) * 2 + 1]);
+            }
           }
         }
       }
@@ -702,7 +727,35 @@ __device__ void sv_tile(const EngineCfg& p, const GG& G, int r, int tr, Ring& R,
   float acc[8];
 #pragma unroll
   for (int i = 0; i < 8; ++i) acc[i] = 0.f;
-  for (int c0 = 0; c0 < G.cols; c0 += CW) {
+  // the lane's VEC input values at column `col` (normalised when the group has a norm), 0 beyond
+  auto load_x = [&](int col, float* xv) {
+    if (col < G.cols && xs) {
+#pragma unroll
+      for (int e = 0; e < VEC; e += 4) {
+        const float4 q = *reinterpret_cast<const float4*>(xs + col + e);
+        xv[e] = q.x; xv[e + 1] = q.y; xv[e + 2] = q.z; xv[e + 3] = q.w;
+      }
+    } else if (col < G.cols) {
+#pragma unroll
+      for (int e = 0; e < VEC; e += 4) {
+        float4 q = *reinterpret_cast<const float4*>(xr + col + e);
+        if (G.normw) {
+          const float4 n4 = *reinterpret_cast<const float4*>(G.normw + col + e);
+          q.x = q.x * rstd * n4.x; q.y = q.y * rstd * n4.y;
+          q.z = q.z * rstd * n4.z; q.w = q.w * rstd * n4.w;
+        }
+        xv[e] = q.x; xv[e + 1] = q.y; xv[e + 2] = q.z; xv[e + 3] = q.w;
+      }
+    } else {
+#pragma unroll
+      for (int e = 0; e < VEC; ++e) xv[e] = 0.f;
+    }
+  };
+  // tall stage: 64 rows x 512 bytes, warp w rows w + 8i (i < 8), lane l chunk l.  Wide stage:
+  // 32 rows x 1024 bytes, warp w rows w + 8i (i < 4), lane l chunks l and l + 32 -- the same
+  // chunks, in the same order, as two consecutive tall stages
+  const bool wide = wide_tile(G, r, tr);
+  for (int c0 = 0; c0 < G.cols; c0 += wide ? 2 * CW : CW) {
     const int s = R.ctr % kStages;
     if (!R.failed && !mbar_wait_bounded(&R.full[s], (R.ctr / kStages) & 1)) {
       if (lane == 0) set_err(st, ERR_TIMEOUT, 50);
@@ -713,39 +766,37 @@ __device__ void sv_tile(const EngineCfg& p, const GG& G, int r, int tr, Ring& R,
       uint4 wq[8];
 #pragma unroll
       for (int i = 0; i < 8; ++i) {  // all eight weight chunks first (independent loads)
-        const int slot = warp + 8 * i;
-        const bool ok = G.nw == 2 ? ((slot & 31) < tr) : (slot < tr);
-        wq[i] = ok ? *reinterpret_cast<const uint4*>(sb + stage_off(slot, lane)) : make_uint4(0, 0, 0, 0);
+        const int slot = wide ? warp + 8 * (i & 3) : warp + 8 * i;
+        const int j = wide ? lane + 32 * (i >> 2) : lane;
+        const bool ok = wide ? slot < tr : (G.nw == 2 ? ((slot & 31) < tr) : (slot < tr));
+        wq[i] = ok ? *reinterpret_cast<const uint4*>(sb + stage_off(slot, j)) : make_uint4(0, 0, 0, 0);
       }
-      const int col = c0 + VEC * lane;
       float xv[VEC];
-      if (col < G.cols && xs) {
+      load_x(c0 + VEC * lane, xv);
+      if (!wide) {
 #pragma unroll
-        for (int e = 0; e < VEC; e += 4) {
-          const float4 q = *reinterpret_cast<const float4*>(xs + col + e);
-          xv[e] = q.x; xv[e + 1] = q.y; xv[e + 2] = q.z; xv[e + 3] = q.w;
-        }
-      } else if (col < G.cols) {
+        for (int i = 0; i < 8; ++i) {
+          float wf[VEC];
+          WTraits<WT>::unpack(wq[i], wf);
 #pragma unroll
-        for (int e = 0; e < VEC; e += 4) {
-          float4 q = *reinterpret_cast<const float4*>(xr + col + e);
-          if (G.normw) {
-            const float4 n4 = *reinterpret_cast<const float4*>(G.normw + col + e);
-            q.x = q.x * rstd * n4.x; q.y = q.y * rstd * n4.y;
-            q.z = q.z * rstd * n4.z; q.w = q.w * rstd * n4.w;
-          }
-          xv[e] = q.x; xv[e + 1] = q.y; xv[e + 2] = q.z; xv[e + 3] = q.w;
+          for (int e = 0; e < VEC; ++e) acc[i] = fmaf(wf[e], xv[e], acc[i]);
         }
       } else {
 #pragma unroll
-        for (int e = 0; e < VEC; ++e) xv[e] = 0.f;
-      }
+        for (int i = 0; i < 4; ++i) {
+          float wf[VEC];
+          WTraits<WT>::unpack(wq[i], wf);
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        float wf[VEC];
-        WTraits<WT>::unpack(wq[i], wf);
+          for (int e = 0; e < VEC; ++e) acc[i] = fmaf(wf[e], xv[e], acc[i]);
+        }
+        load_x(c0 + CW + VEC * lane, xv);
 #pragma unroll
-        for (int e = 0; e < VEC; ++e) acc[i] = fmaf(wf[e], xv[e], acc[i]);
+        for (int i = 0; i < 4; ++i) {
+          float wf[VEC];
+          WTraits<WT>::unpack(wq[i + 4], wf);
+#pragma unroll
+          for (int e = 0; e < VEC; ++e) acc[i] = fmaf(wf[e], xv[e], acc[i]);
+        }
       }
     }
     __syncwarp();
