@@ -142,6 +142,12 @@ def dist_setup(args):
     return world, rank, local
 
 
+def aggregate_tokens_per_s(world: int, steps: int, gen: int, ms_max: float) -> float:
+    """Whole-job committed tokens/s: every rank decodes `gen` tokens per step; the job takes as long
+    as its slowest rank."""
+    return world * steps * gen / (ms_max / 1e3)
+
+
 def barrier(world):
     if world > 1:
         import torch.distributed as dist
@@ -329,7 +335,7 @@ def main_spd(args):
     ms, (toks, st), launches, clocks = timed(spd_step, args.steps, args.warmup, clk, tag="spd_timed")
     ms_max = max_over_ranks(ms, world)
     cycles = st["cycles"]
-    value = world * args.steps * G / (ms_max / 1e3)
+    value = aggregate_tokens_per_s(world, args.steps, G, ms_max)
     ms_step = ms_max / args.steps
     trace = eng.dump(B.DUMP_TRACE)[:, : eng.state()["exits"]]
     accepts = [bool(x) for x in trace[1]]
@@ -384,7 +390,7 @@ def main_spd(args):
         return toks, st
 
     ms_e2e, (toks_e2e, _), _, _ = timed(e2e_step, max(3, args.steps // 2), 1)
-    e2e_val = world * max(3, args.steps // 2) * G / (max_over_ranks(ms_e2e, world) / 1e3)
+    e2e_val = aggregate_tokens_per_s(world, max(3, args.steps // 2), G, max_over_ranks(ms_e2e, world))
     lossless = lossless and toks_e2e.tolist() == ar_list
 
     # --- CPU oracle baseline (rank 0, single GPU only) ---
