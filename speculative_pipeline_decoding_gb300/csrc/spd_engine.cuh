@@ -53,8 +53,9 @@ constexpr int kSlots = 64;                     // weight rows per stage (2 boxes
 constexpr int kStageBytes = kSlots * 512;      // 4 boxes wide
 constexpr int kStages = 4;
 constexpr int kMaxMT = 2;                      // tensor-core path: up to 2 m-tiles of 16 vectors
-constexpr int kMmaCostWeight = 2;              // a weight byte on the tensor-core path costs about
-                                               // twice one on the single-vector path
+constexpr int kCostSV = 2, kCostMma = 3;       // split cost of a weight byte: a tensor-core stage of
+                                               // the draft rows takes ~1.5x a single-vector stage
+                                               // streamed alongside it (measured per CTA)
 // tensor-core path scratch: the warps' partial tiles of one m-tile
 constexpr int kRedBytes = kNCW * 8 * 4 * 32 * 4;  // the 8 warps' partial tiles of one m-tile
 constexpr int kMmaScratch = kRedBytes;
@@ -88,7 +89,7 @@ struct EngineCfg {
 
 // split cost of one output row: its weight elements, weighted by the path's cost per byte
 __device__ __forceinline__ long long rowcost(const GG& g) {
-  return (long long)g.cols * g.nw * (g.mma ? kMmaCostWeight : 1);
+  return (long long)g.cols * g.nw * (g.mma ? kCostMma : kCostSV);
 }
 
 __device__ __forceinline__ int anchor_index(const Dims& D, int layer_done) {
