@@ -27,12 +27,12 @@ namespace {
 using namespace eng;
 
 constexpr int kStepGroups = 36;   // groups of one phase: n target + n+1 draft rows (n <= 16)
-constexpr int kStepTiles = 24;    // attention tiles of one phase: n target tiles + draft-row tiles
+constexpr int kStepTiles = 28;    // attention tiles of one phase: n target tiles + ceil((n+1)/2) draft-row tiles
 constexpr int kProdWarp = kNCW;       // warp 8: producer (weights and K/V chunks into the ring)
 constexpr int kPlanWarp = kNCW + 1;   // warp 9: planner (resolves the next phase)
 constexpr int kStepThreads = (kNCW + 2) * 32;
 constexpr int kNCT = kNCW * 32;       // consumer threads
-constexpr int kStepQT = 4;            // query rows per attention tile of the draft module's rows
+constexpr int kStepQT = 2;            // query rows per attention tile of the draft module's rows
 
 struct StepParams {
   EngineCfg cfg;
