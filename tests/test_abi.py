@@ -23,7 +23,7 @@ def test_every_declared_symbol_is_exported(L):
         assert hasattr(L, n), n
 
 
-def test_header_declares_the_survey_boundary():
+def test_header_declares_the_boundary():
     from speculative_pipeline_decoding_gb300 import binding
     names = set(binding.exported_symbols())
     for n in ("spd_create", "spd_prefill", "spd_cycle", "spd_generate", "spd_rollback",
