@@ -490,6 +490,7 @@ int spd_create(const spd_config* cfg, const spd_weights* w, void* cuda_stream, s
   D.ffn = c.d_ffn; D.V = c.vocab; D.n = c.n_stages; D.S = S; D.Ls = c.pdm_layers; D.m = c.n_anchors;
   D.max_seq = c.max_seq; D.dtype = c.dtype; D.qkv_rows = (c.n_heads + 2 * c.n_kv_heads) * c.head_dim;
   D.gq = gq; D.eps = c.norm_eps;
+  D.box3 = box3_cols(c.d_model, c.dtype) && box3_cols(c.d_ffn, c.dtype);  // every streamed matrix's cols
   for (int i = 0; i < c.n_anchors; ++i) D.anchors[i] = c.anchors[i];
   // f(k) = max{i : b_i <= lmax(k)}, lmax(k) = min(L, k*L/n)   (SPD summary, 核心方法)
   for (int k = 0; k <= c.n_stages; ++k) {
@@ -553,7 +554,7 @@ int spd_create(const spd_config* cfg, const spd_weights* w, void* cuda_stream, s
     int k = 0;
     const int qr = c.n_heads * c.head_dim, kr = c.n_kv_heads * c.head_dim;
     auto enc = [&](const void* W, int rows, int cols) -> const CUtensorMap* {
-      if (e == cudaSuccess) e = gemv_encode_map(&hm[k], W, rows, cols, c.dtype);
+      if (e == cudaSuccess) e = gemv_encode_map(&hm[k], W, rows, cols, c.dtype, D.box3 != 0);
       return dmaps + k++;
     };
     auto layer_maps = [&](LayerW& o) {
@@ -1007,7 +1008,7 @@ int spd_grouped_gemv(const void* const* W, const float* const* x, float* const* 
   // tensor maps of the G weights: encoded here, held in stream-ordered scratch for this launch
   std::vector<CUtensorMap> maps(G);
   for (int g = 0; g < G; ++g) {
-    const cudaError_t em = gemv_encode_map(&maps[g], W[g], rows, cols, dtype);
+    const cudaError_t em = gemv_encode_map(&maps[g], W[g], rows, cols, dtype, box3_cols(cols, dtype));
     if (em != cudaSuccess)
       return fail(nullptr, SPD_ECUDA, "spd_grouped_gemv: tensor map %d: %s", g, cudaGetErrorString(em));
   }

@@ -21,6 +21,7 @@ constexpr int kThreads = 256;   // threads taking part (named barrier 2)
 
 struct Tile {
   int layer, nq, pos0, vid0, nch, rec_off, item_off, tick_off;
+  int kn0;                   // first key the QKV step of this cycle appends for the tile's row group
   int co, old_off, new_off;  // step kernel: chunks written before this cycle; item offsets of the
                              // tile in the lists of such chunks and of the chunks holding new keys
   const unsigned char* kc;  // base of this layer's K cache (head 0, position 1)
@@ -56,6 +57,9 @@ static __device__ int add_tiles(const Dims& D, const Bufs& B, const Launch& lc, 
       T.nq = min(qt, rg[i].nv - r0);
       T.pos0 = rg[i].pos0 + r0;
       T.vid0 = rg[i].vid0 + r0;
+      // every row of the group appends its key in this cycle's QKV step (one row group per layer),
+      // so a tile after the group's first rows also reads keys from rows before its own
+      T.kn0 = rg[i].pos0 - 1;
       const int pos_last = T.pos0 + T.nq - 1;
       T.nch = (pos_last + ck - 1) / ck;
       T.rec_off = rec;
@@ -99,9 +103,6 @@ __device__ __forceinline__ Item item_of(const Tile* tiles, int nt, int item, int
   it.nk = min(ck, pos_last - it.c * ck);
   return it;
 }
-
-// True if chunk c of tile Ti holds a key the QKV step of this cycle appended (key pos0-1 onward).
-__device__ __forceinline__ bool chunk_is_new(const Tile& Ti, int c, int ck) { return c >= (Ti.pos0 - 1) / ck; }
 
 // One item on the 256 calling threads, its K and V chunks already in shared memory (ks, vs:
 // [nk][hd] in the cache dtype): queries -> qs, scores, per-chunk softmax, unnormalised partial
@@ -292,13 +293,14 @@ static __device__ bool run_items(const Dims& D, DevState* st, const Tile* tiles,
 // ------------------------------------------------------------------------------------------------
 constexpr int kWarpCK = 32;
 
-// Chunks of earlier cycles and chunks holding this cycle's keys, per tile (`ck` keys per chunk):
-// fills co / old_off / new_off and returns the totals.
+// Chunks of earlier cycles and chunks holding this cycle's keys (key kn0 onward), per tile (`ck`
+// keys per chunk): fills co / old_off / new_off and returns the totals.  Only old chunks may be
+// fetched before the grid barrier that ends the QKV step.
 __device__ __forceinline__ void split_items(const Dims& D, Tile* tiles, int nt, int ck, int* n_old, int* n_new) {
   int o = 0, w = 0;
   for (int i = 0; i < nt; ++i) {
     Tile& T = tiles[i];
-    T.co = min(T.nch, (T.pos0 - 1) / ck);
+    T.co = min(T.nch, T.kn0 / ck);
     T.old_off = o;
     T.new_off = w;
     o += D.hkv * T.co;

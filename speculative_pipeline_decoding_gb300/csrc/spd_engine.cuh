@@ -322,6 +322,16 @@ __device__ __forceinline__ void tma_box(void* dst, const CUtensorMap* map, int x
       : "memory");
 }
 
+// One 3-D box: chunks z..z+3 (128 bytes each) of rows y..y+31, landing as [chunk][row][128 B].
+__device__ __forceinline__ void tma_box3(void* dst, const CUtensorMap* map, int y, int z, uint64_t* bar,
+                                         uint64_t pol) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(smem_u32(dst)), "l"(map), "r"(0), "r"(y), "r"(z),
+      "r"(smem_u32(bar)), "l"(pol)
+      : "memory");
+}
+
 // Byte offset in a stage of the 16-byte chunk `j` (0..31 across the 512-byte row slice) of slot
 // `slot` (0..63): box (slot/32, j/8), row slot%32, 128-byte swizzle (chunk ^ row % 8).
 __device__ __forceinline__ uint32_t stage_off(int slot, int j) {
@@ -454,59 +464,81 @@ __device__ __forceinline__ bool wide_tile(const GG& G, int r, int tr) {
   return !G.mma && G.nw == 1 && tr <= kBoxRows && !(G.epi == EPI_QKV && r < G.seg2);
 }
 
-template <typename WT>
-__device__ __forceinline__ void issue_stage(const GG& G, int r, int tr, int c0, int hd, Ring& R, DevState* st,
-                                            uint64_t pol, int lane, bool wide = false) {
-  constexpr int BOXC = 128 / sizeof(WT);   // columns per box
-  const int nrb = G.nw == 2 ? 2 : (tr + kBoxRows - 1) / kBoxRows;  // row boxes
+// Where the stages of one tile come from: the tensor map and first physical row of each of its two
+// 32-row boxes, how many boxes high a stage is, and whether it streams wide.  Fixed for the tile (a
+// tile is one 64-slot stage high), so the producer resolves it once per tile, not once per stage.
+struct TileSrc {
   const CUtensorMap* m0;
   const CUtensorMap* m1;
-  int y0, y1;
+  int y0, y1, nrb;
+  bool wide, box3;
+};
+
+__device__ __forceinline__ TileSrc tile_src(const GG& G, int r, int tr, int hd, bool box3) {
+  TileSrc S;
+  S.box3 = box3;
+  S.wide = wide_tile(G, r, tr);
+  S.nrb = G.nw == 2 ? 2 : (tr + kBoxRows - 1) / kBoxRows;
   if (G.nw == 2) {
-    m0 = G.m[0]; m1 = G.m[1]; y0 = y1 = r;
+    S.m0 = G.m[0]; S.m1 = G.m[1]; S.y0 = S.y1 = r;
   } else {
     const int p0 = phys_row(G, r, hd), p1 = phys_row(G, r + kBoxRows, hd);
     const int s0 = p0 < G.seg1 ? 0 : (p0 < G.seg2 ? 1 : 2);
     const int s1 = p1 < G.seg1 ? 0 : (p1 < G.seg2 ? 1 : 2);
-    m0 = G.m[s0]; m1 = G.m[s1];
-    y0 = p0 - (s0 == 0 ? 0 : (s0 == 1 ? G.seg1 : G.seg2));
-    y1 = p1 - (s1 == 0 ? 0 : (s1 == 1 ? G.seg1 : G.seg2));
+    S.m0 = G.m[s0]; S.m1 = G.m[s1];
+    S.y0 = p0 - (s0 == 0 ? 0 : (s0 == 1 ? G.seg1 : G.seg2));
+    S.y1 = p1 - (s1 == 0 ? 0 : (s1 == 1 ? G.seg1 : G.seg2));
   }
+  return S;
+}
+
+// Producer warp: one stage of a tile at column c0 (64 rows x 512 bytes, or 32 rows x 1024 bytes wide).
+template <typename WT>
+__device__ __forceinline__ void issue_stage(const TileSrc& S, int c0, Ring& R, DevState* st, uint64_t pol, int lane) {
+  constexpr int BOXC = 128 / sizeof(WT);   // columns per box
   const int s = R.ctr % kStages;
   if (R.ctr >= (uint32_t)kStages && !mbar_wait_bounded(&R.empty[s], ((R.ctr / kStages) - 1) & 1)) {
     if (lane == 0) set_err(st, ERR_TIMEOUT, 40);
     R.failed = true;
     return;
   }
-  if (lane == 0) mbar_arrive_expect_tx(&R.full[s], (uint32_t)((wide ? 8 : nrb * 4) * kBoxBytes));
+  if (lane == 0) mbar_arrive_expect_tx(&R.full[s], (uint32_t)((S.wide ? 8 : S.nrb * 4) * kBoxBytes));
   __syncwarp();
-  if (wide) {
+  unsigned char* dst = R.base + (size_t)s * kStageBytes;
+  if (S.box3) {
+    // one copy per 32-row band: bands of the two row boxes (tall), or the two 512-byte halves of a
+    // wide stage's 1024 bytes; copy i lands at 16 KB x i, the same bytes as four 2-D boxes each
+    const int z = c0 / BOXC;
+    if (S.wide) {
+      if (lane < 2) tma_box3(dst + (size_t)lane * 4 * kBoxBytes, S.m0, S.y0, z + 4 * lane, &R.full[s], pol);
+    } else if (lane < S.nrb) {
+      tma_box3(dst + (size_t)lane * 4 * kBoxBytes, lane ? S.m1 : S.m0, lane ? S.y1 : S.y0, z, &R.full[s], pol);
+    }
+  } else if (S.wide) {
     if (lane < 8)
-      tma_box(R.base + (size_t)s * kStageBytes + (size_t)lane * kBoxBytes, m0, c0 + lane * BOXC, y0, &R.full[s], pol);
-  } else if (lane < nrb * 4) {
+      tma_box(R.base + (size_t)s * kStageBytes + (size_t)lane * kBoxBytes, S.m0, c0 + lane * BOXC, S.y0, &R.full[s],
+              pol);
+  } else if (lane < S.nrb * 4) {
     const int rbx = lane >> 2, cb = lane & 3;
-    tma_box(R.base + (size_t)s * kStageBytes + (size_t)(rbx * 4 + cb) * kBoxBytes, rbx ? m1 : m0,
-            c0 + cb * BOXC, rbx ? y1 : y0, &R.full[s], pol);
+    tma_box(R.base + (size_t)s * kStageBytes + (size_t)(rbx * 4 + cb) * kBoxBytes, rbx ? S.m1 : S.m0,
+            c0 + cb * BOXC, rbx ? S.y1 : S.y0, &R.full[s], pol);
   }
   ++R.ctr;
 }
 
-// Producer warp (all 32 lanes): issue the tensor copies of every stage of the span.  Single-vector
-// tiles go column chunk by column chunk; tensor-core blocks go chunk-major over their 64-row slices.
+// Producer warp (all 32 lanes): issue the tensor copies of every stage of the span, tile by tile,
+// column chunk by column chunk.
 template <typename WT>
-__device__ void produce_span(const GG* gg, int gb, int rb, int ge, int re, int hd, Ring& R, DevState* st,
+__device__ void produce_span(const GG* gg, int gb, int rb, int ge, int re, int hd, bool box3, Ring& R, DevState* st,
                              uint64_t pol, int lane) {
   constexpr int CW = 512 / sizeof(WT);     // columns per stage
   for (int g = gb, r = rb; (g < ge || (g == ge && r < re)) && !R.failed;) {
     const GG& G = gg[g];
     const int last = (g == ge) ? re : G.rows;
     const int tr = tile_rows(G, r, last);
-    const int srows = kSlots / G.nw;                       // output rows per 64-slot stage
-    const int nsl = G.mma ? (tr + srows - 1) / srows : 1;  // slices of the tile
-    const bool wide = wide_tile(G, r, tr);
-    for (int c0 = 0; c0 < G.cols && !R.failed; c0 += wide ? 2 * CW : CW)
-      for (int j = 0; j < nsl && !R.failed; ++j)
-        issue_stage<WT>(G, r + j * srows, min(srows, tr - j * srows), c0, hd, R, st, pol, lane, wide);
+    const TileSrc S = tile_src(G, r, tr, hd, box3);
+    const int cols = G.cols, step = S.wide ? 2 * CW : CW;
+    for (int c0 = 0; c0 < cols && !R.failed; c0 += step) issue_stage<WT>(S, c0, R, st, pol, lane);
     r += tr;
     if (r >= last) { ++g; r = 0; }
   }

@@ -59,7 +59,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_engine(const __grid_constant
   Ring R{ring, full_bar, empty_bar, 0u, false};
 
   if (warp == kNCW) {  // producer warp
-    produce_span<WT>(gg, s_gb, s_rb, s_ge, s_re, p.cfg.D.hd, R, st, l2_evict_first_policy(), lane);
+    produce_span<WT>(gg, s_gb, s_rb, s_ge, s_re, p.cfg.D.hd, p.cfg.D.box3 != 0, R, st, l2_evict_first_policy(), lane);
     drain_ring(R, lane);
     return;
   }
@@ -137,11 +137,11 @@ cudaError_t launch_gemv_explicit(const GemvExplicit& ge, int dtype, float eps, c
   memset(&p, 0, sizeof(p));
   p.explicit_mode = 1; p.resolve_after_wait = 1; p.ge = ge;
   p.cfg.eps = eps; p.cfg.has_mma = 0;
-  p.cfg.D.dtype = dtype; p.cfg.D.eps = eps;
+  p.cfg.D.dtype = dtype; p.cfg.D.eps = eps; p.cfg.D.box3 = box3_cols(ge.cols, dtype);
   return dtype == SPD_DTYPE_BF16 ? launch_engine<__nv_bfloat16>(p, false, s) : launch_engine<float>(p, false, s);
 }
 
-cudaError_t gemv_encode_map(CUtensorMap* out, const void* W, int rows, int cols, int dtype) {
+cudaError_t gemv_encode_map(CUtensorMap* out, const void* W, int rows, int cols, int dtype, bool box3) {
   static PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
   if (!encode) {
     void* fn = nullptr;
@@ -152,15 +152,28 @@ cudaError_t gemv_encode_map(CUtensorMap* out, const void* W, int rows, int cols,
     if (q != cudaDriverEntryPointSuccess || !fn) return cudaErrorNotSupported;
     encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
   }
+  if (box3 && !box3_cols(cols, dtype)) return cudaErrorInvalidValue;
   const int esz = dtype == SPD_DTYPE_BF16 ? 2 : 4;
-  const cuuint64_t gdim[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
-  const cuuint64_t gstride[1] = {(cuuint64_t)cols * esz};
-  const cuuint32_t box[2] = {(cuuint32_t)(128 / esz), (cuuint32_t)kBoxRows};
-  const cuuint32_t estride[2] = {1, 1};
-  const CUresult r = encode(out, dtype == SPD_DTYPE_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32,
-                            2, const_cast<void*>(W), gdim, gstride, box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  const cuuint32_t ce = (cuuint32_t)(128 / esz);  // elements of one 128-byte chunk
+  const CUtensorMapDataType ty = dtype == SPD_DTYPE_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
+  CUresult r;
+  if (box3) {
+    // (element in chunk, row, chunk): the chunk stride (128 B) is below the row stride, which the
+    // tiled mode accepts; every coordinate in range addresses inside the matrix
+    const cuuint64_t gdim[3] = {ce, (cuuint64_t)rows, (cuuint64_t)(cols / ce)};
+    const cuuint64_t gstride[2] = {(cuuint64_t)cols * esz, 128};
+    const cuuint32_t box[3] = {ce, (cuuint32_t)kBoxRows, 4};
+    const cuuint32_t estride[3] = {1, 1, 1};
+    r = encode(out, ty, 3, const_cast<void*>(W), gdim, gstride, box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE,
+               CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  } else {
+    const cuuint64_t gdim[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+    const cuuint64_t gstride[1] = {(cuuint64_t)cols * esz};
+    const cuuint32_t box[2] = {ce, (cuuint32_t)kBoxRows};
+    const cuuint32_t estride[2] = {1, 1};
+    r = encode(out, ty, 2, const_cast<void*>(W), gdim, gstride, box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE,
+               CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  }
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 

@@ -52,6 +52,7 @@ struct LayerW {
 struct Dims {
   int L, d, hq, hkv, hd, ffn, V, n, S, Ls, m;
   int max_seq, dtype, qkv_rows, gq;
+  int box3;         // weight tensor maps are 3-D (see box3_cols): two copies per GEMV stage
   int anchors[SPD_MAX_ANCHORS];
   int ftab[SPD_MAX_STAGES + 1];
   float eps;
@@ -338,9 +339,14 @@ cudaError_t launch_attn(const Dims& D, const Bufs& B, const Launch& lc, const La
 size_t attn_smem_bytes(const Dims& D, bool multi);
 size_t attn_part_floats(int rows, int hq, int hd, int max_seq, int ck = kAttnChunk);
 cudaError_t gemv_setup_attributes();
-// Encodes the tensor map the GEMV engine streams a row-major [rows, cols] weight matrix with
-// (boxes of 128 bytes x 32 rows, 128-byte swizzle).  Host call; returns a CUDA error code.
-cudaError_t gemv_encode_map(CUtensorMap* out, const void* W, int rows, int cols, int dtype);
+// A row-major [rows, cols] weight matrix is streamed through 3-D tensor maps when its rows are whole
+// 128-byte chunks: (128-byte chunk, row, chunk index), box = 4 chunks x 32 rows (16 KB), so one copy
+// brings a 32-row band of a 512-byte column slice; other widths use 2-D maps with boxes of
+// 128 bytes x 32 rows (four copies per band).  Both land in shared memory as [chunk][row][128 B]
+// with the 128-byte swizzle.
+inline bool box3_cols(int cols, int dtype) { return cols % (dtype == SPD_DTYPE_BF16 ? 64 : 32) == 0; }
+// Encodes that tensor map (3-D when box3, else 2-D).  Host call; returns a CUDA error code.
+cudaError_t gemv_encode_map(CUtensorMap* out, const void* W, int rows, int cols, int dtype, bool box3);
 int gemv_head_grid(int dtype);
 int num_sms();
 cudaError_t attn_setup_attributes(size_t max_smem);

@@ -323,7 +323,7 @@ __global__ void __launch_bounds__(kStepThreads, 1) step_kernel(const __grid_cons
       if (!__shfl_sync(0xffffffffu, ok, 0)) { R.failed = true; break; }
       const Phase& P = s_ph[b];
       if (P.type == PH_GEMV) {
-        produce_span<WT>(gg + b * kStepGroups, s_gb[b], s_rb[b], s_ge[b], s_re[b], D.hd, R, st, pol, lane);
+        produce_span<WT>(gg + b * kStepGroups, s_gb[b], s_rb[b], s_ge[b], s_re[b], D.hd, D.box3 != 0, R, st, pol, lane);
       } else if (P.type == PH_ATTN) {
         const att::Tile* tb = tiles + b * kStepTiles;
         const int nt = s_nt[b];

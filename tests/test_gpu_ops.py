@@ -25,7 +25,8 @@ def _normal(seed, shape, dtype, std=0.02):
 
 @pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
 @pytest.mark.parametrize("rows,cols,G,norm", [(6144, 2560, 8, True), (4099, 9728, 3, False),
-                                              (37, 2048, 1, True), (2560, 12800, 2, False)])
+                                              (37, 2048, 1, True), (2560, 12800, 2, False),
+                                              (300, 2056, 2, True), (129, 2080, 3, False)])
 def test_grouped_gemv_matches_oracle(spd, dtype, rows, cols, G, norm):
     Ws = [_normal(10 + g, (rows, cols), dtype) for g in range(G)]
     xs = [_normal(50 + g, (cols,), torch.float32, std=1.0) for g in range(G)]

@@ -40,6 +40,14 @@ SMALL_BF16 = si.Workload(
                    vocab=2048, dtype="bf16"),
     n_stages=4, pdm_layers=2, anchors=(0, 2, 4, 6, 7), prompt_len=300, gen_len=48, alphas=(0.7,))
 
+# widths that are multiples of 8 but not of 64 (d_model 520, d_ffn 1000): the weight matrices stream
+# through 2-D tensor maps (4 copies per 32-row band) with a zero-filled partial last chunk
+ODD_BF16 = si.Workload(
+    "odd_bf16_n4",
+    si.ModelConfig(n_layers=4, d_model=520, n_heads=8, n_kv_heads=2, head_dim=64, d_ffn=1000,
+                   vocab=1000, dtype="bf16"),
+    n_stages=4, pdm_layers=1, anchors=(0, 2, 4), prompt_len=120, gen_len=32, alphas=(0.7,))
+
 
 def rel(a, b):
     a, b = np.asarray(a, np.float64), np.asarray(b, np.float64)
@@ -187,6 +195,27 @@ def test_small_bf16_spd_equals_ar(small_setup, alpha):
 def test_small_bf16_per_cycle_parity_with_oracle(small_setup):
     worst = per_cycle_parity(small_setup, 0.7, 40, 2e-2)
     print("small bf16 worst relative errors", worst)
+
+
+@pytest.fixture(scope="module")
+def odd_setup(spd):
+    return Setup(spd, ODD_BF16)
+
+
+@pytest.mark.parametrize("alpha", [0.0, 0.7])
+def test_odd_widths_spd_equals_ar(odd_setup, alpha):
+    S = odd_setup
+    toks, stats, trace = S.spd_run(alpha)
+    assert toks == S.ar
+    acc = [bool(x) for x in trace[1]]
+    assert acc == si.accept_mask(S.w.coin_seed, alpha, S.P + 2, S.P + S.G)
+
+
+def test_odd_widths_per_cycle_parity_with_oracle(odd_setup):
+    flagged, _ = teacher_forced_check(odd_setup.models, odd_setup.prompt, odd_setup.ar)
+    assert flagged <= 3
+    worst = per_cycle_parity(odd_setup, 0.7, 30, 2e-2)
+    print("odd-width bf16 worst relative errors", worst)
 
 
 def test_rollback_state_and_kv_lengths(tiny_setup):
