@@ -8,8 +8,8 @@ title and section:
   Decoding: Higher-Accruacy and Zero-Bubble Speculation via Pipeline
   Parallelism), sections 核心方法 and 方法步骤详情 (the six steps).
 * "SPD news" -- the techwalker.com article on arXiv 2605.30852, sections 三-八.
-* "SPD v3" -- the paperlayer.ai summary of arXiv 2605.30852v3, sections 3.1-3.4
-  and Appendix A.1-A.3.
+* "SPD v3" -- the paperlayer.ai summary of arXiv 2605.30852v3, sections 3.1-3.4,
+  section 4 (the scheduling ablation) and Appendix A.1-A.3.
 
 Readings taken where the pages are silent or loose (each also listed in the
 design notes):
@@ -34,6 +34,15 @@ design notes):
    position q is replaced by the reference token when mode[q] = FORCE_REF,
    and by the draft module's best-ranked token other than the reference when
    mode[q] = FORCE_OTHER.
+7. Post-step schedule (the ablation of SPD v3 §4 and SPD news 十: the draft
+   module waits for the target step and reads its output state).  The pages
+   give only its effect, so the plainest reading is taken: after the step, an
+   in-flight row i has depth t - i + 1 (one stage more), the exiting row is
+   at depth n, the verified prefix stays at n; the rows processed are the same
+   ones (first not-yet-cached row to t), and the exiting row, which is
+   committed whatever the verdict on its successor, joins the draft-module
+   cache.  The draft still enters stage 1 at the end of the cycle and a
+   rejected cycle's draft is discarded, so the cycle count is unchanged.
 """
 from __future__ import annotations
 
@@ -83,6 +92,11 @@ def depth_of(i: int, t: int, a: int, n: int) -> int:
     return t - i if t - i < a else n
 
 
+def depth_after_step(i: int, t: int, a: int, n: int) -> int:
+    """Depth of row i after the step (post-step schedule, reading 7): in-flight rows one stage deeper."""
+    return t - i + 1 if t - i < a else n
+
+
 # ---------------------------------------------------------------------------
 # draft module (PDM)
 # ---------------------------------------------------------------------------
@@ -120,7 +134,7 @@ class SPDRun:
     def __init__(self, target: Decoder, pdm: DraftModule, n: int, Ls: int, B: Sequence[int],
                  prompt: Sequence[int], max_len: int,
                  modes: Optional[Dict[int, int]] = None, ref: Optional[Dict[int, int]] = None,
-                 check_full_recompute: bool = False, record: bool = False):
+                 check_full_recompute: bool = False, record: bool = False, post_step: bool = False):
         L = target.L
         check_config(L, n, Ls, B)
         self.T, self.pdm, self.n, self.S, self.B = target, pdm, n, L // n, list(B)
@@ -129,6 +143,7 @@ class SPDRun:
         self.modes, self.ref = modes or {}, ref or {}
         self.check_full = check_full_recompute
         self.record = record
+        self.post_step = post_step
         self.P = len(prompt)
         # prefill: the prompt passes all L layers (verified prefix)
         self.cache = target.new_cache(max_len)
@@ -169,9 +184,28 @@ class SPDRun:
         """Generated tokens known correct: positions P+1 .. v+1."""
         return [self.seq[p] for p in range(self.P + 1, self.v + 2)]
 
+    def _depth(self, i: int) -> int:
+        # t and a are those of the pre-step state in both schedules (the step does not change them)
+        return (depth_after_step if self.post_step else depth_of)(i, self.t, self.a, self.n)
+
     def staircase(self) -> List[Tuple[int, int]]:
-        """(position, depth) of the rows the draft module processes this cycle."""
-        return [(i, depth_of(i, self.t, self.a, self.n)) for i in range(self.pdm_len + 1, self.t + 1)]
+        """(position, depth) of the rows the draft module processes this cycle (at the time it runs)."""
+        return [(i, self._depth(i)) for i in range(self.pdm_len + 1, self.t + 1)]
+
+    def _draft_module(self) -> Tuple[List[Tuple[int, int]], np.ndarray, Tuple[int, int, float, float]]:
+        """Steps 2-4: rows, anchor features, the Ls layers over the cached prefix, the head of row t."""
+        n, S = self.n, self.S
+        rows = self.staircase()
+        # the closed-form staircase must agree with how far each row has actually run
+        for i, k in rows:
+            if self.done_layers[i] != (self.L if k == n else k * S):
+                raise AssertionError(f"row {i}: depth {k} but {self.done_layers[i]} layers done")
+        self.pdm_cache.truncate(self.pdm_len)
+        Z = np.stack([self.pdm.feature(self.anchor[i], self.B, self.ftab[k]) for i, k in rows])
+        Z = self.pdm.forward(Z, [i for i, _ in rows], self.pdm_cache)
+        if self.check_full:
+            self._check_full_recompute(rows, Z)
+        return rows, Z, top2(self.pdm.stack.logits(Z[-1]))
 
     def _draft(self, top1: int, top2_: int) -> int:
         q = self.t + 1
@@ -185,19 +219,11 @@ class SPDRun:
     # -- one cycle ----------------------------------------------------------
     def cycle(self) -> Dict:
         n, S, t, a, v = self.n, self.S, self.t, self.a, self.v
-        rows = self.staircase()
-        # the closed-form staircase must agree with how far each row has actually run
-        for i, k in rows:
-            if self.done_layers[i] != (self.L if k == n else k * S):
-                raise AssertionError(f"row {i}: depth {k} but {self.done_layers[i]} layers done")
-        # (step 2-4) draft module on pre-step features, concurrently with the target step
-        self.pdm_cache.truncate(self.pdm_len)
-        Z = np.stack([self.pdm.feature(self.anchor[i], self.B, self.ftab[k]) for i, k in rows])
-        Z = self.pdm.forward(Z, [i for i, _ in rows], self.pdm_cache)
-        p1, p2, pv1, pv2 = top2(self.pdm.stack.logits(Z[-1]))
-        if self.check_full:
-            self._check_full_recompute(rows, Z)
-        pdm_len_next = v
+        if not self.post_step:
+            # (step 2-4) draft module on pre-step features, concurrently with the target step
+            rows, Z, (p1, p2, pv1, pv2) = self._draft_module()
+        # rows at depth n when the draft module ran keep their draft-module KV
+        pdm_len_next = v + 1 if (self.post_step and a == n) else v
         # (step 1) target step: the token at depth j runs layers j*S .. j*S+S-1
         for j in range(a):
             p = t - j
@@ -208,6 +234,9 @@ class SPDRun:
                     self.anchor[p][l + 1] = h[0].copy()
             self.resid[p] = h[0]
             self.done_layers[p] += S
+        if self.post_step:
+            # post-step schedule: the draft module waits for the step and reads its output state
+            rows, Z, (p1, p2, pv1, pv2) = self._draft_module()
         draft = self._draft(p1, p2)
         info = {"t": t, "a": a, "rows": rows, "pdm_top": (p1, p2), "pdm_gap": pv1 - pv2,
                 "draft": draft, "exited": a == n}
@@ -247,7 +276,7 @@ class SPDRun:
 
     def _check_full_recompute(self, rows, Z_inc: np.ndarray) -> None:
         """Draft-module rows recomputed from scratch over the whole G_t must equal the incremental ones."""
-        all_rows = [(i, depth_of(i, self.t, self.a, self.n)) for i in range(1, self.t + 1)]
+        all_rows = [(i, self._depth(i)) for i in range(1, self.t + 1)]
         cache = self.pdm.stack.new_cache(self.t + 1)
         Z = np.stack([self.pdm.feature(self.anchor[i], self.B, self.ftab[k]) for i, k in all_rows])
         Z = self.pdm.forward(Z, [i for i, _ in all_rows], cache)
@@ -286,7 +315,8 @@ def build(workload, params: Dict):
 
 def run_spd(workload, params: Dict, prompt: Sequence[int], gen: int, alpha: Optional[float],
             ref: Optional[Sequence[int]] = None, coin_seed: Optional[int] = None,
-            check_full_recompute: bool = False, record: bool = False, models=None) -> SPDRun:
+            check_full_recompute: bool = False, record: bool = False, models=None,
+            post_step: bool = False) -> SPDRun:
     """SPD greedy decode; with ``alpha`` set, drafts follow the seeded-acceptance modes."""
     import spd_inputs as si
     target, pdm = models if models is not None else build(workload, params)
@@ -300,10 +330,10 @@ def run_spd(workload, params: Dict, prompt: Sequence[int], gen: int, alpha: Opti
             refd[q] = int(ref[q - P - 1])
     run = SPDRun(target, pdm, workload.n_stages, workload.pdm_layers, workload.anchors, prompt,
                  max_len=P + gen + workload.n_stages + 2, modes=modes, ref=refd,
-                 check_full_recompute=check_full_recompute, record=record)
+                 check_full_recompute=check_full_recompute, record=record, post_step=post_step)
     run.generate(gen)
     return run
 
 
-__all__ = ["lmax", "f_of", "f_table", "check_config", "depth_of", "DraftModule", "SPDRun",
+__all__ = ["lmax", "f_of", "f_table", "check_config", "depth_of", "depth_after_step", "DraftModule", "SPDRun",
            "expected_cycles", "build", "run_spd", "greedy_ar", "RAW", "FORCE_REF", "FORCE_OTHER"]
