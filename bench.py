@@ -358,10 +358,17 @@ def main_spd(args):
     ms_tgt, (toks_t, st_t), _, _ = timed(spd_step, max(3, args.steps // 2), 1)
     eng.set_options(step)
     ms_ser, _, _, _ = timed(spd_step, max(3, args.steps // 2), 1)
+    # post-step schedule (the pages' scheduling ablation): the draft module after the target step,
+    # on its output state; same cycles and committed stream, drafting no longer hidden
+    eng.set_options(step | B.OPT_POST_STEP)
+    ms_post, (toks_p, st_p), _, _ = timed(spd_step, max(3, args.steps // 2), 1)
     Kx = max(3, args.steps // 2)
     t_cycle = ms_step / cycles
     t_tgt = ms_tgt / Kx / st_t["cycles"]
     t_ser = ms_ser / Kx / cycles
+    t_post = ms_post / Kx / st_p["cycles"]
+    post_tps = Kx * G / (ms_post / 1e3)
+    post_lossless = toks_p.tolist() == ar_list and st_p["cycles"] == cycles
 
     # --- instrumented pass: phase timers of the step kernel (CTA 0, grid barrier to grid barrier),
     # draft module in its own phases so that its time is separate ---
@@ -432,6 +439,8 @@ def main_spd(args):
                 "cycle_hbm_frac_spec": cycle_gbs / SPEC_HBM_GBS, "alg_bytes_per_step": step_bytes,
                 "ar_tokens_per_s": ar_tps, "spd_over_ar": value / world / ar_tps,
                 "target_only_cycle_ms": t_tgt, "serial_pdm_cycle_ms": t_ser,
+                "post_step": {"cycle_ms": t_post, "tokens_per_s": post_tps,
+                              "lossless_and_same_cycles": post_lossless},
                 "pdm_alone_ms_per_cycle": pdm_alone, "pdm_hidden_frac": hidden,
                 "control_us": 1e3 * kt["control"][1] / max(1, kt["control"][0]),
                 "phases_ms_per_cycle": kern},

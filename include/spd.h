@@ -194,6 +194,13 @@ int spd_set_draft_override(spd_handle* h, int32_t first_pos, int32_t count,
 #define SPD_OPT_STEP        32  /* one persistent cooperative kernel per cycle / AR step (one CTA
                                    per SM, phases separated by grid barriers, weights streamed
                                    across phase boundaries); off: one launch per operator      */
+#define SPD_OPT_POST_STEP   64  /* post-step schedule (the scheduling ablation, SPD v3 summary §4;
+                                   SPD news 十): the draft module runs after the target step on
+                                   its OUTPUT state -- in-flight rows one stage deeper (depth
+                                   t-i+1), the exiting row at depth n and cached -- so drafting
+                                   is serial with the step.  Overrides SPD_OPT_COSCHED; no
+                                   effect with SPD_OPT_TARGET_ONLY.  The committed stream and
+                                   the cycle count are those of the default schedule.          */
 int spd_set_options(spd_handle* h, int32_t flags);
 
 /* Copy internal state to a HOST buffer of `bytes` bytes (synchronising).  Layouts:

@@ -24,6 +24,7 @@ from . import build_ext
 MAX_ANCHORS = 8
 DTYPE_F32, DTYPE_BF16 = 0, 1
 OPT_GRAPHS, OPT_COSCHED, OPT_TARGET_ONLY, OPT_DEBUG_LOGITS, OPT_PDL, OPT_STEP = 1, 2, 4, 8, 16, 32
+OPT_POST_STEP = 64  # draft module after the target step, on its output state
 OPT_DEFAULT = OPT_GRAPHS | OPT_COSCHED | OPT_PDL | OPT_STEP
 DUMP_STATE, DUMP_RESID, DUMP_ANCHORS, DUMP_PDM_Z, DUMP_LOGITS, DUMP_SEQ, DUMP_TRACE, DUMP_KVLEN = range(8)
 _OPS = ["qkv", "rope_append", "attention", "o_proj", "gate_up", "down", "anchor_fc", "head",

@@ -185,6 +185,12 @@ Launch mk(int kind, int stack, int sub, const Act& act, int pos0, int cnt) {
 
 bool use_step(const spd_handle* h) { return (h->opts & SPD_OPT_STEP) && h->step_smem > 0; }
 
+// Control-block flags of an option set: the device side reads which schedule runs.
+int state_flags(int opts) {
+  if (opts & SPD_OPT_TARGET_ONLY) return SF_TARGET_ONLY;
+  return (opts & SPD_OPT_POST_STEP) ? SF_POST_STEP : 0;
+}
+
 Phase ph_gemv(int op, int kind, const Launch& a, const Launch* b) {
   Phase P;
   memset(&P, 0, sizeof(P));
@@ -218,17 +224,22 @@ int build_programs(spd_handle* h) {
   const Dims& D = h->D;
   std::vector<Phase> cyc, ar;
   const bool pdm = !(h->opts & SPD_OPT_TARGET_ONLY);
-  const bool cos = pdm && (h->opts & SPD_OPT_COSCHED);
-  if (pdm) {
+  const bool post = pdm && (h->opts & SPD_OPT_POST_STEP);
+  const bool cos = pdm && !post && (h->opts & SPD_OPT_COSCHED);
+  auto draft_serial = [&]() {  // anchor FC, then the Ls draft layers on their own phases
     cyc.push_back(ph_gemv(OP_FC, KK_FC + 9, mk(LK_PDMROWS, 1, 0, h->act_p, 0, 0), nullptr));
-    if (!cos)
-      for (int lp = 0; lp < D.Ls; ++lp) layer_phases(cyc, mk(LK_PDMROWS, 1, lp, h->act_p, 0, 0), nullptr);
+    for (int lp = 0; lp < D.Ls; ++lp) layer_phases(cyc, mk(LK_PDMROWS, 1, lp, h->act_p, 0, 0), nullptr);
+  };
+  if (pdm && !post) {
+    if (cos) cyc.push_back(ph_gemv(OP_FC, KK_FC + 9, mk(LK_PDMROWS, 1, 0, h->act_p, 0, 0), nullptr));
+    else draft_serial();
   }
   for (int s = 0; s < D.S; ++s) {
     const Launch lt = mk(LK_DIAG, 0, s, h->act_t, 0, 0);
     const Launch lp = mk(LK_PDMROWS, 1, s, h->act_p, 0, 0);
     layer_phases(cyc, lt, (cos && s < D.Ls) ? &lp : nullptr);
   }
+  if (post) draft_serial();  // on the step's output state
   cyc.push_back(ph_gemv(OP_HEAD, KK_HEAD, mk(LK_DIAG, 0, 0, h->act_head, 0, 0), nullptr));
   {
     Phase c;
@@ -274,19 +285,28 @@ int enqueue_cycle(spd_handle* h) {
   if (use_step(h)) return enqueue_step(h, true);
   int rc;
   const bool pdm = !(h->opts & SPD_OPT_TARGET_ONLY);
-  const bool cos = pdm && (h->opts & SPD_OPT_COSCHED);
+  const bool post = pdm && (h->opts & SPD_OPT_POST_STEP);
+  const bool cos = pdm && !post && (h->opts & SPD_OPT_COSCHED);
   cudaStream_t sm = h->s_main;
   h->st_dirty = true;  // the previous cycle's control kernel (or the host) wrote the control block
-  if (pdm) {
-    if ((rc = run_gemv(h, OP_FC, mk(LK_PDMROWS, 1, 0, h->act_p, 0, 0), nullptr, sm))) return rc;
-    if (!cos)  // serialised draft module: its Ls layers before the target step
-      for (int lp = 0; lp < h->D.Ls; ++lp)
-        if ((rc = enqueue_layer(h, mk(LK_PDMROWS, 1, lp, h->act_p, 0, 0), nullptr, sm))) return rc;
+  auto draft_fc = [&]() { return run_gemv(h, OP_FC, mk(LK_PDMROWS, 1, 0, h->act_p, 0, 0), nullptr, sm); };
+  auto draft_layers = [&]() {  // serialised draft module: its Ls layers on their own launches
+    for (int lp = 0; lp < h->D.Ls; ++lp)
+      if (int r = enqueue_layer(h, mk(LK_PDMROWS, 1, lp, h->act_p, 0, 0), nullptr, sm)) return r;
+    return (int)SPD_OK;
+  };
+  if (pdm && !post) {  // before the target step, on its input state
+    if ((rc = draft_fc())) return rc;
+    if (!cos && (rc = draft_layers())) return rc;
   }
   for (int s = 0; s < h->D.S; ++s) {
     const Launch lt = mk(LK_DIAG, 0, s, h->act_t, 0, 0);
     const Launch lp = mk(LK_PDMROWS, 1, s, h->act_p, 0, 0);
     if ((rc = enqueue_layer(h, lt, (cos && s < h->D.Ls) ? &lp : nullptr, sm))) return rc;
+  }
+  if (post) {  // post-step schedule: after the target step, on its output state
+    if ((rc = draft_fc())) return rc;
+    if ((rc = draft_layers())) return rc;
   }
   if ((rc = run_gemv(h, OP_HEAD, mk(LK_DIAG, 0, 0, h->act_head, 0, 0), nullptr, sm))) return rc;
   Timed tm(h, KK_CTRL, sm);
@@ -717,7 +737,7 @@ int spd_prefill(spd_handle* h, const int32_t* tokens, int32_t P, int32_t* first_
   SPD_CUDA(h, cudaMemsetAsync(h->B.ovr_mode, 0, D.max_seq + 2, s));
   SPD_CUDA(h, cudaMemsetAsync(h->B.st, 0, sizeof(DevState), s));
   if (h->d_bar) SPD_CUDA(h, cudaMemsetAsync(h->d_bar, 0, 2 * sizeof(unsigned), s));
-  const int flags = (h->opts & SPD_OPT_TARGET_ONLY) ? SF_TARGET_ONLY : 0;
+  const int flags = state_flags(h->opts);
   h->host_state->flags = flags;
   SPD_CUDA(h, cudaMemcpyAsync(&h->B.st->flags, &h->host_state->flags, sizeof(int),
                               cudaMemcpyHostToDevice, s));
@@ -809,17 +829,17 @@ int spd_set_draft_override(spd_handle* h, int32_t first_pos, int32_t count, cons
 int spd_set_options(spd_handle* h, int32_t flags) {
   if (!h) return SPD_EINVAL;
   if (flags & ~(SPD_OPT_GRAPHS | SPD_OPT_COSCHED | SPD_OPT_TARGET_ONLY | SPD_OPT_DEBUG_LOGITS | SPD_OPT_PDL |
-                SPD_OPT_STEP))
+                SPD_OPT_STEP | SPD_OPT_POST_STEP))
     return fail(h, SPD_EINVAL, "unknown option bits");
   SPD_CUDA(h, cudaStreamSynchronize(h->s_main));
   if ((flags ^ h->opts) & (SPD_OPT_COSCHED | SPD_OPT_TARGET_ONLY | SPD_OPT_DEBUG_LOGITS | SPD_OPT_PDL |
-                           SPD_OPT_STEP))
+                           SPD_OPT_STEP | SPD_OPT_POST_STEP))
     drop_graphs(h);
   h->opts = flags;
   int rcp;
   if ((rcp = build_programs(h))) return rcp;
   h->LC.debug_logits = (flags & SPD_OPT_DEBUG_LOGITS) ? 1 : 0;
-  h->host_state->flags = (flags & SPD_OPT_TARGET_ONLY) ? SF_TARGET_ONLY : 0;
+  h->host_state->flags = state_flags(flags);
   SPD_CUDA(h, cudaMemcpyAsync(&h->B.st->flags, &h->host_state->flags, sizeof(int),
                               cudaMemcpyHostToDevice, h->s_main));
   SPD_CUDA(h, cudaStreamSynchronize(h->s_main));

@@ -11,7 +11,8 @@
 //             are overwritten later), (ii) in-flight states flushed (a <- 0, t <- t_e),
 //             (iii) y enters stage 1 at t_e+1; this cycle's draft is discarded.
 //   no exit (warm-up / refill, a < n): the draft enters stage 1.
-//   draft-module cache length <- the pre-step v (rows at depth n are cached, SPD v3 App. A.1).
+//   draft-module cache length <- the pre-step v (rows at depth n are cached, SPD v3 App. A.1); in
+//   the post-step schedule the exiting row t_e was at depth n when the draft module ran, so <- t_e.
 // "Entering stage 1" writes the token's embedding into the residual ring and anchor b_0 = 0.
 #pragma once
 #include "spd_internal.cuh"
@@ -69,6 +70,8 @@ static __device__ void control_cycle(const Dims& D, const Bufs& B, Top2 (*red)[2
     int t = st->t, a = st->a, v = st->v;
     const int v_pre = v;
     const bool target_only = (st->flags & SF_TARGET_ONLY) != 0;
+    const bool post = (st->flags & SF_POST_STEP) != 0;
+    int pdm_next = v_pre;
     s_tok = -1;
     if (t + 1 > D.max_seq) {
       set_err(st, ERR_BOUNDS, 500);
@@ -96,6 +99,7 @@ static __device__ void control_cycle(const Dims& D, const Bufs& B, Top2 (*red)[2
         st->exits = k + 1;
         st->last_exited = 1; st->last_exit_pos = te; st->last_accept = accept; st->target_top1 = y;
         v = te;
+        if (post) pdm_next = te;
         if (accept) {
           a -= 1;
         } else {
@@ -112,7 +116,7 @@ static __device__ void control_cycle(const Dims& D, const Bufs& B, Top2 (*red)[2
         set_err(st, ERR_BOUNDS, 501);
         push = -1;
       }
-      if (!target_only) st->pdm_len = v_pre;
+      if (!target_only) st->pdm_len = pdm_next;
       t += 1;
       a += 1;
       B.seq[t] = push;

@@ -158,10 +158,13 @@ static __device__ int add_part(const EngineCfg& p, const GemvPart& pt, GG* gg, i
       set_err(st, ERR_PDM_ROWS, 300);
       return ng;
     }
+    // pre-step depth t-pos of an in-flight row; one stage more when the draft module runs after the
+    // step (post-step schedule); the verified prefix at n
+    const int post = (sv->flags & SF_POST_STEP) ? 1 : 0;
     int prev_f = -1;
     for (int r = 0; r < R; ++r) {
       const int pos = sv->pdm_len + 1 + r;
-      const int depth = (t - pos < a) ? (t - pos) : D.n;
+      const int depth = (t - pos < a) ? (t - pos + post) : D.n;
       const int f = D.ftab[depth];
       if (f != prev_f) {
         GG& o = gg[ng++];

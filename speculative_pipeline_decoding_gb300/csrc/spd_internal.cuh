@@ -42,7 +42,7 @@ struct DevState {
 };
 
 enum ErrCode { ERR_TIMEOUT = 1, ERR_PDM_ROWS = 2, ERR_BOUNDS = 4 };
-enum StateFlags { SF_TARGET_ONLY = 1 };
+enum StateFlags { SF_TARGET_ONLY = 1, SF_POST_STEP = 2 };  // SF_POST_STEP: draft module after the step
 
 struct LayerW {
   const void *attn_norm, *wq, *wk, *wv, *wo, *ffn_norm, *wg, *wu, *wd;

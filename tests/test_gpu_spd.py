@@ -98,8 +98,9 @@ def teacher_forced_check(models, prompt, stream):
     return flagged, ref
 
 
-def per_cycle_parity(S: Setup, alpha, n_cycles, tol):
-    """Run GPU and oracle SPD side by side on identical drafts; compare after every cycle."""
+def per_cycle_parity(S: Setup, alpha, n_cycles, tol, post_step=False):
+    """Run GPU and oracle SPD side by side on identical drafts; compare after every cycle (with
+    ``post_step``: both in the post-step schedule, the draft module after the target step)."""
     w, eng = S.w, S.eng
     target, pdm = S.models
     first, ref, md = S.modes(alpha)
@@ -108,7 +109,7 @@ def per_cycle_parity(S: Setup, alpha, n_cycles, tol):
     modes = {q: m for q, m in zip(range(first, first + len(md)), md)}
     refd = {q: r for q, r in zip(range(first, first + len(ref)), ref)}
     run = ospd.SPDRun(target, pdm, w.n_stages, w.pdm_layers, w.anchors, S.prompt,
-                      S.P + S.G + w.n_stages + 2, modes, refd, record=True)
+                      S.P + S.G + w.n_stages + 2, modes, refd, record=True, post_step=post_step)
     n, B = w.n_stages, list(w.anchors)
     worst = {"resid": 0.0, "anch": 0.0, "pdm": 0.0}
     for c in range(n_cycles):
@@ -280,11 +281,13 @@ def _option_sets():
         "step_cosched_eager": B.OPT_STEP | B.OPT_PDL | B.OPT_COSCHED,
         "ops_cosched_graphs": B.OPT_GRAPHS | B.OPT_PDL | B.OPT_COSCHED,
         "ops_serial_eager": 0,
+        "step_post_graphs": B.OPT_STEP | B.OPT_PDL | B.OPT_GRAPHS | B.OPT_POST_STEP,
+        "ops_post_eager": B.OPT_POST_STEP,
     }
 
 
 @pytest.mark.parametrize("name", ["step_serial_graphs", "step_cosched_eager", "ops_cosched_graphs",
-                                  "ops_serial_eager"])
+                                  "ops_serial_eager", "step_post_graphs", "ops_post_eager"])
 @pytest.mark.parametrize("setup", ["tiny_setup", "small_setup"])
 def test_execution_options_give_identical_streams(request, setup, name):
     from speculative_pipeline_decoding_gb300 import binding as B
@@ -372,3 +375,47 @@ def test_gqa4b_full_size_sampled_tokens_match_oracle(spd):
             assert gap < NEAR_TIE, f"token {i}: gpu {g} oracle {o} gap {gap}"
             flagged += 1
     assert flagged <= 1
+
+
+# ------------------------------------------------------------------------------------------------
+# post-step schedule (the scheduling ablation: draft module after the target step, on its output
+# state) -- per-cycle parity with the oracle's post-step run, through the step kernel and through
+# the per-operator launches
+# ------------------------------------------------------------------------------------------------
+@pytest.mark.parametrize("opts", ["step", "ops"])
+@pytest.mark.parametrize("setup,tol", [("tiny_setup", 1e-4), ("small_setup", 2e-2)])
+def test_post_step_per_cycle_parity_with_oracle(request, setup, tol, opts):
+    from speculative_pipeline_decoding_gb300 import binding as B
+    S = request.getfixturevalue(setup)
+    S.eng.set_options(B.OPT_POST_STEP | (B.OPT_STEP | B.OPT_PDL if opts == "step" else 0))
+    try:
+        worst = per_cycle_parity(S, S.w.alphas[0], 40, tol, post_step=True)
+    finally:
+        S.eng.set_options(B.OPT_DEFAULT)
+    print(setup, opts, "post-step worst relative errors", worst)
+
+
+def test_post_step_cycle_count_and_pdm_cache_length(tiny_setup):
+    """Same cycles and trace as the default schedule; the exiting row joins the draft-module cache."""
+    from speculative_pipeline_decoding_gb300 import binding as B
+    S = tiny_setup
+    alpha = 0.7
+    toks0, stats0, trace0 = S.spd_run(alpha)
+    S.eng.set_options(B.OPT_DEFAULT | B.OPT_POST_STEP)
+    try:
+        toks, stats, trace = S.spd_run(alpha)
+        assert toks == S.ar and stats["cycles"] == stats0["cycles"]
+        assert np.array_equal(trace, trace0)
+        first, ref, md = S.modes(alpha)
+        S.eng.rollback(S.P, S.first)
+        S.eng.set_draft_override(first, ref, md)
+        for _ in range(30):
+            g = S.eng.cycle()
+            st = S.eng.state()
+            # after an exit the draft-module cache holds every verified row (the exiting one included)
+            if g["exited"]:
+                assert st["pdm_len"] == g["exit_pos"], st
+            else:
+                assert st["pdm_len"] == st["v"], st
+    finally:
+        S.eng.set_options(B.OPT_DEFAULT)
