@@ -43,6 +43,9 @@ design notes):
    committed whatever the verdict on its successor, joins the draft-module
    cache.  The draft still enters stage 1 at the end of the cycle and a
    rejected cycle's draft is discarded, so the cycle count is unchanged.
+8. Sampled decoding (T > 0): drafts are drawn from the draft module's top-k
+   distribution and verified by rejection sampling (oracle/sampling.py); the
+   streaming order, the rollback and the cycle arithmetic are unchanged.
 """
 from __future__ import annotations
 
@@ -51,6 +54,7 @@ from typing import Dict, List, Optional, Sequence, Tuple
 import numpy as np
 
 from .model import Decoder, KVCache, _f32, greedy_ar, top2
+from . import sampling as osm
 
 # draft-override modes (same values as spd_inputs.DRAFT_*)
 RAW, FORCE_REF, FORCE_OTHER = 0, 1, 2
@@ -134,7 +138,11 @@ class SPDRun:
     def __init__(self, target: Decoder, pdm: DraftModule, n: int, Ls: int, B: Sequence[int],
                  prompt: Sequence[int], max_len: int,
                  modes: Optional[Dict[int, int]] = None, ref: Optional[Dict[int, int]] = None,
-                 check_full_recompute: bool = False, record: bool = False, post_step: bool = False):
+                 check_full_recompute: bool = False, record: bool = False, post_step: bool = False,
+                 sampling: Optional[Dict] = None):
+        """``sampling``: None for greedy decoding, else {"T": temperature, "k": top-k, "u_draft",
+        "u_accept", "u_resample": {position: uniform}} (oracle/sampling.py; the harness modes
+        are not used then)."""
         L = target.L
         check_config(L, n, Ls, B)
         self.T, self.pdm, self.n, self.S, self.B = target, pdm, n, L // n, list(B)
@@ -144,6 +152,9 @@ class SPDRun:
         self.check_full = check_full_recompute
         self.record = record
         self.post_step = post_step
+        self.sampling = sampling
+        self.qdist: Dict[int, "osm.Dist"] = {}   # draft distribution of each drafted position
+        self.margins: List[float] = []           # sampled decisions' distances from a boundary
         self.P = len(prompt)
         # prefill: the prompt passes all L layers (verified prefix)
         self.cache = target.new_cache(max_len)
@@ -205,7 +216,8 @@ class SPDRun:
         Z = self.pdm.forward(Z, [i for i, _ in rows], self.pdm_cache)
         if self.check_full:
             self._check_full_recompute(rows, Z)
-        return rows, Z, top2(self.pdm.stack.logits(Z[-1]))
+        self._pdm_logits = self.pdm.stack.logits(Z[-1])
+        return rows, Z, top2(self._pdm_logits)
 
     def _draft(self, top1: int, top2_: int) -> int:
         q = self.t + 1
@@ -237,7 +249,15 @@ class SPDRun:
         if self.post_step:
             # post-step schedule: the draft module waits for the step and reads its output state
             rows, Z, (p1, p2, pv1, pv2) = self._draft_module()
-        draft = self._draft(p1, p2)
+        if self.sampling is None:
+            draft = self._draft(p1, p2)
+        else:
+            # the draft for t+1 is drawn from the draft module's top-k distribution of row t
+            smp = self.sampling
+            dq = osm.Dist(self._pdm_logits, smp["T"], smp["k"])
+            draft, m = osm.sample(dq, smp["u_draft"][t + 1])
+            self.qdist[t + 1] = dq
+            self.margins.append(m)
         info = {"t": t, "a": a, "rows": rows, "pdm_top": (p1, p2), "pdm_gap": pv1 - pv2,
                 "draft": draft, "exited": a == n}
         if self.record:
@@ -245,9 +265,19 @@ class SPDRun:
         # (step 5) streaming verification
         if a == n:
             te = t - n + 1
-            i1, i2, v1, v2 = top2(self.T.logits(self.resid[te]))
+            tl = self.T.logits(self.resid[te])
+            i1, i2, v1, v2 = top2(tl)
             succ = self.seq[te + 1] if te + 1 <= t else draft
-            accept = succ == i1
+            if self.sampling is None:
+                accept, reseed = succ == i1, i1
+            else:
+                # rejection sampling against the target's top-k distribution at t_e
+                smp = self.sampling
+                pd = osm.Dist(tl, smp["T"], smp["k"])
+                dq = self.qdist[te + 1]
+                accept, reseed, m = osm.verify(pd, succ, dq.prob(succ), dq.prob,
+                                               smp["u_accept"][te + 1], smp["u_resample"][te + 1])
+                self.margins.append(m)
             self.trace.append((te + 1, accept))
             info.update(exit_pos=te, target_top=(i1, i2), target_gap=v1 - v2, accept=accept)
             del self.resid[te]
@@ -265,7 +295,7 @@ class SPDRun:
                     self.done_layers.pop(p, None)
                     self.seq.pop(p, None)
                 self.t, self.a = te, 0
-                self._push(i1)
+                self._push(reseed)
         else:
             self._push(draft)
         self.pdm_len = pdm_len_next
@@ -316,7 +346,7 @@ def build(workload, params: Dict):
 def run_spd(workload, params: Dict, prompt: Sequence[int], gen: int, alpha: Optional[float],
             ref: Optional[Sequence[int]] = None, coin_seed: Optional[int] = None,
             check_full_recompute: bool = False, record: bool = False, models=None,
-            post_step: bool = False) -> SPDRun:
+            post_step: bool = False, sampling: Optional[Dict] = None) -> SPDRun:
     """SPD greedy decode; with ``alpha`` set, drafts follow the seeded-acceptance modes."""
     import spd_inputs as si
     target, pdm = models if models is not None else build(workload, params)
@@ -330,7 +360,8 @@ def run_spd(workload, params: Dict, prompt: Sequence[int], gen: int, alpha: Opti
             refd[q] = int(ref[q - P - 1])
     run = SPDRun(target, pdm, workload.n_stages, workload.pdm_layers, workload.anchors, prompt,
                  max_len=P + gen + workload.n_stages + 2, modes=modes, ref=refd,
-                 check_full_recompute=check_full_recompute, record=record, post_step=post_step)
+                 check_full_recompute=check_full_recompute, record=record, post_step=post_step,
+                 sampling=sampling)
     run.generate(gen)
     return run
 

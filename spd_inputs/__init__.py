@@ -22,6 +22,8 @@ Generator definitions (identical results on any device and any torch version):
 * prompts: token ``i`` is the top 53 bits of the ``i``-th output modulo vocab.
 * acceptance coins: ``coin(q)`` is the top 53 bits of
   ``splitmix64(seed XOR q*0x9E3779B97F4A7C15)`` divided by 2**53.
+* sampling uniforms: stream s (draft, accept, resample, ar) is the coin sequence
+  of the key ``splitmix64(seed XOR (s+1))``, rounded to fp32 (kept below 1).
 """
 from __future__ import annotations
 
@@ -278,6 +280,27 @@ DRAFT_FORCE_OTHER = 2  # draft module's highest-ranked token that differs from t
 def override_modes(seed: int, alpha: float, first: int, last: int) -> List[int]:
     return [DRAFT_FORCE_REF if ok else DRAFT_FORCE_OTHER
             for ok in accept_mask(seed, alpha, first, last)]
+
+
+# ---------------------------------------------------------------------------
+# uniforms of sampled decoding (the random numbers the method draws are inputs)
+# ---------------------------------------------------------------------------
+SAMPLING_STREAMS = ("draft", "accept", "resample", "ar")
+
+
+def sampling_uniforms(seed: int, first: int, last: int) -> Dict[str, List[float]]:
+    """Per stream, uniforms u[q] in [0, 1) for positions q in [first, last]: stream s of seed is
+    the coin sequence of the key splitmix64(seed XOR (s+1)), rounded to fp32 below 1."""
+    out = {}
+    for s, name in enumerate(SAMPLING_STREAMS):
+        key = splitmix64(seed ^ (s + 1))
+        vals = []
+        for q in range(first, last + 1):
+            u = coin(key, q)
+            f = float(torch.tensor(u, dtype=torch.float32))
+            vals.append(f if f < 1.0 else float(torch.nextafter(torch.tensor(1.0), torch.tensor(0.0))))
+        out[name] = vals
+    return out
 
 
 __all__ = [n for n in dir() if not n.startswith("_")]
