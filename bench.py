@@ -272,6 +272,7 @@ def main_reference(args):
 
 
 def main_spd(args):
+    import numpy as np
     import torch
     import spd_inputs as si
     import speculative_pipeline_decoding_gb300 as spd
@@ -369,6 +370,17 @@ def main_spd(args):
     t_post = ms_post / Kx / st_p["cycles"]
     post_tps = Kx * G / (ms_post / 1e3)
     post_lossless = toks_p.tolist() == ar_list and st_p["cycles"] == cycles
+    # sampled decoding (T = 1, top-k 50, rejection-sampling verification) on seeded uniforms: the
+    # acceptance is the draft module's (random weights: rarely), so this times cycles with the
+    # sampling control step and mostly refills
+    eng.set_options(B.OPT_DEFAULT)
+    us = si.sampling_uniforms(w.coin_seed + 1, P + 1, P + G + n + 2)
+    eng.set_sampling(1.0, 50, P + 1, np.array([us[k] for k in si.SAMPLING_STREAMS], dtype=np.float32))
+    ms_smp, (_, st_s), _, _ = timed(spd_step, Kx, 1)
+    eng.set_sampling(0.0)
+    t_smp = ms_smp / Kx / st_s["cycles"]
+    smp_line = {"temperature": 1.0, "top_k": 50, "cycle_ms": t_smp, "tokens_per_s": Kx * G / (ms_smp / 1e3),
+                "accept_rate": 1.0 - st_s["rejects"] / max(1, st_s["exits"])}
 
     # --- instrumented pass: phase timers of the step kernel (CTA 0, grid barrier to grid barrier),
     # draft module in its own phases so that its time is separate ---
@@ -441,6 +453,7 @@ def main_spd(args):
                 "target_only_cycle_ms": t_tgt, "serial_pdm_cycle_ms": t_ser,
                 "post_step": {"cycle_ms": t_post, "tokens_per_s": post_tps,
                               "lossless_and_same_cycles": post_lossless},
+                "sampled_t1": smp_line,
                 "pdm_alone_ms_per_cycle": pdm_alone, "pdm_hidden_frac": hidden,
                 "control_us": 1e3 * kt["control"][1] / max(1, kt["control"][0]),
                 "phases_ms_per_cycle": kern},

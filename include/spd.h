@@ -178,6 +178,23 @@ int spd_rollback(spd_handle* h, int32_t keep_len, int32_t reseed_token);
 int spd_set_draft_override(spd_handle* h, int32_t first_pos, int32_t count,
                            const int32_t* ref_tokens, const uint8_t* modes);
 
+/* Sampled decoding (temperature > 0, top-k; SPD news 六 and SPD summary 复现评估: T in {0, 1},
+ * top-k 50, top-p 1.0).  Drafts are drawn from the draft module's top-k distribution and verified
+ * by rejection sampling: accept with probability min(1, p/q), else the token is drawn from
+ * normalize(max(0, p - q)) (the speculative decoding engineering page §2.1-2.2).  Plain AR
+ * (spd_generate_ar) draws from the target's top-k distribution.  The k tokens are ordered by logit
+ * descending (lower id first among equals); a draw with uniform u takes the first token whose fp32
+ * running sum of exp(l_i/T - l_0/T) exceeds u times the total.
+ *   temperature <= 0: greedy decoding (the default; top_k and the uniforms are ignored).
+ *   top_k: 1..64 (capped at the vocabulary size).
+ *   uniforms: HOST array of 4*count floats in [0, 1), copied: uniforms[s*count + i] is stream s
+ *     (0 draft, 1 accept, 2 resample, 3 ar) at position first_pos + i; other positions keep their
+ *     values.  The random numbers are inputs so that a caller can reproduce every draw.
+ * The token at P+1 (returned by spd_prefill) stays the greedy one.  The seeded-acceptance harness
+ * (spd_set_draft_override) does not apply while sampling.  SPD_EINVAL for a bad range or value. */
+int spd_set_sampling(spd_handle* h, float temperature, int32_t top_k, int32_t first_pos, int32_t count,
+                     const float* uniforms);
+
 /* Execution options (bit flags), default SPD_OPT_GRAPHS | SPD_OPT_COSCHED | SPD_OPT_PDL |
  * SPD_OPT_STEP. */
 #define SPD_OPT_GRAPHS       1  /* replay captured CUDA graphs instead of eager launches      */

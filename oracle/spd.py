@@ -154,7 +154,7 @@ class SPDRun:
         self.post_step = post_step
         self.sampling = sampling
         self.qdist: Dict[int, "osm.Dist"] = {}   # draft distribution of each drafted position
-        self.margins: List[float] = []           # sampled decisions' distances from a boundary
+        self.margins: List[Tuple[int, float]] = []  # (position, distance of a sampled decision from a boundary)
         self.P = len(prompt)
         # prefill: the prompt passes all L layers (verified prefix)
         self.cache = target.new_cache(max_len)
@@ -257,7 +257,7 @@ class SPDRun:
             dq = osm.Dist(self._pdm_logits, smp["T"], smp["k"])
             draft, m = osm.sample(dq, smp["u_draft"][t + 1])
             self.qdist[t + 1] = dq
-            self.margins.append(m)
+            self.margins.append((t + 1, m))
         info = {"t": t, "a": a, "rows": rows, "pdm_top": (p1, p2), "pdm_gap": pv1 - pv2,
                 "draft": draft, "exited": a == n}
         if self.record:
@@ -277,7 +277,7 @@ class SPDRun:
                 dq = self.qdist[te + 1]
                 accept, reseed, m = osm.verify(pd, succ, dq.prob(succ), dq.prob,
                                                smp["u_accept"][te + 1], smp["u_resample"][te + 1])
-                self.margins.append(m)
+                self.margins.append((te + 1, m))
             self.trace.append((te + 1, accept))
             info.update(exit_pos=te, target_top=(i1, i2), target_gap=v1 - v2, accept=accept)
             del self.resid[te]

@@ -108,6 +108,7 @@ def lib() -> ctypes.CDLL:
         "spd_rollback": (ctypes.c_int, [vp, i32, i32]),
         "spd_set_draft_override": (ctypes.c_int, [vp, i32, i32, _I32P, ctypes.POINTER(ctypes.c_uint8)]),
         "spd_set_options": (ctypes.c_int, [vp, i32]),
+        "spd_set_sampling": (ctypes.c_int, [vp, ctypes.c_float, i32, i32, i32, ctypes.POINTER(ctypes.c_float)]),
         "spd_dump_size": (sz, [vp, i32]),
         "spd_debug_dump": (ctypes.c_int, [vp, i32, vp, sz]),
         "spd_time_kernels": (ctypes.c_int, [vp, i32]),
@@ -308,6 +309,16 @@ class Engine:
 
     def set_options(self, flags: int) -> None:
         _check(lib().spd_set_options(self.h, int(flags)), self.h)
+
+    def set_sampling(self, temperature: float, top_k: int = 50, first_pos: int = 1, uniforms=None) -> None:
+        """Sampled decoding (temperature > 0) or greedy (<= 0).  ``uniforms``: [4][count] floats in
+        [0, 1) for positions first_pos.. (streams draft, accept, resample, ar)."""
+        u = np.zeros((4, 0), np.float32) if uniforms is None else np.asarray(uniforms, dtype=np.float32)
+        if u.ndim != 2 or u.shape[0] != 4:
+            raise SpdError(-1, "uniforms must be [4][count]")
+        u = np.ascontiguousarray(u)
+        _check(lib().spd_set_sampling(self.h, float(temperature), int(top_k), int(first_pos), int(u.shape[1]),
+                                      u.ctypes.data_as(ctypes.POINTER(ctypes.c_float))), self.h)
 
     # -- inspection -------------------------------------------------------------
     def dump(self, what: int) -> np.ndarray:

@@ -624,6 +624,13 @@ int spd_create(const spd_config* cfg, const spd_weights* w, void* cuda_stream, s
   B.head_grid = gemv_head_grid(c.dtype);
   ALLOC(B.head_part, float, (size_t)B.head_grid * 8);
   ALLOC(B.logits, float, (size_t)2 * c.vocab);
+  {  // sampled decoding: uniforms by position, draft distributions by position % (n+1)
+    float* u;
+    ALLOC(u, float, (size_t)4 * (c.max_seq + 2));
+    B.u_smp = u;
+    ALLOC(B.q_prob, float, (size_t)(n + 1) * kMaxTopK);
+    ALLOC(B.q_id, int, (size_t)(n + 1) * kMaxTopK);
+  }
   const int qkvr = D.qkv_rows, hqd = c.n_heads * c.head_dim, f = c.d_ffn;
   // target decode scratch
   Act& T = h->act_t;
@@ -826,6 +833,32 @@ int spd_set_draft_override(spd_handle* h, int32_t first_pos, int32_t count, cons
   return SPD_OK;
 }
 
+int spd_set_sampling(spd_handle* h, float temperature, int32_t top_k, int32_t first_pos, int32_t count,
+                     const float* uniforms) {
+  if (!h) return SPD_EINVAL;
+  const bool on = temperature > 0.f;
+  if (on && (top_k < 1 || top_k > kMaxTopK || !(temperature < 1e30f)))
+    return fail(h, SPD_EINVAL, "top_k must be 1..%d and the temperature finite", kMaxTopK);
+  if (count < 0 || first_pos < 1 || (size_t)first_pos + count > (size_t)h->D.max_seq + 2 || (count && !uniforms))
+    return fail(h, SPD_EINVAL, "uniform range outside 1..max_seq+1");
+  for (int i = 0; i < 4 * count; ++i)
+    if (!(uniforms[i] >= 0.f && uniforms[i] < 1.f)) return fail(h, SPD_EINVAL, "uniform %d outside [0, 1)", i);
+  SPD_CUDA(h, cudaStreamSynchronize(h->s_main));
+  const int k = on ? top_k : 0;
+  const float T = on ? temperature : 0.f;
+  if (k != h->D.top_k || T != h->D.temp) drop_graphs(h);  // graphs hold the kernels' parameters
+  h->D.top_k = k;
+  h->D.temp = T;
+  h->LC.debug_logits = ((h->opts & SPD_OPT_DEBUG_LOGITS) || k > 0) ? 1 : 0;
+  const size_t L = (size_t)h->D.max_seq + 2;
+  float* u = const_cast<float*>(h->B.u_smp);
+  for (int s = 0; s < 4 && count; ++s)
+    SPD_CUDA(h, cudaMemcpyAsync(u + s * L + first_pos, uniforms + (size_t)s * count, sizeof(float) * count,
+                                cudaMemcpyHostToDevice, h->s_main));
+  SPD_CUDA(h, cudaStreamSynchronize(h->s_main));
+  return SPD_OK;
+}
+
 int spd_set_options(spd_handle* h, int32_t flags) {
   if (!h) return SPD_EINVAL;
   if (flags & ~(SPD_OPT_GRAPHS | SPD_OPT_COSCHED | SPD_OPT_TARGET_ONLY | SPD_OPT_DEBUG_LOGITS | SPD_OPT_PDL |
@@ -838,7 +871,7 @@ int spd_set_options(spd_handle* h, int32_t flags) {
   h->opts = flags;
   int rcp;
   if ((rcp = build_programs(h))) return rcp;
-  h->LC.debug_logits = (flags & SPD_OPT_DEBUG_LOGITS) ? 1 : 0;
+  h->LC.debug_logits = ((flags & SPD_OPT_DEBUG_LOGITS) || h->D.top_k > 0) ? 1 : 0;
   h->host_state->flags = state_flags(flags);
   SPD_CUDA(h, cudaMemcpyAsync(&h->B.st->flags, &h->host_state->flags, sizeof(int),
                               cudaMemcpyHostToDevice, h->s_main));

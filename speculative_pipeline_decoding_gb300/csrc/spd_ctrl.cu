@@ -25,14 +25,16 @@ template <typename WT>
 __global__ void __launch_bounds__(256) control_cycle_kernel(Dims D, Bufs B) {
   __shared__ Top2 red[256][2];
   __shared__ int s_tok, s_slot;
-  ctl::control_cycle<WT>(D, B, red, s_tok, s_slot, 256, 1);
+  __shared__ ctl::SampleSmem S;
+  ctl::control_cycle<WT>(D, B, red, s_tok, s_slot, 256, 1, S);
 }
 
 template <typename WT>
 __global__ void __launch_bounds__(256) control_ar_kernel(Dims D, Bufs B) {
   __shared__ Top2 red[256][2];
   __shared__ int s_tok, s_slot;
-  ctl::control_ar<WT>(D, B, red, s_tok, s_slot, 256, 1);
+  __shared__ ctl::SampleSmem S;
+  ctl::control_ar<WT>(D, B, red, s_tok, s_slot, 256, 1, S);
 }
 
 template <typename WT>

@@ -14,8 +14,12 @@
 //   draft-module cache length <- the pre-step v (rows at depth n are cached, SPD v3 App. A.1); in
 //   the post-step schedule the exiting row t_e was at depth n when the draft module ran, so <- t_e.
 // "Entering stage 1" writes the token's embedding into the residual ring and anchor b_0 = 0.
+//   sampled decoding (T > 0): the draft is drawn from the draft module's top-k distribution,
+//   which is kept (slot q % (n+1)) until position q is verified; verification accepts with
+//   probability min(1, p/q) and a reject reseeds with a draw from max(0, p - q) (spd_sample.cuh).
 #pragma once
 #include "spd_internal.cuh"
+#include "spd_sample.cuh"
 
 namespace spd {
 namespace ctl {
@@ -58,13 +62,56 @@ static __device__ void reduce_head(const Bufs& B, Top2 (*red)[2], int nthreads, 
   }
 }
 
-// One SPD cycle's control step on `nthreads` threads (a power of two; `red` holds nthreads x 2).
+// Shared memory of the sampled control step: one selection, the target's distribution (p) and
+// the draft module's (q), and the residual weights max(0, p_i - q(id_i)) of p's tokens.
+struct SampleSmem {
+  smp::Sel sel;
+  smp::Dist p, q;
+  float resid[kMaxTopK];
+};
+
+// Block-wide part of a sampled control step: the distributions, then (cycle with an exit) the
+// residual weights of p against the stored draft distribution of the verified position.
+static __device__ void sampled_prologue(const Dims& D, const Bufs& B, SampleSmem& S, bool cycle, int nthreads,
+                                        int bar) {
+  const DevState* st = B.st;
+  const int t = st->t, a = st->a, n = D.n;
+  const int k = min(D.top_k, D.V);
+  const bool target_only = (st->flags & SF_TARGET_ONLY) != 0;
+  const bool q_now = cycle && !target_only;
+  const bool p_now = !cycle || a == n;
+  if (q_now) smp::topk_select(B.logits + D.V, D.V, k, D.temp, S.sel, S.q, nthreads, bar);
+  if (p_now) smp::topk_select(B.logits, D.V, k, D.temp, S.sel, S.p, nthreads, bar);
+  if (threadIdx.x == 0) {
+    if (q_now) smp::dist_weights(S.q);
+    if (p_now) smp::dist_weights(S.p);
+  }
+  named_bar(bar, nthreads);
+  if (cycle && a == n && (int)threadIdx.x < k) {
+    const int i = threadIdx.x, te = t - n + 1;
+    const float pi = S.p.w[i] / S.p.cum[k - 1];
+    float qi;
+    if (te + 1 <= t) {  // the successor was drafted in an earlier cycle: its stored distribution
+      const int slot = (te + 1) % (n + 1);
+      qi = smp::stored_prob(B.q_id + slot * kMaxTopK, B.q_prob + slot * kMaxTopK, k, S.p.id[i]);
+    } else {            // n == 1: this cycle's draft
+      qi = target_only ? (S.p.id[i] == B.seq[t] ? 1.f : 0.f) : smp::prob_of(S.q, S.p.id[i]);
+    }
+    S.resid[i] = fmaxf(0.f, pi - qi);
+  }
+  named_bar(bar, nthreads);
+}
+
+// One SPD cycle's control step on `nthreads` threads (a power of two; `red` holds nthreads x 2;
+// `S` is shared-memory scratch of the sampled step, untouched in greedy decoding).
 template <typename WT>
 static __device__ void control_cycle(const Dims& D, const Bufs& B, Top2 (*red)[2], int& s_tok, int& s_slot,
-                              int nthreads, int bar) {
+                              int nthreads, int bar, SampleSmem& S) {
   DevState* st = B.st;
   if (st->done || st->err) return;
   reduce_head(B, red, nthreads, bar);
+  const bool sampled = D.top_k > 0;
+  if (sampled) sampled_prologue(D, B, S, true, nthreads, bar);
   if (threadIdx.x == 0) {
     const int n = D.n, P = st->P;
     int t = st->t, a = st->a, v = st->v;
@@ -84,13 +131,40 @@ static __device__ void control_cycle(const Dims& D, const Bufs& B, Top2 (*red)[2
       int draft = p1;
       if (mode == 1) draft = ref;
       else if (mode == 2) draft = target_only ? (ref + 1) % D.V : ((p1 != ref) ? p1 : p2);
+      const int topk = min(D.top_k, D.V);
+      if (sampled) {
+        // draw the draft for q = t+1 and keep its distribution until q is verified
+        int* qid = B.q_id + (q % (n + 1)) * kMaxTopK;
+        float* qp = B.q_prob + (q % (n + 1)) * kMaxTopK;
+        if (target_only) {  // no draft module: the draft is a point mass on the token at t
+          draft = B.seq[t];
+          for (int i = 0; i < topk; ++i) { qid[i] = i ? -1 : draft; qp[i] = i ? 0.f : 1.f; }
+        } else {
+          draft = S.q.id[smp::draw(S.q.cum, topk, B.u_smp[(size_t)q])];
+          for (int i = 0; i < topk; ++i) { qid[i] = S.q.id[i]; qp[i] = S.q.w[i] / S.q.cum[topk - 1]; }
+        }
+      }
       st->pdm_top1 = p1; st->pdm_top2 = p2; st->draft = draft;
       int push = draft;
       if (a == n) {
         const int te = t - n + 1;
-        const int y = red[0][0].i1;
+        int y = red[0][0].i1;
         const int succ = (te + 1 <= t) ? B.seq[te + 1] : draft;
-        const int accept = succ == y;
+        int accept = succ == y;
+        if (sampled) {
+          // rejection sampling: accept iff u * q(succ) < p(succ); else a draw from the residual
+          const size_t L = (size_t)D.max_seq + 2;
+          const int slot = (te + 1) % (n + 1);
+          const float qx = smp::stored_prob(B.q_id + slot * kMaxTopK, B.q_prob + slot * kMaxTopK, topk, succ);
+          const float px = smp::prob_of(S.p, succ);
+          accept = B.u_smp[L + te + 1] * qx < px;
+          if (!accept) {
+            float c = 0.f;
+            for (int i = 0; i < topk; ++i) { c += S.resid[i]; S.resid[i] = c; }
+            const float u = B.u_smp[2 * L + te + 1];
+            y = (c > 0.f) ? S.p.id[smp::draw(S.resid, topk, u)] : S.p.id[smp::draw(S.p.cum, topk, u)];
+          }
+        }
         const int k = st->exits;
         if (k < D.max_seq) {
           B.trace[k] = te + 1;
@@ -135,17 +209,22 @@ static __device__ void control_cycle(const Dims& D, const Bufs& B, Top2 (*red)[2
 // One plain greedy AR step's control on `nthreads` threads.
 template <typename WT>
 static __device__ void control_ar(const Dims& D, const Bufs& B, Top2 (*red)[2], int& s_tok, int& s_slot,
-                           int nthreads, int bar) {
+                           int nthreads, int bar, SampleSmem& S) {
   DevState* st = B.st;
   if (st->done || st->err) return;
   reduce_head(B, red, nthreads, bar);
+  const bool sampled = D.top_k > 0;
+  if (sampled) sampled_prologue(D, B, S, false, nthreads, bar);
   if (threadIdx.x == 0) {
     s_tok = -1;
     const int t = st->t;
     if (t + 1 > D.max_seq) {
       set_err(st, ERR_BOUNDS, 510);
     } else {
-      const int y = red[0][0].i1;
+      // greedy: the argmax; sampled: a draw from the top-k distribution with u_ar of position t+1
+      const int y = sampled ? S.p.id[smp::draw(S.p.cum, min(D.top_k, D.V),
+                                               B.u_smp[3 * ((size_t)D.max_seq + 2) + t + 1])]
+                            : red[0][0].i1;
       if (y < 0 || y >= D.V) {
         set_err(st, ERR_BOUNDS, 511);
         s_tok = -1;

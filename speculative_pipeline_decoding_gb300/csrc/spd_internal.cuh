@@ -49,10 +49,14 @@ struct LayerW {
   const CUtensorMap *tq, *tk, *tv, *to, *tg, *tu, *td;  // tensor maps of the seven matrices
 };
 
+constexpr int kMaxTopK = 64;  // largest top-k of sampled decoding
+
 struct Dims {
   int L, d, hq, hkv, hd, ffn, V, n, S, Ls, m;
   int max_seq, dtype, qkv_rows, gq;
   int box3;         // weight tensor maps are 3-D (see box3_cols): two copies per GEMV stage
+  int top_k;        // sampled decoding: top-k (0: greedy decoding)
+  float temp;       // sampled decoding: temperature T > 0
   int anchors[SPD_MAX_ANCHORS];
   int ftab[SPD_MAX_STAGES + 1];
   float eps;
@@ -70,7 +74,11 @@ struct Bufs {
   void *kc, *vc, *pkc, *pvc;
   const float *rope_cos, *rope_sin;
   float* head_part;  // [grid][2][4]
-  float* logits;     // [2][V] (debug)
+  float* logits;     // [2][V] (debug, and the heads' logits of sampled decoding)
+  const float* u_smp;  // sampled decoding: [4][max_seq + 2] uniforms by position (draft, accept,
+                       // resample, ar)
+  float* q_prob;     // sampled decoding: draft distribution of position q in slot q % (n+1):
+  int* q_id;         //   [(n+1)][kMaxTopK] probabilities and token ids, canonical order
   int head_grid;
   const LayerW* tl;
   const LayerW* pl;

@@ -416,8 +416,12 @@ __global__ void __launch_bounds__(kStepThreads, 1) step_kernel(const __grid_cons
       if (s_fail) R.failed = true;
     } else if (blockIdx.x == 0 && !R.failed) {  // control: the last phase
       Top2 (*red)[2] = reinterpret_cast<Top2(*)[2]>(uni);
-      if (P.type == PH_CTRL_CYCLE) ctl::control_cycle<WT>(D, cfg.B, red, s_tok, s_slot, kNCT, 1);
-      else ctl::control_ar<WT>(D, cfg.B, red, s_tok, s_slot, kNCT, 1);
+      // the ring is idle in the control phase (every stage of the head phase was consumed): the
+      // sampled control step borrows its first bytes as scratch
+      static_assert(sizeof(ctl::SampleSmem) <= kStageBytes, "sampling scratch exceeds a ring stage");
+      ctl::SampleSmem& S = *reinterpret_cast<ctl::SampleSmem*>(ring);
+      if (P.type == PH_CTRL_CYCLE) ctl::control_cycle<WT>(D, cfg.B, red, s_tok, s_slot, kNCT, 1, S);
+      else ctl::control_ar<WT>(D, cfg.B, red, s_tok, s_slot, kNCT, 1, S);
     }
     if (ph + 1 < p.nphases) {
       named_bar(1, kNCT);  // this phase's writes are done

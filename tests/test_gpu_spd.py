@@ -17,6 +17,7 @@ import torch
 
 import spd_inputs as si
 from oracle import model as om
+from oracle import sampling as osm
 from oracle import spd as ospd
 
 from speculative_pipeline_decoding_gb300.binding import (DUMP_ANCHORS, DUMP_KVLEN, DUMP_PDM_Z,
@@ -419,3 +420,69 @@ def test_post_step_cycle_count_and_pdm_cache_length(tiny_setup):
                 assert st["pdm_len"] == st["v"], st
     finally:
         S.eng.set_options(B.OPT_DEFAULT)
+
+
+# ------------------------------------------------------------------------------------------------
+# sampled decoding (T > 0, top-k; rejection-sampling verification): the GPU streams and traces
+# equal the oracle's on the same uniforms, up to the first decision the oracle took within `thr`
+# of a boundary (a different rounding may take the other side there)
+# ------------------------------------------------------------------------------------------------
+def _uniforms(S, seed):
+    first, last = S.P + 1, S.P + S.G + S.w.n_stages + 2
+    u = si.sampling_uniforms(seed, first, last)
+    arr = np.array([u[s] for s in si.SAMPLING_STREAMS], dtype=np.float32)
+    by_pos = {s: {q: float(v) for q, v in zip(range(first, last + 1), u[s])} for s in si.SAMPLING_STREAMS}
+    return first, arr, by_pos
+
+
+def _first_mismatch(a, b):
+    for j, (x, y) in enumerate(zip(a, b)):
+        if x != y:
+            return j
+    return None if len(a) == len(b) else min(len(a), len(b))
+
+
+@pytest.mark.parametrize("opts", ["step", "ops"])
+# thr: the fp32 workload matches to rounding order; on the bf16 one the two sides' K/V caches
+# occasionally round an element to different bf16 neighbours, which moves hidden states by ~2e-4
+# (relative) and a probability by about as much, so a draw within 1e-3 of a boundary may differ
+@pytest.mark.parametrize("setup,thr", [("tiny_setup", 1e-4), ("small_setup", 1e-3)])
+def test_sampled_spd_and_ar_match_oracle(request, setup, thr, opts):
+    from speculative_pipeline_decoding_gb300 import binding as B
+    S = request.getfixturevalue(setup)
+    target, pdm = S.models
+    T, k, seed = 1.0, 50, 4242
+    first, arr, u = _uniforms(S, seed)
+    if opts == "ops":
+        S.eng.set_options(B.OPT_GRAPHS | B.OPT_PDL | B.OPT_COSCHED)
+    S.eng.set_sampling(T, k, first, arr)
+    try:
+        S.eng.rollback(S.P, S.first)
+        toks, stats = S.eng.generate(S.G)
+        toks = toks.tolist()
+        trace = S.eng.dump(DUMP_TRACE)[:, : S.eng.state()["exits"]]
+        S.eng.rollback(S.P, S.first)
+        ar, _ = S.eng.generate_ar(S.G)
+        ar = ar.tolist()
+    finally:
+        S.eng.set_sampling(0.0)
+        S.eng.set_options(B.OPT_DEFAULT)
+    smp = {"T": T, "k": k, "u_draft": u["draft"], "u_accept": u["accept"], "u_resample": u["resample"]}
+    run = ospd.SPDRun(target, pdm, S.w.n_stages, S.w.pdm_layers, S.w.anchors, S.prompt,
+                      S.P + S.G + S.w.n_stages + 2, sampling=smp)
+    ref = run.generate(S.G)
+    j = _first_mismatch(toks, ref)
+    if j is not None:  # only after a near-boundary decision of the oracle
+        q = S.P + 1 + j
+        assert min([m for p, m in run.margins if p <= q] + [1.0]) < thr, (j, toks[j:j + 3], ref[j:j + 3])
+    upto = S.G if j is None else j
+    assert list(trace[0][:upto - 1]) == [p for p, _ in run.trace][:upto - 1]
+    assert [bool(x) for x in trace[1][:upto - 1]] == [ok for _, ok in run.trace][:upto - 1]
+    accepted = [bool(x) for x in trace[1]]
+    assert stats["cycles"] == ospd.expected_cycles(S.w.n_stages, accepted)
+    # sampled AR from the same kernels
+    ora = osm.sampled_ar(target, S.prompt, S.G, T, k, u["ar"])
+    ja = _first_mismatch(ar, ora["tokens"])
+    if ja is not None:
+        assert min(ora["margins"][:ja] + [1.0]) < thr, (ja, ar[ja:ja + 3], ora["tokens"][ja:ja + 3])
+    print(setup, opts, "sampled SPD first mismatch", j, "AR", ja, "accepts", sum(accepted), "/", len(accepted))
