@@ -6,11 +6,14 @@
 // at depth j runs layer j*S+s, SPD summary 方法步骤详情 step 1) together with the draft module's rows
 // (steps 3-4).
 //
-// Weight streaming: one producer warp issues 2-D TMA tensor copies (cp.async.bulk.tensor, boxes of
-// 128 bytes x 32 rows with the 128-byte swizzle, L2 evict-first) into a 4-deep ring of 32 KB stages
-// guarded by mbarriers; a stage holds 64 weight rows x 512 bytes (4 boxes wide, 2 boxes high).
-// Every weight matrix has its own tensor map, encoded once when the handle is created.  Copies of
-// 4 KB keep the per-copy cost of the copy engine below the HBM time of the bytes it moves.
+// Weight streaming: one producer warp issues TMA tensor copies (cp.async.bulk.tensor, 128-byte
+// swizzle, L2 evict-first) into a 4-deep ring of 32 KB stages guarded by mbarriers; a stage holds
+// 64 weight rows x 512 bytes (two 32-row bands of four 128-byte chunks), or 32 rows x 1024 bytes.
+// Every weight matrix has its own tensor map, encoded once when the handle is created: 3-D (chunk,
+// row, chunk index) when its rows are whole 128-byte chunks, so a band is one 16 KB copy and a
+// stage two; else 2-D with 128-byte x 32-row boxes, eight copies a stage.  Issuing a copy costs the
+// warp tens of nanoseconds, and an SM must start a stage every ~0.7 us to keep HBM busy, so the
+// producer resolves a tile's maps and rows once per tile and issues as few copies as it can.
 //
 // Work split: every CTA of the persistent grid (one per SM) takes a contiguous share of the
 // launch's weight bytes, cut at 32-row boundaries; tiles never straddle a group or a share.

@@ -1,6 +1,6 @@
 // Stand-alone launches of the grouped GEMV engine (spd_engine.cuh): the prefill blocks, the
 // per-operator path used when the step kernel is not, and the stand-alone operator
-// spd_grouped_gemv.  One CTA per SM; one producer warp streams the weights with 2-D TMA tensor
+// spd_grouped_gemv.  One CTA per SM; one producer warp streams the weights with TMA tensor
 // copies, eight consumer warps compute.
 #include <cudaTypedefs.h>
 
