@@ -486,3 +486,57 @@ def test_sampled_spd_and_ar_match_oracle(request, setup, thr, opts):
     if ja is not None:
         assert min(ora["margins"][:ja] + [1.0]) < thr, (ja, ar[ja:ja + 3], ora["tokens"][ja:ja + 3])
     print(setup, opts, "sampled SPD first mismatch", j, "AR", ja, "accepts", sum(accepted), "/", len(accepted))
+
+
+# ------------------------------------------------------------------------------------------------
+# degenerate shapes: a one-stage pipeline (n = 1: the exiting token verifies the draft of the same
+# cycle, SPD degenerates to AR with a draft per step) on a one-token prompt
+# ------------------------------------------------------------------------------------------------
+MICRO_N1 = si.Workload(
+    "micro_f32_n1",
+    si.ModelConfig(n_layers=4, d_model=128, n_heads=2, n_kv_heads=1, head_dim=64, d_ffn=256,
+                   vocab=512, dtype="f32", init_std=0.1),
+    n_stages=1, pdm_layers=1, anchors=(0, 2, 4), prompt_len=1, gen_len=24, alphas=(0.5,))
+
+
+@pytest.fixture(scope="module")
+def n1_setup(spd):
+    return Setup(spd, MICRO_N1)
+
+
+def test_one_stage_one_token_prompt_greedy(n1_setup):
+    S = n1_setup
+    assert S.P == 1
+    flagged, _ = teacher_forced_check(S.models, S.prompt, S.ar)
+    assert flagged <= 1
+    for alpha in (0.0, 0.5, 1.0):
+        toks, stats, trace = S.spd_run(alpha)
+        assert toks == S.ar
+        acc = [bool(x) for x in trace[1]]
+        assert acc == si.accept_mask(S.w.coin_seed, alpha, S.P + 2, S.P + S.G)
+        assert stats["cycles"] == ospd.expected_cycles(1, acc)
+    S.eng.rollback(S.P, S.first)
+    one, st1 = S.eng.generate(1)  # only the token of the prefill
+    assert one.tolist() == [S.first] and st1["cycles"] == 0
+
+
+def test_one_stage_sampled_matches_oracle(n1_setup):
+    S = n1_setup
+    target, pdm = S.models
+    first, arr, u = _uniforms(S, 99)
+    S.eng.set_sampling(1.0, 50, first, arr)
+    try:
+        S.eng.rollback(S.P, S.first)
+        toks, stats = S.eng.generate(S.G)
+        trace = S.eng.dump(DUMP_TRACE)[:, : S.eng.state()["exits"]]
+    finally:
+        S.eng.set_sampling(0.0)
+    smp = {"T": 1.0, "k": 50, "u_draft": u["draft"], "u_accept": u["accept"], "u_resample": u["resample"]}
+    run = ospd.SPDRun(target, pdm, 1, 1, S.w.anchors, S.prompt, S.P + S.G + 3, sampling=smp)
+    ref = run.generate(S.G)
+    j = _first_mismatch(toks.tolist(), ref)
+    if j is not None:
+        assert min([m for p, m in run.margins if p <= S.P + 1 + j] + [1.0]) < 1e-4
+    upto = S.G if j is None else j
+    assert [bool(x) for x in trace[1][:upto - 1]] == [ok for _, ok in run.trace][:upto - 1]
+    assert stats["cycles"] == ospd.expected_cycles(1, [bool(x) for x in trace[1]])
