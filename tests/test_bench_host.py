@@ -16,7 +16,6 @@ ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 sys.path.insert(0, ROOT)
 
 import bench  # noqa: E402
-import spd_inputs as si  # noqa: E402
 from oracle import spd as ospd  # noqa: E402
 
 
