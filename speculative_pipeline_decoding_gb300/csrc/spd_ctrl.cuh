@@ -148,9 +148,10 @@ static __device__ void control_cycle(const Dims& D, const Bufs& B, Top2 (*red)[2
       int push = draft;
       if (a == n) {
         const int te = t - n + 1;
-        int y = red[0][0].i1;
+        const int y = red[0][0].i1;  // the target's argmax at t_e
         const int succ = (te + 1 <= t) ? B.seq[te + 1] : draft;
         int accept = succ == y;
+        int reseed = y;              // greedy: the argmax re-seeds stage 1 after a reject
         if (sampled) {
           // rejection sampling: accept iff u * q(succ) < p(succ); else a draw from the residual
           const size_t L = (size_t)D.max_seq + 2;
@@ -162,7 +163,7 @@ static __device__ void control_cycle(const Dims& D, const Bufs& B, Top2 (*red)[2
             float c = 0.f;
             for (int i = 0; i < topk; ++i) { c += S.resid[i]; S.resid[i] = c; }
             const float u = B.u_smp[2 * L + te + 1];
-            y = (c > 0.f) ? S.p.id[smp::draw(S.resid, topk, u)] : S.p.id[smp::draw(S.p.cum, topk, u)];
+            reseed = (c > 0.f) ? S.p.id[smp::draw(S.resid, topk, u)] : S.p.id[smp::draw(S.p.cum, topk, u)];
           }
         }
         const int k = st->exits;
@@ -181,7 +182,7 @@ static __device__ void control_cycle(const Dims& D, const Bufs& B, Top2 (*red)[2
           for (int l = 0; l < D.L; ++l) B.kvlen[l] = te;
           a = 0;
           t = te;
-          push = y;
+          push = reseed;
         }
       } else {
         st->last_exited = 0; st->last_exit_pos = 0; st->last_accept = 0;
