@@ -72,3 +72,20 @@ def test_accept_mask_rate_and_position_keying():
     # keyed by position only: a sub-range gives the same bits
     assert si.accept_mask(2, 0.8, 500, 599) == m[500:600]
     assert all(si.accept_mask(2, 1.0, 0, 999)) and not any(si.accept_mask(2, 0.0, 0, 999))
+
+
+def test_sampling_uniforms_range_streams_and_position_keying():
+    u = si.sampling_uniforms(11, 100, 4099)
+    assert set(u) == set(si.SAMPLING_STREAMS)
+    for name, vals in u.items():
+        a = np.asarray(vals, dtype=np.float64)
+        assert len(a) == 4000 and a.min() >= 0.0 and a.max() < 1.0
+        assert np.float32(a.max()) < 1.0                      # representable below 1 in fp32
+        assert abs(a.mean() - 0.5) < 0.02 and abs(a.var() - 1 / 12) < 0.01
+        assert abs(np.corrcoef(a[:-1], a[1:])[0, 1]) < 0.05   # neighbouring positions independent
+    # the four streams differ, and a position's uniform does not depend on the range asked for
+    assert len({tuple(v[:8]) for v in u.values()}) == 4
+    v = si.sampling_uniforms(11, 2000, 2007)
+    for name in si.SAMPLING_STREAMS:
+        assert v[name] == u[name][1900:1908]
+    assert si.sampling_uniforms(12, 100, 107)["draft"] != u["draft"][:8]
