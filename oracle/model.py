@@ -27,7 +27,9 @@ What is computed, and from where:
 
 Pins (tests/test_oracle_model.py) hold this file to facts that do not come
 from it: torch's own scaled-dot-product attention / rms_norm / silu on the
-same numbers, the complex-rotation form of RoPE, closed forms of special cases
+same numbers, the complex-rotation form of RoPE, the LM heads (final norm with
+the stack's own weight, then the vocab matrix) against torch's rms_norm and a
+float64 product with planted mistakes caught, closed forms of special cases
 (one key -> the value, zero query -> the mean value), causality, and
 prefill-vs-incremental agreement.
 """

@@ -199,3 +199,62 @@ def test_greedy_ar_teacher_forcing_reproduces_free_run(tiny, tiny_ar):
 def test_top2_lowest_index_on_ties():
     x = np.float32([1.0, 3.0, 2.0, 3.0, 3.0])
     assert om.top2(x)[:2] == (1, 3)
+
+
+def _head_workload(dtype):
+    cfg = si.small_model(n_layers=1, d_model=64, n_heads=4, n_kv_heads=2, head_dim=16,
+                         d_ffn=96, vocab=211, dtype=dtype, init_std=0.1)
+    w = si.Workload("h", cfg, 1, 1, (0, 1), 4, 4, (0.5,))
+    params = si.generate_weights(w)
+    # non-unit, sign-changing norm weights, different for the two heads
+    params["final_norm"] = torch.linspace(-1.25, 2.0, 64)
+    params["pdm.norm"] = torch.linspace(1.75, 0.25, 64)
+    return cfg, w, params
+
+
+def _torch_head(h, norm_w, head_w, eps):
+    """logits = W_lm . rms_norm(h; w), from torch's rms_norm and a float64 product."""
+    T = lambda a: torch.as_tensor(np.asarray(a)).double()
+    x = F.rms_norm(T(h), (h.shape[-1],), T(norm_w), eps=eps)
+    return (T(head_w) @ x).numpy()
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_head_logits_match_torch_norm_and_float64_product(dtype):
+    """Target LM head (SPD summary step 5: the exiting token's logits) and the draft module's own
+    head (step 4) = final RMSNorm with that stack's own weight, then the untied vocab matrix."""
+    from oracle import spd as ospd
+    cfg, w, params = _head_workload(dtype)
+    target, pdm = ospd.build(w, params)
+    for seed, stack, norm, head in ((21, target, "final_norm", "lm_head"),
+                                    (22, pdm.stack, "pdm.norm", "pdm.lm_head")):
+        h = _rand(64, seed, 3.0)
+        want = _torch_head(h, params[norm], params[head].float(), cfg.norm_eps)
+        got = stack.logits(h)
+        assert got.shape == (cfg.vocab,)
+        np.testing.assert_allclose(got, want, rtol=2e-5, atol=2e-5 * np.abs(want).max())
+        # the argmax the verification uses is the float64 construction's
+        assert om.top2(got)[0] == int(np.argmax(want)) or \
+            np.sort(want)[-1] - np.sort(want)[-2] < 1e-4
+
+
+def test_planted_head_mistakes_are_caught(monkeypatch):
+    """A head that skips the final norm, or normalises with the other stack's weight, fails the pin."""
+    from oracle import spd as ospd
+    cfg, w, params = _head_workload("f32")
+    target, pdm = ospd.build(w, params)
+    h = _rand(64, 23, 3.0)
+    want = _torch_head(h, params["final_norm"], params["lm_head"], cfg.norm_eps)
+
+    def far(got):
+        return np.abs(got - want).max() > 1e-2 * np.abs(want).max()
+
+    with monkeypatch.context() as m:  # dropped final norm
+        m.setattr(om, "rmsnorm", lambda x, wt, eps: x)
+        assert far(target.logits(h))
+    swapped = om.Decoder(cfg, params, norm_name="pdm.norm")  # the draft module's norm weight
+    assert far(swapped.logits(h))
+    with monkeypatch.context() as m:  # norm without its weight (all ones)
+        m.setattr(target, "norm", np.ones(64, np.float32))
+        assert far(target.logits(h))
+    assert not far(target.logits(h))
