@@ -178,6 +178,28 @@ int spd_rollback(spd_handle* h, int32_t keep_len, int32_t reseed_token);
 int spd_set_draft_override(spd_handle* h, int32_t first_pos, int32_t count,
                            const int32_t* ref_tokens, const uint8_t* modes);
 
+/* Seeded acceptance from (alpha, seed) alone -- the same harness knob as spd_set_draft_override,
+ * with the coins drawn inside the library so that a C caller reproduces a workload's acceptance
+ * rate without computing them.  Not part of the method: random-init draft weights cannot reproduce
+ * a trained draft module's acceptance, so each workload fixes alpha.
+ *   coin(q) = (SplitMix64 output from state seed ^ q * 0x9E3779B97F4A7C15) >> 11, divided by 2^53
+ *   (SplitMix64: Steele, Lea, Flood, OOPSLA 2014); keyed by the position q only.
+ *   The draft for position q (P+2 <= q <= P+n_ref) becomes ref_tokens[q-P-1] when coin(q) < alpha
+ *   (mode 1 of spd_set_draft_override), else the draft module's best-ranked token that differs from
+ *   it (mode 2).  The draft module always runs in full; every such position is verified once on a
+ *   correct prefix, so the reject set is exactly {q : coin(q) >= alpha}.
+ *   ref_tokens: HOST array of n_ref tokens at positions P+1..P+n_ref (the plain greedy AR stream,
+ *   e.g. from spd_generate_ar), copied.  alpha is compared in double precision; alpha < 0 switches
+ *   the knob off (raw draft-module drafts).  Call after spd_prefill (which clears it).
+ *   SPD_ESTATE before a prefill; SPD_EINVAL for alpha > 1, n_ref < 1, P + n_ref > max_seq or a token
+ *   outside 0..V-1. */
+int spd_set_acceptance(spd_handle* h, double alpha, uint64_t seed, const int32_t* ref_tokens, int32_t n_ref);
+
+/* The modes spd_set_acceptance derives, on the host, without a handle or a GPU:
+ * modes[i] = 1 if coin(first_pos + i) < alpha else 2, for i < count.  SPD_EINVAL (message in
+ * spd_last_error(NULL)) for count < 0, first_pos < 0 or a NULL array with count > 0. */
+int spd_acceptance_modes(double alpha, uint64_t seed, int32_t first_pos, int32_t count, uint8_t* modes);
+
 /* Sampled decoding (temperature > 0, top-k; SPD news 六 and SPD summary 复现评估: T in {0, 1},
  * top-k 50, top-p 1.0).  Drafts are drawn from the draft module's top-k distribution and verified
  * by rejection sampling: accept with probability min(1, p/q), else the token is drawn from
@@ -266,7 +288,9 @@ int spd_cycle_bytes(const spd_handle* h, int32_t t, int32_t fill, int32_t exited
  * and each query head h, out[r][h][:] = softmax(q_r,h . K[kv(h)][0..pos[r]-1]^T / sqrt(hd)) V,
  * with kv(h) = h / (Hq/Hkv).  q: fp32 [R][Hq][hd] (already rotated); k_cache, v_cache:
  * [Hkv][max_seq][hd] in `dtype`; pos: device int32 [R] (1 <= pos <= max_seq); out: fp32
- * [R][Hq][hd].  Split over key chunks of 128 positions (the split count depends only on pos);
+ * [R][Hq][hd].  A row whose pos lies outside 1..max_seq is not computed: its output row is set to
+ * NaN (the device array cannot be checked on the host without a synchronisation).
+ * Split over key chunks of 128 positions (the split count depends only on pos);
  * chunk partials are merged in chunk order by the last chunk to finish.  `workspace` (device,
  * >= spd_attention_workspace_bytes(...) bytes, 16-byte aligned) holds the partials and
  * counters; it must be zeroed before its first use and is left zeroed by each call.

@@ -107,6 +107,9 @@ def lib() -> ctypes.CDLL:
         "spd_generate_ar": (ctypes.c_int, [vp, i32, vp, _I32P, ctypes.POINTER(spd_stats)]),
         "spd_rollback": (ctypes.c_int, [vp, i32, i32]),
         "spd_set_draft_override": (ctypes.c_int, [vp, i32, i32, _I32P, ctypes.POINTER(ctypes.c_uint8)]),
+        "spd_set_acceptance": (ctypes.c_int, [vp, ctypes.c_double, ctypes.c_uint64, _I32P, i32]),
+        "spd_acceptance_modes": (ctypes.c_int, [ctypes.c_double, ctypes.c_uint64, i32, i32,
+                                                ctypes.POINTER(ctypes.c_uint8)]),
         "spd_set_options": (ctypes.c_int, [vp, i32]),
         "spd_set_sampling": (ctypes.c_int, [vp, ctypes.c_float, i32, i32, i32, ctypes.POINTER(ctypes.c_float)]),
         "spd_dump_size": (sz, [vp, i32]),
@@ -307,6 +310,13 @@ class Engine:
                                             ref.ctypes.data_as(_I32P),
                                             md.ctypes.data_as(ctypes.POINTER(ctypes.c_uint8))), self.h)
 
+    def set_acceptance(self, alpha: float, seed: int, ref_tokens) -> None:
+        """Seeded acceptance from (alpha, seed): ref_tokens are the reference tokens at positions
+        P+1.. (the plain AR stream); alpha < 0 switches the knob off."""
+        ref = np.ascontiguousarray(np.asarray(ref_tokens, dtype=np.int32))
+        _check(lib().spd_set_acceptance(self.h, float(alpha), int(seed) & ((1 << 64) - 1),
+                                        ref.ctypes.data_as(_I32P), int(ref.size)), self.h)
+
     def set_options(self, flags: int) -> None:
         _check(lib().spd_set_options(self.h, int(flags)), self.h)
 
@@ -359,6 +369,15 @@ class Engine:
         _check(lib().spd_cycle_bytes(self.h, int(t), int(fill), int(bool(exited)), int(bool(with_pdm)),
                                      out, n), self.h)
         return {KIND_NAMES[k]: float(out[k]) for k in range(n)}
+
+
+def acceptance_modes(alpha: float, seed: int, first_pos: int, count: int) -> np.ndarray:
+    """The harness modes spd_set_acceptance derives (1 = reference token, 2 = another token), computed
+    by the library on the host for positions first_pos .. first_pos+count-1."""
+    out = np.zeros(max(0, int(count)), dtype=np.uint8)
+    _check(lib().spd_acceptance_modes(float(alpha), int(seed) & ((1 << 64) - 1), int(first_pos), int(count),
+                                      out.ctypes.data_as(ctypes.POINTER(ctypes.c_uint8))))
+    return out
 
 
 # ---------------------------------------------------------------------------

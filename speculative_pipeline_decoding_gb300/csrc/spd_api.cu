@@ -833,6 +833,45 @@ int spd_set_draft_override(spd_handle* h, int32_t first_pos, int32_t count, cons
   return SPD_OK;
 }
 
+int spd_acceptance_modes(double alpha, uint64_t seed, int32_t first_pos, int32_t count, uint8_t* modes) {
+  if (count < 0 || (count && !modes) || first_pos < 0)
+    return fail(nullptr, SPD_EINVAL, "acceptance modes: bad range or NULL output");
+  // SplitMix64 (Steele, Lea, Flood, OOPSLA 2014): one step from state x = seed ^ q * golden, i.e.
+  // mix(x + golden); the coin is its top 53 bits over 2^53, compared with alpha in double precision
+  const uint64_t golden = 0x9E3779B97F4A7C15ull;
+  for (int32_t i = 0; i < count; ++i) {
+    const uint64_t q = (uint64_t)(first_pos + i);
+    uint64_t z = (seed ^ (q * golden)) + golden;
+    z = (z ^ (z >> 30)) * 0xBF58476D1CE4E5B9ull;
+    z = (z ^ (z >> 27)) * 0x94D049BB133111EBull;
+    z ^= z >> 31;
+    const double coin = (double)(z >> 11) / 9007199254740992.0;  // 2^53
+    modes[i] = coin < alpha ? 1 : 2;
+  }
+  return SPD_OK;
+}
+
+int spd_set_acceptance(spd_handle* h, double alpha, uint64_t seed, const int32_t* ref_tokens, int32_t n_ref) {
+  if (!h) return SPD_EINVAL;
+  if (!h->prefilled) return fail(h, SPD_ESTATE, "set_acceptance before prefill");
+  const int P = h->P;
+  if (alpha < 0.0) {  // knob off: raw draft-module drafts
+    SPD_CUDA(h, cudaMemsetAsync(h->B.ovr_mode, 0, h->D.max_seq + 2, h->s_main));
+    SPD_CUDA(h, cudaStreamSynchronize(h->s_main));
+    return SPD_OK;
+  }
+  if (!(alpha <= 1.0)) return fail(h, SPD_EINVAL, "alpha must be <= 1 (or < 0 to switch the knob off)");
+  if (n_ref < 1 || !ref_tokens) return fail(h, SPD_EINVAL, "need >= 1 reference token");
+  if (P + n_ref > h->D.max_seq) return fail(h, SPD_EINVAL, "P + n_ref exceeds max_seq");
+  // positions P+2..P+n_ref are drafted (P+1 comes from the prefill); ref_tokens[i] is position P+1+i
+  const int count = n_ref - 1;
+  if (!count) return SPD_OK;
+  std::vector<uint8_t> modes(count);
+  int rc;
+  if ((rc = spd_acceptance_modes(alpha, seed, P + 2, count, modes.data()))) return fail(h, rc, "%s", g_create_error.c_str());
+  return spd_set_draft_override(h, P + 2, count, ref_tokens + 1, modes.data());
+}
+
 int spd_set_sampling(spd_handle* h, float temperature, int32_t top_k, int32_t first_pos, int32_t count,
                      const float* uniforms) {
   if (!h) return SPD_EINVAL;

@@ -94,3 +94,33 @@ def test_no_oracle_import_in_the_product_package():
                 text = open(os.path.join(dirpath, f), encoding="utf-8").read()
                 assert not re.search(r"^\s*(import|from)\s+oracle", text, re.M), f
                 assert "spd_inputs" not in text, f
+
+
+@pytest.mark.parametrize("seed,alpha", [(2, 0.8), (2, 0.5), (2, 0.9), (7, 0.6), (2**64 - 1, 0.85),
+                                        (0, 0.0), (123456789, 1.0)])
+def test_library_acceptance_modes_equal_the_harness_coins(L, seed, alpha):
+    """spd_acceptance_modes (C, host only) draws the same SplitMix64 coins as the seeded input module."""
+    import spd_inputs as si
+    from speculative_pipeline_decoding_gb300 import binding
+    first, last = 514, 514 + 700
+    got = binding.acceptance_modes(alpha, seed, first, last - first + 1).tolist()
+    assert got == si.override_modes(seed, alpha, first, last)
+
+
+def test_library_acceptance_compares_in_double_precision(L):
+    """A coin exactly at alpha is a reject; one ulp above it is an accept (no float rounding of alpha)."""
+    import math
+    import spd_inputs as si
+    from speculative_pipeline_decoding_gb300 import binding
+    for q in (3, 1000, 40000):
+        c = si.coin(2, q)
+        assert binding.acceptance_modes(c, 2, q, 1).tolist() == [2]
+        assert binding.acceptance_modes(math.nextafter(c, 2.0), 2, q, 1).tolist() == [1]
+
+
+def test_acceptance_argument_checks_on_the_host(L):
+    from speculative_pipeline_decoding_gb300 import binding
+    with pytest.raises(binding.SpdError):
+        binding.acceptance_modes(0.5, 1, -1, 4)
+    assert L.spd_acceptance_modes(0.5, 1, 0, 3, None) == -1
+    assert L.spd_set_acceptance(None, 0.5, 1, None, 0) == -1

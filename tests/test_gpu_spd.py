@@ -173,6 +173,28 @@ def test_tiny_spd_equals_ar_trace_equals_coins(tiny_setup, alpha):
         assert stats["rejects"] == acc.count(False)
 
 
+@pytest.mark.parametrize("setup", ["tiny_setup", "small_setup"])
+def test_library_acceptance_knob_equals_host_modes(request, setup):
+    """spd_set_acceptance(alpha, seed, ref) draws its coins in the library; the committed stream,
+    the trace and the cycle count equal those of the modes computed on the host."""
+    S = request.getfixturevalue(setup)
+    alpha = S.w.alphas[0]
+    toks0, stats0, trace0 = S.spd_run(alpha)
+    S.eng.rollback(S.P, S.first)
+    S.eng.set_draft_override(S.P + 2, S.ar[1:], [0] * (S.G - 1))  # cleared below by the knob
+    S.eng.set_acceptance(alpha, S.w.coin_seed, S.ar)
+    toks, stats = S.eng.generate(S.G)
+    trace = S.eng.dump(DUMP_TRACE)[:, : S.eng.state()["exits"]]
+    assert toks.tolist() == toks0 == S.ar
+    assert np.array_equal(trace, trace0)
+    assert stats["cycles"] == stats0["cycles"] and stats["rejects"] == stats0["rejects"]
+    # alpha < 0: raw draft-module drafts (no override), still lossless
+    S.eng.rollback(S.P, S.first)
+    S.eng.set_acceptance(-1.0, 0, S.ar)
+    raw, _ = S.eng.generate(S.G)
+    assert raw.tolist() == S.ar
+
+
 def test_tiny_per_cycle_parity_with_oracle(tiny_setup):
     worst = per_cycle_parity(tiny_setup, 0.7, 60, 1e-4)
     print("tiny fp32 worst relative errors", worst)
