@@ -12,6 +12,8 @@
 // Stand-alone launches of decode attention (device code in spd_attn.cuh): prefill blocks, the
 // per-operator path used when the step kernel is not, and the stand-alone operators.  Chunks of
 // 128 keys; every CTA of the grid takes items blockIdx.x, blockIdx.x + gridDim.x, ...
+#include <mutex>
+
 #include "spd_attn.cuh"
 
 namespace spd {
@@ -73,16 +75,21 @@ int attn_grid(const Dims& D, bool multi) {
   return num_sms() * (occ > 0 ? occ : 1);
 }
 
-// Raise the kernels' dynamic shared-memory limit to `need` (never lowered by a later call).
+// Raise the kernels' dynamic shared-memory limit on the current device to `need` (never lowered by a
+// later call).  The limit belongs to one device, so the raised value is kept per device ordinal,
+// under a mutex (host threads may make their first calls concurrently).
 cudaError_t attn_setup_attributes(size_t need) {
-  static size_t current = 0;
-  if (need <= current) return cudaSuccess;
-  cudaError_t e = cudaFuncSetAttribute(attn_kernel<float>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       (int)need);
+  static std::mutex mu;
+  static size_t current[64] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  e = cudaFuncSetAttribute(attn_kernel<__nv_bfloat16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           (int)need);
-  if (e == cudaSuccess) current = need;
+  std::lock_guard<std::mutex> lock(mu);
+  if (dev >= 0 && dev < 64 && need <= current[dev]) return cudaSuccess;
+  e = cudaFuncSetAttribute(attn_kernel<float>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)need);
+  if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(attn_kernel<__nv_bfloat16>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)need);
+  if (e == cudaSuccess && dev >= 0 && dev < 64) current[dev] = need;
   return e;
 }
 

@@ -39,9 +39,19 @@ static __device__ int add_tiles(const Dims& D, const Bufs& B, const Launch& lc, 
   RowGroup rg[kMaxGroups];
   int nr;
   if (lc.kind == LK_EXPLICIT) {
-    nr = lc.cnt;
-    for (int r = 0; r < nr; ++r) {
-      rg[r].layer = 0; rg[r].nv = 1; rg[r].pos0 = lc.act.pos_arr[r]; rg[r].vid0 = r; rg[r].rrow0 = 0;
+    // caller-given positions: a row outside 1..max_seq would read keys and write partials past the
+    // cache and the scratch; it gets no tile, and its output row is filled with NaN so that the
+    // caller sees it (every CTA writes the same value)
+    nr = 0;
+    for (int r = 0; r < lc.cnt && r < kMaxGroups; ++r) {
+      const int p = lc.act.pos_arr[r];
+      if (p < 1 || p > D.max_seq) {
+        float* o = lc.act.attn + (size_t)r * D.hq * D.hd;
+        for (int i = 0; i < D.hq * D.hd; ++i) o[i] = __int_as_float(0x7fc00000);
+        continue;
+      }
+      rg[nr].layer = 0; rg[nr].nv = 1; rg[nr].pos0 = p; rg[nr].vid0 = r; rg[nr].rrow0 = 0;
+      ++nr;
     }
   } else {
     nr = build_rows(lc, D, sv, st, rg);

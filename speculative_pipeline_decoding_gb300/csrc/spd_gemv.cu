@@ -4,6 +4,8 @@
 // copies, eight consumer warps compute.
 #include <cudaTypedefs.h>
 
+#include <atomic>
+
 #include "spd_engine.cuh"
 
 namespace spd {
@@ -93,15 +95,24 @@ cudaError_t launch_engine(const GemvParams& p, bool pdl, cudaStream_t s) {
 
 }  // namespace
 
+// SM count of the current device, looked up once per device ordinal (atomics: host threads may make
+// their first calls concurrently; a repeated lookup stores the same value).
 int num_sms() {
-  static int sms = 0;
-  if (sms == 0) {
-    int dev = 0;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    if (sms <= 0) sms = 1;
+  static std::atomic<int> sms[64];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) dev = 0;
+  if (dev >= 64) {
+    int n = 0;
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    return n > 0 ? n : 1;
   }
-  return sms;
+  int n = sms[dev].load(std::memory_order_relaxed);
+  if (n == 0) {
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    if (n <= 0) n = 1;
+    sms[dev].store(n, std::memory_order_relaxed);
+  }
+  return n;
 }
 
 int gemv_head_grid(int dtype) {

@@ -103,3 +103,30 @@ def test_attention_split_count_depends_only_on_position(spd):
                       torch.tensor([positions[r]], dtype=torch.int32, device="cuda"), out1, ws)
         torch.cuda.synchronize()
         assert torch.equal(out1[0], out8[r])
+
+
+def test_attention_rows_outside_the_cache_come_back_nan(spd):
+    """A caller position outside 1..max_seq is not computed (no read past the cache, no partial past
+    the workspace); that row reads NaN and the other rows are unaffected."""
+    hq, hkv, hd, max_seq = 8, 2, 64, 300
+    g = torch.Generator(device="cpu").manual_seed(2)
+    k = torch.randn(hkv, max_seq, hd, generator=g).to(torch.bfloat16).cuda()
+    v = torch.randn(hkv, max_seq, hd, generator=g).to(torch.bfloat16).cuda()
+    positions = [5, 0, max_seq + 1, 300, -3]
+    R = len(positions)
+    q = torch.randn(R, hq, hd, generator=g).cuda()
+    pos = torch.tensor(positions, dtype=torch.int32, device="cuda")
+    out = torch.zeros(R, hq, hd, device="cuda")
+    ws = torch.zeros(spd.attention_workspace_bytes(R, hq, hkv, hd, max_seq) // 4 + 1,
+                     dtype=torch.int32, device="cuda")
+    spd.attention(q, k, v, pos, out, ws)
+    torch.cuda.synchronize()
+    oc = out.cpu()
+    for r in (1, 2, 4):
+        assert torch.isnan(oc[r]).all(), r
+    kc, vc, qc = (t.float().cpu().numpy() for t in (k, v, q))
+    for r in (0, 3):
+        p = positions[r]
+        for h in range(hq):
+            want = om.softmax_attend(qc[r, h], kc[h // (hq // hkv), :p], vc[h // (hq // hkv), :p])
+            np.testing.assert_allclose(oc[r, h].numpy(), want, rtol=2e-5, atol=2e-5)
