@@ -7,6 +7,10 @@ cycles until gen_len tokens are committed.  Inputs (weights, prompt KV, draft ov
 resident in HBM before the timed region; the weights (>= 3.4 GB per cycle) are larger than L2, so
 no flush is needed between steps.  Prints ONE JSON line on rank 0.
 
+Default workload: the 9B-class model (L 32, d 4096, 32 q / 8 kv heads x 128, ffn 12288, vocab
+151936, bf16) at n = 8, Ls = 4, prompt 2048, 512 tokens, alpha 0.9 (its other acceptance rate, 0.5,
+and the 1.5B-class and 4B-class workloads are reported under extra keys).
+
   python bench.py [--gpus N --steps K --warmup W --workload NAME --alpha A]
   python bench.py --impl reference      # the CPU oracle timed on the host cores
   python bench.py --profile-cycles K    # K eager SPD cycles, for ncu launch lists and captures
@@ -25,8 +29,10 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "committed tokens/s (1 seq, greedy SPD n=8) and cycle HBM GB/s vs peak"
-DEFAULT_WORKLOAD = "dense1.5b_bf16_n8"
+DEFAULT_WORKLOAD = "gqa9b_bf16_n8"
+EXTRA_WORKLOADS = ("dense1.5b_bf16_n8", "gqa4b_bf16_n8")
 SPEC_HBM_GBS = 8000.0
+TRAFFIC_FILE = os.path.join("profiles", "step_kernel_traffic.json")
 
 
 def parse():
@@ -39,32 +45,38 @@ def parse():
     ap.add_argument("--alpha", type=float, default=None)
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--extra", default=",".join(EXTRA_WORKLOADS),
+                    help="comma-separated workloads measured briefly after the headline one ('' for none)")
     ap.add_argument("--profile-cycles", type=int, default=0,
                     help="profiling case: prefill, then this many SPD cycles as plain (non-graph) "
                          "launches of the step kernel, one per cycle; prints one summary line")
     return ap.parse_args()
 
 
-def step_kernel_traffic_ratio():
-    """DRAM bytes / algorithmic bytes of one ncu-captured step-kernel launch, from the committed profile
-    summary -- only while the CUDA sources are the ones that were profiled (else None)."""
+def sources_sha1() -> str:
+    """SHA-1 over the CUDA sources (.cu, .cuh) in name order."""
     import hashlib
     src = os.path.join(ROOT, "speculative_pipeline_decoding_gb300", "csrc")
-    prof = os.path.join(ROOT, "profiles", "step_kernel_dense1.5b_n8_sections.md")
+    h = hashlib.sha1()
+    for f in sorted(os.listdir(src)):
+        if f.endswith((".cu", ".cuh")):
+            with open(os.path.join(src, f), "rb") as fh:
+                h.update(fh.read())
+    return h.hexdigest()
+
+
+def step_kernel_traffic_ratio(workload: str):
+    """DRAM bytes / algorithmic bytes of one ncu-captured step-kernel launch of `workload`, from the
+    machine-readable capture record under profiles/ -- only while the CUDA sources are the ones that
+    were captured (else None)."""
     try:
-        h = hashlib.sha1()
-        for f in sorted(os.listdir(src)):
-            if f.endswith((".cu", ".cuh")):
-                with open(os.path.join(src, f), "rb") as fh:
-                    h.update(fh.read())
-        with open(prof) as fh:
-            for line in fh:
-                parts = line.split()
-                if len(parts) == 4 and parts[0] == "traffic_ratio:" and parts[2] == "sources_sha1:":
-                    return float(parts[1]) if parts[3] == h.hexdigest() else None
-    except OSError:
+        with open(os.path.join(ROOT, TRAFFIC_FILE)) as fh:
+            rec = json.load(fh)
+        if rec.get("workload") != workload or rec.get("sources_sha1") != sources_sha1():
+            return None
+        return float(rec["dram_bytes"]) / float(rec["algorithmic_bytes"])
+    except (OSError, ValueError, KeyError, TypeError):
         return None
-    return None
 
 
 def measured_peaks():
@@ -168,14 +180,25 @@ def max_over_ranks(x: float, world: int) -> float:
 # ------------------------------------------------------------------------------------------------
 # the CPU oracle (baseline / reference arm)
 # ------------------------------------------------------------------------------------------------
-def oracle_run(w, alpha, params_cpu, prompt, ar_tokens):
+def oracle_refs(w):
+    """The oracle's own greedy AR stream after the workload's prompt (stored by
+    tests/golden/make_oracle_ar.py): the reference tokens of the seeded drafts when the oracle is
+    timed, so that nothing it computes comes from the GPU."""
+    sys.path.insert(0, os.path.join(ROOT, "tests", "golden"))
+    import make_oracle_ar
+    return make_oracle_ar.stream_for(w)
+
+
+def oracle_run(w, alpha, params_cpu, prompt, ref_tokens):
+    """The oracle's SPD run (prefill included, untimed) with the seeded drafts of `alpha`; positions
+    beyond the stored reference stream get no override (raw drafts)."""
     from oracle import spd as ospd
     import spd_inputs as si
     target, pdm = ospd.build(w, params_cpu)
     P, G = len(prompt), w.gen_len
-    first, last = P + 2, P + G
+    first, last = P + 2, min(P + G, P + len(ref_tokens))
     modes = dict(zip(range(first, last + 1), si.override_modes(w.coin_seed, alpha, first, last)))
-    ref = {q: int(ar_tokens[q - P - 1]) for q in range(first, last + 1)}
+    ref = {q: int(ref_tokens[q - P - 1]) for q in range(first, last + 1)}
     return ospd.SPDRun(target, pdm, w.n_stages, w.pdm_layers, w.anchors, prompt, P + G + w.n_stages + 2,
                        modes, ref)
 
@@ -200,6 +223,48 @@ def cpu_cores():
         return os.cpu_count() or 1
 
 
+def _oracle_child(conn, name, alpha, seconds):
+    """Spawned process: builds the oracle of `name` (CPU weights, untimed prefill of the whole prompt),
+    waits for the parent's go (its GPU measurements are done), times a sample of SPD cycles and sends
+    the cpu_baseline record."""
+    try:
+        import spd_inputs as si
+        w = si.WORKLOADS[name]
+        params = si.generate_weights(w, device="cpu")
+        prompt = si.prompt_tokens(w).tolist()
+        refs = oracle_refs(w)
+        if refs is None:
+            conn.send({"error": f"no stored oracle reference stream for {name}"})
+            return
+        t0 = time.perf_counter()
+        run = oracle_run(w, alpha, params, prompt, refs)
+        del params
+        prep = time.perf_counter() - t0
+        conn.send({"ready": True})
+        if conn.recv() != "go":
+            return
+        tps, c, toks, el = oracle_sample(run, seconds, w.n_stages + 2)
+        conn.send({"value": tps, "unit": "tokens/s", "cores": cpu_cores(), "kind": "oracle",
+                   "sample": f"{c} SPD cycles of the fp32 numpy oracle after its untimed prefill of the "
+                             f"{len(prompt)}-token prompt ({prep:.0f} s, overlapped with the GPU legs): "
+                             f"{toks} tokens in {el:.1f} s"})
+    except Exception as e:  # reported in the JSON line instead of a baseline
+        conn.send({"error": repr(e)})
+
+
+def bench_config(w, alpha, world):
+    """The `config` object of both arms: the same keys for the same workload."""
+    return {"workload": w.name, "prompt": w.prompt_len, "gen": w.gen_len, "alpha": alpha,
+            "n_stages": w.n_stages, "pdm_layers": w.pdm_layers, "anchors": list(w.anchors),
+            "l2": "inputs larger than L2: every cycle streams all weights (>= 3.4 GB)",
+            "parallelism": f"replicas x{world}"}
+
+
+def default_alpha(w, args):
+    """The headline acceptance rate: --alpha, else the workload's highest."""
+    return args.alpha if args.alpha is not None else max(w.alphas)
+
+
 # ------------------------------------------------------------------------------------------------
 # per-cycle accounting from the verification trace
 # ------------------------------------------------------------------------------------------------
@@ -222,27 +287,22 @@ def cycle_states(P, n, accepts, n_cycles):
 
 
 def main_reference(args):
-    import torch
     import spd_inputs as si
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     if world > 1 and rank != 0:
         return 0
     w = si.WORKLOADS[args.workload]
-    alpha = args.alpha if args.alpha is not None else w.alphas[0]
-    params = si.generate_weights(w, device="cuda" if torch.cuda.is_available() else "cpu")
-    params_cpu = {k: v.cpu() for k, v in params.items()}
-    del params
+    alpha = default_alpha(w, args)
+    refs = oracle_refs(w)
+    if refs is None:
+        print(json.dumps({"impl": "reference", "unavailable": f"no stored oracle reference stream for {w.name}"}))
+        return 0
+    params_cpu = si.generate_weights(w, device="cpu")
     prompt = si.prompt_tokens(w).tolist()
-    # the reference stream for the seeded drafts comes from the oracle itself (greedy AR)
-    from oracle import model as om
-    from oracle import spd as ospd
     cycles_per_step = max(2, w.n_stages // 2)
-    need = min(w.gen_len, (args.warmup + args.steps) * cycles_per_step + 2 * w.n_stages + 2)
-    target, _ = ospd.build(w, params_cpu)
-    ar = om.greedy_ar(target, prompt, need)["tokens"]
-    ar = ar + [0] * (w.gen_len - len(ar))  # positions the sample never reaches
-    run = oracle_run(w, alpha, params_cpu, prompt, ar)
+    run = oracle_run(w, alpha, params_cpu, prompt, refs)
+    del params_cpu
     for _ in range(w.n_stages):  # untimed pipeline fill: the first token exits after n cycles
         run.cycle()
     for _ in range(args.warmup):
@@ -262,8 +322,7 @@ def main_reference(args):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * el / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
         "data": "synthetic",
-        "config": {"workload": w.name, "prompt": len(prompt), "gen": w.gen_len, "alpha": alpha,
-                   "n_stages": w.n_stages, "pdm_layers": w.pdm_layers, "anchors": list(w.anchors)},
+        "config": bench_config(w, alpha, world),
         "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle",
                          "sample": f"{args.steps} steps x {cycles_per_step} SPD cycles of the fp32 "
                                    f"numpy oracle after its prefill and an untimed pipeline fill of "
@@ -274,44 +333,83 @@ def main_reference(args):
     return 0
 
 
+class GpuWorkload:
+    """One workload's engine on the GPU: weights, prefill, its plain AR stream, seeded drafts."""
+
+    def __init__(self, name, alpha, stream):
+        import torch
+        import spd_inputs as si
+        import speculative_pipeline_decoding_gb300 as spd
+        self.w = w = si.WORKLOADS[name]
+        self.alpha = alpha
+        self.P, self.G, self.n = w.prompt_len, w.gen_len, w.n_stages
+        self.params = si.generate_weights(w, device="cuda")
+        self.prompt = si.prompt_tokens(w).tolist()
+        torch.cuda.synchronize()  # weights are written on torch's stream; the engine uses its own
+        self.stream = stream
+        self.eng = spd.Engine(spd.Config.from_workload(w), self.params, stream=stream)
+        self.first = self.eng.prefill(self.prompt)
+        ar, _ = self.eng.generate_ar(self.G)
+        self.ar = ar.tolist()
+        self.set_alpha(alpha)
+
+    def set_alpha(self, alpha):
+        self.alpha = alpha
+        self.eng.set_acceptance(alpha, self.w.coin_seed, self.ar)
+
+    def spd_step(self):
+        self.eng.rollback(self.P, self.first)
+        return self.eng.generate(self.G)
+
+    def ar_step(self):
+        self.eng.rollback(self.P, self.first)
+        return self.eng.generate_ar(self.G)
+
+    def step_bytes(self, cycles):
+        """Algorithmic bytes of the last SPD run's cycles, rebuilt from its verification trace."""
+        from speculative_pipeline_decoding_gb300 import binding as B
+        trace = self.eng.dump(B.DUMP_TRACE)[:, : self.eng.state()["exits"]]
+        accepts = [bool(x) for x in trace[1]]
+        total = 0.0
+        for (t, a, ex) in cycle_states(self.P, self.n, accepts, cycles):
+            total += sum(self.eng.cycle_bytes(t, a, ex, True).values())
+        return total
+
+    def close(self):
+        import torch
+        self.eng.close()
+        del self.params
+        torch.cuda.empty_cache()
+
+
 def main_spd(args):
     import numpy as np
     import torch
     import spd_inputs as si
-    import speculative_pipeline_decoding_gb300 as spd
     from speculative_pipeline_decoding_gb300 import binding as B
     from speculative_pipeline_decoding_gb300 import build_ext
 
     world, rank, local = dist_setup(args)
+    w = si.WORKLOADS[args.workload]
+    alpha = default_alpha(w, args)
+    # the CPU oracle's baseline: its process is spawned before the first GPU call and prepares its
+    # (long, untimed) prefill while the GPU legs run; its timed sample starts after them
+    child = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        import multiprocessing as mp
+        ctx = mp.get_context("spawn")
+        conn, child_conn = ctx.Pipe()
+        child = ctx.Process(target=_oracle_child, args=(child_conn, w.name, alpha, args.cpu_seconds), daemon=True)
+        child.start()
     build_ext.build()
     torch.cuda.set_device(local)
-    w = si.WORKLOADS[args.workload]
-    alpha = args.alpha if args.alpha is not None else w.alphas[0]
-    m = w.model
-    P, G, n = w.prompt_len, w.gen_len, w.n_stages
-    params = si.generate_weights(w, device="cuda")
-    prompt = si.prompt_tokens(w).tolist()
     stream = torch.cuda.Stream()
-    torch.cuda.synchronize()  # weights are written on torch's stream; the engine uses its own
-    eng = spd.Engine(spd.Config.from_workload(w), params, stream=stream)
-    first = eng.prefill(prompt)
-    ar, _ = eng.generate_ar(G)
-    ar_list = ar.tolist()
-    modes = si.override_modes(w.coin_seed, alpha, P + 2, P + G)
-    eng.set_draft_override(P + 2, ar_list[1:], modes)
+    W = GpuWorkload(w.name, alpha, stream)
+    P, G, n = W.P, W.G, W.n
+    eng = W.eng
 
-    def spd_step():
-        eng.rollback(P, first)
-        toks, st = eng.generate(G)
-        return toks, st
-
-    def ar_step():
-        eng.rollback(P, first)
-        toks, st = eng.generate_ar(G)
-        return toks, st
-
-    def timed(fn, K, W, clocks=None, tag="spd_other"):
-        for _ in range(W):
+    def timed(fn, K, Wm, clocks=None, tag="spd_other"):
+        for _ in range(Wm):
             fn()
         barrier(world)
         torch.cuda.synchronize()
@@ -332,64 +430,75 @@ def main_spd(args):
         barrier(world)
         return e0.elapsed_time(e1), last, launches, ck
 
-    # --- main measurement: SPD, graphs, draft module on its own stream ---
-    toks, _ = spd_step()
-    lossless = toks.tolist() == ar_list
+    # --- main measurement: SPD, one step-kernel launch per cycle replayed from a CUDA graph ---
+    toks, _ = W.spd_step()
+    lossless = toks.tolist() == W.ar
     clk = Clocks(local)
-    ms, (toks, st), launches, clocks = timed(spd_step, args.steps, args.warmup, clk, tag="spd_timed")
+    ms, (toks, st), launches, clocks = timed(W.spd_step, args.steps, args.warmup, clk, tag="spd_timed")
     ms_max = max_over_ranks(ms, world)
     cycles = st["cycles"]
     value = aggregate_tokens_per_s(world, args.steps, G, ms_max)
     ms_step = ms_max / args.steps
-    trace = eng.dump(B.DUMP_TRACE)[:, : eng.state()["exits"]]
-    accepts = [bool(x) for x in trace[1]]
-    states = cycle_states(P, n, accepts, cycles)
-    bytes_kind = [0.0] * len(B.KIND_NAMES)
-    for (t, a, ex) in states:
-        cb = eng.cycle_bytes(t, a, ex, True)
-        for k, name in enumerate(B.KIND_NAMES):
-            bytes_kind[k] += cb[name]
-    step_bytes = sum(bytes_kind)
+    step_bytes = W.step_bytes(cycles)
     cycle_gbs = step_bytes / (ms_step / 1e3) / 1e9
+    Kx = 3
+
+    # --- the workload's other acceptance rates (same kernels, same bytes per full cycle) ---
+    other_alphas = {}
+    for a2 in w.alphas:
+        if a2 == alpha:
+            continue
+        W.set_alpha(a2)
+        ms2, (toks2, st2), _, _ = timed(W.spd_step, Kx, 1)
+        b2 = W.step_bytes(st2["cycles"])
+        other_alphas[str(a2)] = {"tokens_per_s": Kx * G / (ms2 / 1e3), "cycles_per_step": st2["cycles"],
+                                 "rejects_per_step": st2["rejects"], "cycle_ms": ms2 / Kx / st2["cycles"],
+                                 "cycle_hbm_frac": b2 / (ms2 / Kx / 1e3) / 1e9 / measured_peaks()[0],
+                                 "lossless_vs_ar": toks2.tolist() == W.ar}
+    W.set_alpha(alpha)
 
     # --- AR from the same kernels ---
-    ms_ar, _, _, _ = timed(ar_step, max(3, args.steps // 2), 2)
-    ar_tps = max(3, args.steps // 2) * G / (ms_ar / 1e3)
+    ms_ar, _, _, _ = timed(W.ar_step, Kx, 1)
+    ar_tps = Kx * G / (ms_ar / 1e3)
+    ar_bytes = sum(eng.cycle_bytes(P + G // 2, n, True, False).values())  # one token through all layers
 
     # --- target only (no draft module), and draft module serialised (its own phases first) ---
     step = B.OPT_STEP | B.OPT_PDL | B.OPT_GRAPHS
     eng.set_options(step | B.OPT_TARGET_ONLY)
-    ms_tgt, (toks_t, st_t), _, _ = timed(spd_step, max(3, args.steps // 2), 1)
+    ms_tgt, (toks_t, st_t), _, _ = timed(W.spd_step, Kx, 1)
+    tgt_bytes = 0.0
+    tr_t = eng.dump(B.DUMP_TRACE)[:, : eng.state()["exits"]]
+    for (t, a, ex) in cycle_states(P, n, [bool(x) for x in tr_t[1]], st_t["cycles"]):
+        tgt_bytes += sum(eng.cycle_bytes(t, a, ex, False).values())
     eng.set_options(step)
-    ms_ser, _, _, _ = timed(spd_step, max(3, args.steps // 2), 1)
+    ms_ser, _, _, _ = timed(W.spd_step, Kx, 1)
     # post-step schedule (the pages' scheduling ablation): the draft module after the target step,
     # on its output state; same cycles and committed stream, drafting no longer hidden
     eng.set_options(step | B.OPT_POST_STEP)
-    ms_post, (toks_p, st_p), _, _ = timed(spd_step, max(3, args.steps // 2), 1)
-    Kx = max(3, args.steps // 2)
+    ms_post, (toks_p, st_p), _, _ = timed(W.spd_step, Kx, 1)
     t_cycle = ms_step / cycles
     t_tgt = ms_tgt / Kx / st_t["cycles"]
     t_ser = ms_ser / Kx / cycles
     t_post = ms_post / Kx / st_p["cycles"]
     post_tps = Kx * G / (ms_post / 1e3)
-    post_lossless = toks_p.tolist() == ar_list and st_p["cycles"] == cycles
+    post_lossless = toks_p.tolist() == W.ar and st_p["cycles"] == cycles
     # sampled decoding (T = 1, top-k 50, rejection-sampling verification) on seeded uniforms: the
     # acceptance is the draft module's (random weights: rarely), so this times cycles with the
     # sampling control step and mostly refills
     eng.set_options(B.OPT_DEFAULT)
     us = si.sampling_uniforms(w.coin_seed + 1, P + 1, P + G + n + 2)
     eng.set_sampling(1.0, 50, P + 1, np.array([us[k] for k in si.SAMPLING_STREAMS], dtype=np.float32))
-    ms_smp, (_, st_s), _, _ = timed(spd_step, Kx, 1)
+    ms_smp, (_, st_s), _, _ = timed(W.spd_step, 2, 1)
     eng.set_sampling(0.0)
-    t_smp = ms_smp / Kx / st_s["cycles"]
-    smp_line = {"temperature": 1.0, "top_k": 50, "cycle_ms": t_smp, "tokens_per_s": Kx * G / (ms_smp / 1e3),
+    t_smp = ms_smp / 2 / st_s["cycles"]
+    smp_line = {"temperature": 1.0, "top_k": 50, "cycle_ms": t_smp, "tokens_per_s": 2 * G / (ms_smp / 1e3),
                 "accept_rate": 1.0 - st_s["rejects"] / max(1, st_s["exits"])}
 
     # --- instrumented pass: phase timers of the step kernel (CTA 0, grid barrier to grid barrier),
     # draft module in its own phases so that its time is separate ---
     eng.set_options(B.OPT_STEP | B.OPT_PDL)
     eng.time_kernels(True)
-    spd_step()
+    W.spd_step()
     kt = eng.kernel_times()
     eng.time_kernels(False)
     eng.set_options(B.OPT_DEFAULT)
@@ -399,31 +508,57 @@ def main_spd(args):
     # the cycle's algorithmic bytes, its duration the CUDA-event cycle time of the timed region
     peak, peak_src = measured_peaks()
     achieved = step_bytes / cycles / (t_cycle / 1e3) / 1e9
-    traffic_ratio = step_kernel_traffic_ratio()
+    traffic_ratio = step_kernel_traffic_ratio(w.name)
 
     # --- end to end through the public API with host buffers ---
-    prompt_np = __import__("numpy").asarray(prompt, dtype="int32")
-    ref_np = ar_list[1:]
+    prompt_np = np.asarray(W.prompt, dtype="int32")
+    ar_np = np.asarray(W.ar, dtype="int32")
 
     def e2e_step():
         eng.prefill(prompt_np)
-        eng.set_draft_override(P + 2, ref_np, modes)
-        toks, st = eng.generate(G)  # copies the committed tokens into a host array
-        return toks, st
+        eng.set_acceptance(alpha, w.coin_seed, ar_np)
+        return eng.generate(G)  # copies the committed tokens into a host array
 
-    ms_e2e, (toks_e2e, _), _, _ = timed(e2e_step, max(3, args.steps // 2), 1)
-    e2e_val = aggregate_tokens_per_s(world, max(3, args.steps // 2), G, max_over_ranks(ms_e2e, world))
-    lossless = lossless and toks_e2e.tolist() == ar_list
+    ms_e2e, (toks_e2e, _), _, _ = timed(e2e_step, Kx, 1)
+    e2e_val = aggregate_tokens_per_s(world, Kx, G, max_over_ranks(ms_e2e, world))
+    lossless = lossless and toks_e2e.tolist() == W.ar
+    W.close()
 
-    # --- CPU oracle baseline (rank 0, single GPU only) ---
+    # --- the other workloads, briefly (same kernels): tokens/s, AR, cycle time, roofline fraction ---
+    extra = {}
+    if rank == 0:
+        for name in [x for x in args.extra.split(",") if x and x != w.name]:
+            if name not in si.WORKLOADS:
+                continue
+            X = GpuWorkload(name, max(si.WORKLOADS[name].alphas), stream)
+            mx, (tx, sx), _, _ = timed(X.spd_step, Kx, 1)
+            bx = X.step_bytes(sx["cycles"])
+            ma, _, _, _ = timed(X.ar_step, 2, 1)
+            X.eng.set_options(step | B.OPT_TARGET_ONLY)
+            mt, (_, stt), _, _ = timed(X.spd_step, 2, 1)
+            X.eng.set_options(B.OPT_DEFAULT)
+            extra[name] = {"alpha": X.alpha, "tokens_per_s": Kx * X.G / (mx / 1e3),
+                           "ar_tokens_per_s": 2 * X.G / (ma / 1e3), "cycles_per_step": sx["cycles"],
+                           "cycle_ms": mx / Kx / sx["cycles"], "target_only_cycle_ms": mt / 2 / stt["cycles"],
+                           "cycle_hbm_gbs": bx / (mx / Kx / 1e3) / 1e9,
+                           "cycle_hbm_frac": bx / (mx / Kx / 1e3) / 1e9 / peak,
+                           "lossless_vs_ar": tx.tolist() == X.ar}
+            X.close()
+
+    # --- CPU oracle baseline (rank 0, single GPU only): the child's timed sample starts now ---
     cpu = None
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        params_cpu = {k: v.cpu() for k, v in params.items()}
-        run = oracle_run(w, alpha, params_cpu, prompt, ar_list)
-        tps, c, toks_c, el = oracle_sample(run, args.cpu_seconds, n + 2)
-        cpu = {"value": tps, "unit": "tokens/s", "cores": cpu_cores(), "kind": "oracle",
-               "sample": f"{c} SPD cycles of the fp32 numpy oracle after its (untimed) prefill: "
-                         f"{toks_c} tokens in {el:.1f} s"}
+    if child is not None:
+        try:
+            msg = conn.recv() if conn.poll(1800) else {"error": "oracle prefill did not finish in 30 min"}
+            if msg.get("ready"):
+                conn.send("go")
+                msg = conn.recv() if conn.poll(600) else {"error": "oracle sample did not finish"}
+            cpu = msg if "error" not in msg else {"value": None, "unit": "tokens/s", "kind": "oracle",
+                                                  "cores": cpu_cores(), "sample": msg["error"]}
+        finally:
+            child.join(timeout=30)
+            if child.is_alive():
+                child.terminate()
 
     if rank != 0:
         return 0
@@ -431,18 +566,15 @@ def main_spd(args):
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": m.dtype, "data": "synthetic",
-        "config": {"workload": w.name, "prompt": P, "gen": G, "alpha": alpha, "n_stages": n,
-                   "pdm_layers": w.pdm_layers, "anchors": list(w.anchors),
-                   "l2": "inputs larger than L2: every cycle streams all weights (>=3.4 GB)",
-                   "parallelism": f"replicas x{world}"},
+        "vs_baseline": None, "dtype": w.model.dtype, "data": "synthetic",
+        "config": bench_config(w, alpha, world),
         "roofline": {"bound": "hbm", "kernel": "step_kernel (one SPD cycle per launch)",
                      "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                      "peak_source": peak_src,
                      "traffic": None if traffic_ratio is None else traffic_ratio * step_bytes / cycles,
-                     "traffic_source": "ncu dram bytes / algorithmic bytes of one captured launch "
-                                       "(profiles/step_kernel_dense1.5b_n8_sections.md) x bytes_per_launch"
-                                       if traffic_ratio is not None else "no capture of the current sources",
+                     "traffic_source": f"ncu dram bytes / algorithmic bytes of one captured launch ({TRAFFIC_FILE})"
+                                       " x bytes_per_launch" if traffic_ratio is not None
+                                       else "no capture of the current sources for this workload",
                      "launches": args.steps * cycles, "bytes_per_launch": step_bytes / cycles},
         "cpu_baseline": cpu,
         "e2e": {"value": e2e_val, "unit": "tokens/s", "h2d_bytes_per_step": 4 * P + 5 * (G - 1),
@@ -452,17 +584,22 @@ def main_spd(args):
         "spd": {"lossless_vs_ar": lossless, "cycles_per_step": cycles, "rejects_per_step": st["rejects"],
                 "cycle_ms": t_cycle, "cycle_hbm_gbs": cycle_gbs, "cycle_hbm_frac": cycle_gbs / peak,
                 "cycle_hbm_frac_spec": cycle_gbs / SPEC_HBM_GBS, "alg_bytes_per_step": step_bytes,
-                "ar_tokens_per_s": ar_tps, "spd_over_ar": value / world / ar_tps,
-                "target_only_cycle_ms": t_tgt, "serial_pdm_cycle_ms": t_ser,
+                "ar_tokens_per_s": ar_tps, "ar_hbm_frac": ar_bytes * ar_tps / 1e9 / peak,
+                "spd_over_ar": value / world / ar_tps,
+                "spd_over_ar_byte_model": 1.0 / (alpha + (1 - alpha) * (n + 1) / 2),
+                "target_only_cycle_ms": t_tgt,
+                "target_only_hbm_frac": tgt_bytes / st_t["cycles"] / (t_tgt / 1e3) / 1e9 / peak,
+                "serial_pdm_cycle_ms": t_ser,
                 "post_step": {"cycle_ms": t_post, "tokens_per_s": post_tps,
                               "lossless_and_same_cycles": post_lossless},
                 "sampled_t1": smp_line,
                 "pdm_alone_ms_per_cycle": pdm_alone, "pdm_hidden_frac": hidden,
                 "control_us": 1e3 * kt["control"][1] / max(1, kt["control"][0]),
-                "phases_ms_per_cycle": kern},
+                "phases_ms_per_cycle": kern,
+                "other_alphas": other_alphas},
+        "other_workloads": extra,
     }
     print(json.dumps(line))
-    eng.close()
     return 0
 
 
@@ -479,7 +616,7 @@ def main_profile(args):
 
     build_ext.build()
     w = si.WORKLOADS[args.workload]
-    alpha = args.alpha if args.alpha is not None else w.alphas[0]
+    alpha = default_alpha(w, args)
     P, G = w.prompt_len, w.gen_len
     params = si.generate_weights(w, device="cuda")
     prompt = si.prompt_tokens(w).tolist()
@@ -489,8 +626,7 @@ def main_profile(args):
     first = eng.prefill(prompt)
     ar, _ = eng.generate_ar(G)  # G step-kernel launches, one per token: the reference stream
     eng.rollback(P, first)
-    modes = si.override_modes(w.coin_seed, alpha, P + 2, P + G)
-    eng.set_draft_override(P + 2, ar.tolist()[1:], modes)
+    eng.set_acceptance(alpha, w.coin_seed, ar)
     t0 = time.time()
     exits = 0
     st = eng.state()

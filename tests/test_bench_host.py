@@ -4,8 +4,8 @@
   algorithmic bytes of the roofline are summed over those states.  It is held to the oracle's own
   cycle-by-cycle state on a run with rejects.
 * ``Clocks`` parses nvidia-smi's sampled lines: median SM clock, max clock, active slowdown reasons.
-* ``step_kernel_traffic_ratio`` reports the ncu traffic ratio only while the CUDA sources hash to
-  the captured ones.
+* ``step_kernel_traffic_ratio`` reports the ncu traffic ratio only for the captured workload and
+  while the CUDA sources hash to the captured ones; both arms share one ``config`` helper.
 """
 import os
 import sys
@@ -74,6 +74,7 @@ def test_clock_parser_without_nvidia_smi():
 
 def test_traffic_ratio_only_for_the_captured_sources(tmp_path, monkeypatch):
     import hashlib
+    import json
     src = tmp_path / "speculative_pipeline_decoding_gb300" / "csrc"
     src.mkdir(parents=True)
     (src / "a.cu").write_text("kernel one")
@@ -84,14 +85,25 @@ def test_traffic_ratio_only_for_the_captured_sources(tmp_path, monkeypatch):
         h.update((src / f).read_bytes())
     prof = tmp_path / "profiles"
     prof.mkdir()
-    (prof / "step_kernel_dense1.5b_n8_sections.md").write_text(
-        "# summary\n\n    traffic_ratio: 0.9871 sources_sha1: " + h.hexdigest() + "\n")
+    (prof / "step_kernel_traffic.json").write_text(json.dumps(
+        {"workload": "gqa9b_bf16_n8", "sources_sha1": h.hexdigest(), "dram_bytes": 9.871e9,
+         "algorithmic_bytes": 1.0e10}))
     monkeypatch.setattr(bench, "ROOT", str(tmp_path))
-    assert bench.step_kernel_traffic_ratio() == pytest.approx(0.9871)
+    assert bench.step_kernel_traffic_ratio("gqa9b_bf16_n8") == pytest.approx(0.9871)
+    assert bench.step_kernel_traffic_ratio("dense1.5b_bf16_n8") is None  # another workload's capture
     (src / "notes.txt").write_text("still not hashed")
-    assert bench.step_kernel_traffic_ratio() == pytest.approx(0.9871)
+    assert bench.step_kernel_traffic_ratio("gqa9b_bf16_n8") == pytest.approx(0.9871)
     (src / "a.cu").write_text("kernel two")
-    assert bench.step_kernel_traffic_ratio() is None
+    assert bench.step_kernel_traffic_ratio("gqa9b_bf16_n8") is None
+
+
+def test_both_arms_report_the_same_config_keys():
+    import spd_inputs as si
+    w = si.WORKLOADS["gqa9b_bf16_n8"]
+    c = bench.bench_config(w, 0.9, 1)
+    assert c["workload"] == "gqa9b_bf16_n8" and c["alpha"] == 0.9 and c["prompt"] == 2048
+    assert set(c) >= {"workload", "prompt", "gen", "alpha", "n_stages", "pdm_layers", "anchors", "l2",
+                      "parallelism"}
 
 
 def test_measured_peaks_fallback(tmp_path, monkeypatch):
