@@ -217,6 +217,16 @@ int spd_acceptance_modes(double alpha, uint64_t seed, int32_t first_pos, int32_t
 int spd_set_sampling(spd_handle* h, float temperature, int32_t top_k, int32_t first_pos, int32_t count,
                      const float* uniforms);
 
+/* Self-check of the failure path (no GPU fault involved): runs one of the bounded device waits the
+ * kernels use -- which = 0: the grid-barrier counter wait of the step kernel, 1: an mbarrier phase
+ * wait (weight ring, tensor-core completion), 2: the shared-memory progress counter wait between the
+ * step kernel's warp roles -- on a condition that nothing satisfies, with a limit of limit_ns
+ * nanoseconds (1e3 .. 2e9; the kernels themselves use 2e9).  The wait gives up, the kernel sets the
+ * control block's error word and returns, and the host turns it into SPD_ETIMEOUT, which this call
+ * returns; the error word is cleared afterwards, so the handle stays usable.  Returns SPD_OK only if
+ * the wait did not give up (a defect).  SPD_EINVAL for a bad `which` or limit. */
+int spd_debug_wait_timeout(spd_handle* h, int32_t which, int64_t limit_ns);
+
 /* Execution options (bit flags), default SPD_OPT_GRAPHS | SPD_OPT_COSCHED | SPD_OPT_PDL |
  * SPD_OPT_STEP. */
 #define SPD_OPT_GRAPHS       1  /* replay captured CUDA graphs instead of eager launches      */
@@ -321,6 +331,22 @@ int spd_attention_static_scratch(const float* q, const void* k_cache, const void
                                  int32_t dtype, const int32_t* pos, int32_t R, int32_t n_heads,
                                  int32_t n_kv_heads, int32_t head_dim, int32_t max_seq, float* out,
                                  void* cuda_stream);
+
+/* Causal attention of a prefill block on the tensor cores (tcgen05): R (1..32) query rows at the
+ * consecutive positions pos0..pos0+R-1, whose keys and values are already in the cache, so row r
+ * sees keys 1..pos0+r: out[r][h][:] = softmax(q_r,h . K[kv(h)][0..pos0+r-1]^T / sqrt(hd)) V.
+ * q: fp32 [R][n_heads][hd] (rotated); k_cache, v_cache: bf16 [n_kv_heads][max_seq][hd]; out: fp32
+ * [R][n_heads][hd]; hd 64 or 128; every pointer 16-byte aligned.  The query, and the probabilities,
+ * enter the bf16 MMAs as high + low halves (fp32 accumulation in TMEM), so the result keeps about
+ * 16 significant bits of the fp32 operands.  Long contexts are split over CTAs by 128-key chunks and
+ * merged in split order.  `workspace` (device, >= spd_prefill_attention_workspace_bytes bytes) holds
+ * the split partials and tickets; zero it before its first use, each call leaves the tickets zeroed.
+ * This is the kernel the prefill uses for bf16 models with those head sizes.  SPD_EINVAL on bad sizes. */
+size_t spd_prefill_attention_workspace_bytes(int32_t n_heads, int32_t n_kv_heads, int32_t head_dim,
+                                             int32_t max_seq);
+int spd_prefill_attention(const float* q, const void* k_cache, const void* v_cache, int32_t pos0, int32_t R,
+                          int32_t n_heads, int32_t n_kv_heads, int32_t head_dim, int32_t max_seq, float* out,
+                          void* workspace, size_t ws_bytes, void* cuda_stream);
 
 /* Grouped GEMV with RMSNorm prologue: for group g (0..G-1), y_g = W_g . (x_g / rms(x_g) * nw)
  * (norm skipped when nw == NULL), W_g [rows, cols] row-major in `dtype`, x_g fp32 [cols],

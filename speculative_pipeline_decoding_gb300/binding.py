@@ -110,6 +110,7 @@ def lib() -> ctypes.CDLL:
         "spd_set_acceptance": (ctypes.c_int, [vp, ctypes.c_double, ctypes.c_uint64, _I32P, i32]),
         "spd_acceptance_modes": (ctypes.c_int, [ctypes.c_double, ctypes.c_uint64, i32, i32,
                                                 ctypes.POINTER(ctypes.c_uint8)]),
+        "spd_debug_wait_timeout": (ctypes.c_int, [vp, i32, ctypes.c_int64]),
         "spd_set_options": (ctypes.c_int, [vp, i32]),
         "spd_set_sampling": (ctypes.c_int, [vp, ctypes.c_float, i32, i32, i32, ctypes.POINTER(ctypes.c_float)]),
         "spd_dump_size": (sz, [vp, i32]),
@@ -124,6 +125,8 @@ def lib() -> ctypes.CDLL:
                                             i32, i32, i32, i32, vp, ctypes.c_float, vp]),
         "spd_attention_static_scratch": (ctypes.c_int, [vp, vp, vp, i32, vp, i32, i32, i32, i32, i32,
                                                         vp, vp]),
+        "spd_prefill_attention_workspace_bytes": (sz, [i32, i32, i32, i32]),
+        "spd_prefill_attention": (ctypes.c_int, [vp, vp, vp, i32, i32, i32, i32, i32, i32, vp, vp, sz, vp]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(L, name)
@@ -239,6 +242,7 @@ class Engine:
         _check(rc, None)
         self.h = h
         self.P = 0
+        self.opts = OPT_DEFAULT
 
     # -- lifecycle ------------------------------------------------------------
     def close(self) -> None:
@@ -317,8 +321,14 @@ class Engine:
         _check(lib().spd_set_acceptance(self.h, float(alpha), int(seed) & ((1 << 64) - 1),
                                         ref.ctypes.data_as(_I32P), int(ref.size)), self.h)
 
+    def debug_wait_timeout(self, which: int, limit_ns: int) -> int:
+        """Run one bounded device wait on a condition nothing satisfies; returns the status code
+        (SPD_ETIMEOUT = -5 when the wait gave up, as it must) without raising."""
+        return int(lib().spd_debug_wait_timeout(self.h, int(which), int(limit_ns)))
+
     def set_options(self, flags: int) -> None:
         _check(lib().spd_set_options(self.h, int(flags)), self.h)
+        self.opts = int(flags)
 
     def set_sampling(self, temperature: float, top_k: int = 50, first_pos: int = 1, uniforms=None) -> None:
         """Sampled decoding (temperature > 0) or greedy (<= 0).  ``uniforms``: [4][count] floats in
@@ -421,3 +431,18 @@ def attention_static_scratch(q: torch.Tensor, k_cache: torch.Tensor, v_cache: to
     dt = DTYPE_BF16 if k_cache.dtype == torch.bfloat16 else DTYPE_F32
     _check(lib().spd_attention_static_scratch(_ptr(q), _ptr(k_cache), _ptr(v_cache), dt, _ptr(pos), R,
                                               hq, hkv, hd, max_seq, _ptr(out), _stream_handle(stream)))
+
+
+def prefill_attention_workspace_bytes(n_heads: int, n_kv_heads: int, head_dim: int, max_seq: int) -> int:
+    return int(lib().spd_prefill_attention_workspace_bytes(n_heads, n_kv_heads, head_dim, max_seq))
+
+
+def prefill_attention(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, pos0: int,
+                      out: torch.Tensor, workspace: torch.Tensor, stream=None) -> None:
+    """Causal attention of R = q.shape[0] rows at positions pos0..pos0+R-1 on the tensor cores.
+    Shapes: q, out [R, Hq, hd] fp32; caches [Hkv, max_seq, hd] bf16."""
+    R, hq, hd = q.shape
+    hkv, max_seq, _ = k_cache.shape
+    _check(lib().spd_prefill_attention(_ptr(q), _ptr(k_cache), _ptr(v_cache), int(pos0), R, hq, hkv, hd, max_seq,
+                                       _ptr(out), _ptr(workspace), workspace.numel() * workspace.element_size(),
+                                       _stream_handle(stream)))

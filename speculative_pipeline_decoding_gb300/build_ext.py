@@ -17,7 +17,7 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(os.path.dirname(HERE), "include")
 LIBDIR = os.path.join(HERE, "_lib")
 LIBPATH = os.path.join(LIBDIR, "libspd.so")
-SOURCES = ["spd_api.cu", "spd_gemv.cu", "spd_attn.cu", "spd_ctrl.cu", "spd_step.cu"]
+SOURCES = ["spd_api.cu", "spd_gemv.cu", "spd_attn.cu", "spd_ctrl.cu", "spd_step.cu", "spd_pfattn.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-cudart", "shared",
          "--expt-relaxed-constexpr"]

@@ -70,6 +70,11 @@ struct spd_handle {
   int64_t launches[SPD_NUM_KINDS] = {0};
   double ms[SPD_NUM_KINDS] = {0};
   DevState* host_state = nullptr;  // pinned mirror
+  // prefill blocks' causal attention on the tensor cores (bf16, head size 64 or 128)
+  bool pf_on = false;
+  CUtensorMap pf_map[4];          // K, V of the target cache; K, V of the draft-module cache
+  float* pf_part = nullptr;       // split partials
+  int* pf_tick = nullptr;         // merge tickets (left at zero)
 };
 
 namespace {
@@ -164,12 +169,32 @@ int run_attn(spd_handle* h, const Launch& lc, cudaStream_t s) {
   return SPD_OK;
 }
 
+// Causal attention of a prefill block (rows pos0..pos0+cnt-1 of layer `sub` of `stack`) on the
+// tensor-core kernel.
+int run_pfattn(spd_handle* h, const Launch& lc, cudaStream_t s) {
+  Timed tm(h, KK_ATTN + (lc.stack == 1 ? kDraftKinds : 0), s);
+  const Dims& D = h->D;
+  PfAttnArgs a;
+  memset(&a, 0, sizeof(a));
+  a.kmap = &h->pf_map[lc.stack == 1 ? 2 : 0];
+  a.vmap = &h->pf_map[lc.stack == 1 ? 3 : 1];
+  a.q = lc.act.qkv; a.q_stride = D.qkv_rows;
+  a.out = lc.act.attn;
+  a.part = h->pf_part; a.tick = h->pf_tick; a.st = h->B.st;
+  a.kv_row0 = lc.sub * D.hkv * D.max_seq;
+  a.max_seq = D.max_seq; a.hq = D.hq; a.hkv = D.hkv; a.hd = D.hd;
+  a.pos0 = lc.pos0; a.nq = lc.cnt; a.sms = h->LC.sms;
+  SPD_CUDA(h, launch_pfattn(a, s));
+  h->st_dirty = false;
+  return SPD_OK;
+}
+
 // One decoder layer (or the layer-s slice of a co-scheduled step) for the rows of `lc` and, when
 // given, `extra` (5 launches; the draft rows need their own attention launch).
 int enqueue_layer(spd_handle* h, const Launch& lc, const Launch* extra, cudaStream_t s) {
   int rc;
   if ((rc = run_gemv(h, OP_QKV, lc, extra, s))) return rc;
-  if ((rc = run_attn(h, lc, s))) return rc;
+  if ((rc = (lc.kind == LK_ROWS && h->pf_on) ? run_pfattn(h, lc, s) : run_attn(h, lc, s))) return rc;
   if (extra && (rc = run_attn(h, *extra, s))) return rc;
   if ((rc = run_gemv(h, OP_O, lc, extra, s))) return rc;
   if ((rc = run_gemv(h, OP_GATEUP, lc, extra, s))) return rc;
@@ -511,6 +536,7 @@ int spd_create(const spd_config* cfg, const spd_weights* w, void* cuda_stream, s
   D.max_seq = c.max_seq; D.dtype = c.dtype; D.qkv_rows = (c.n_heads + 2 * c.n_kv_heads) * c.head_dim;
   D.gq = gq; D.eps = c.norm_eps;
   D.box3 = box3_cols(c.d_model, c.dtype) && box3_cols(c.d_ffn, c.dtype);  // every streamed matrix's cols
+  D.tc = D.box3 && c.dtype == SPD_DTYPE_BF16 && c.head_dim <= 128;       // tcgen05 draft tiles
   for (int i = 0; i < c.n_anchors; ++i) D.anchors[i] = c.anchors[i];
   // f(k) = max{i : b_i <= lmax(k)}, lmax(k) = min(L, k*L/n)   (SPD summary, 核心方法)
   for (int k = 0; k <= c.n_stages; ++k) {
@@ -567,7 +593,8 @@ int spd_create(const spd_config* cfg, const spd_weights* w, void* cuda_stream, s
   } while (0)
   // tensor maps of every weight matrix the GEMV engine streams (7 per layer, FCs, two heads)
   {
-    const int nmaps = 7 * (c.n_layers + c.pdm_layers) + c.n_anchors + 2;
+    const int per = D.tc ? 2 : 1;  // with tcgen05 tiles every stream map is followed by its 128-row map
+    const int nmaps = per * (7 * (c.n_layers + c.pdm_layers) + c.n_anchors + 2);
     CUtensorMap* dmaps;
     ALLOC(dmaps, CUtensorMap, nmaps);
     std::vector<CUtensorMap> hm(nmaps);
@@ -575,7 +602,10 @@ int spd_create(const spd_config* cfg, const spd_weights* w, void* cuda_stream, s
     const int qr = c.n_heads * c.head_dim, kr = c.n_kv_heads * c.head_dim;
     auto enc = [&](const void* W, int rows, int cols) -> const CUtensorMap* {
       if (e == cudaSuccess) e = gemv_encode_map(&hm[k], W, rows, cols, c.dtype, D.box3 != 0);
-      return dmaps + k++;
+      if (per == 2 && e == cudaSuccess) e = gemv_encode_tc_map(&hm[k + 1], W, rows, cols);
+      const CUtensorMap* m = dmaps + k;
+      k += per;
+      return m;
     };
     auto layer_maps = [&](LayerW& o) {
       o.tq = enc(o.wq, qr, c.d_model); o.tk = enc(o.wk, kr, c.d_model); o.tv = enc(o.wv, kr, c.d_model);
@@ -671,6 +701,20 @@ int spd_create(const spd_config* cfg, const spd_weights* w, void* cuda_stream, s
   FP = F;
   ALLOC(FP.resid, float, (size_t)PB * d);
   FP.anch = F.anch;  // anchor source of the prefix rows for the draft FC
+  // prefill attention on the tensor cores: maps over the whole caches (row = layer, kv head, position)
+  if (pfattn_supported(c.dtype, hd, PB, gq)) {
+    const int sms = num_sms();
+    ALLOC(h->pf_part, float, pfattn_part_floats(c.n_kv_heads, gq, ms, sms));
+    ALLOC(h->pf_tick, int, (size_t)c.n_heads);
+    const long long rt = (long long)c.n_layers * c.n_kv_heads * ms, rp = (long long)c.pdm_layers * c.n_kv_heads * ms;
+    e = pfattn_encode_map(&h->pf_map[0], kc, rt, hd);
+    if (e == cudaSuccess) e = pfattn_encode_map(&h->pf_map[1], vc, rt, hd);
+    if (e == cudaSuccess) e = pfattn_encode_map(&h->pf_map[2], pkc, rp, hd);
+    if (e == cudaSuccess) e = pfattn_encode_map(&h->pf_map[3], pvc, rp, hd);
+    if (e == cudaSuccess) e = pfattn_setup_attributes();
+    if (e != cudaSuccess) { spd_destroy(h); return fail(nullptr, SPD_ECUDA, "prefill attention set-up: %s", cudaGetErrorString(e)); }
+    h->pf_on = true;
+  }
   e = cudaMallocHost(reinterpret_cast<void**>(&h->host_state), sizeof(DevState));
   if (e != cudaSuccess) { spd_destroy(h); return fail(nullptr, SPD_ENOMEM, "cudaMallocHost failed"); }
   memset(h->host_state, 0, sizeof(DevState));
@@ -870,6 +914,25 @@ int spd_set_acceptance(spd_handle* h, double alpha, uint64_t seed, const int32_t
   int rc;
   if ((rc = spd_acceptance_modes(alpha, seed, P + 2, count, modes.data()))) return fail(h, rc, "%s", g_create_error.c_str());
   return spd_set_draft_override(h, P + 2, count, ref_tokens + 1, modes.data());
+}
+
+int spd_debug_wait_timeout(spd_handle* h, int32_t which, int64_t limit_ns) {
+  if (!h) return SPD_EINVAL;
+  if (which < 0 || which > 2 || limit_ns < 1000 || limit_ns > (int64_t)kWaitLimitNs)
+    return fail(h, SPD_EINVAL, "which must be 0..2 and limit_ns in [1e3, %llu]", (unsigned long long)kWaitLimitNs);
+  cudaStream_t s = h->s_main;
+  SPD_CUDA(h, cudaMemsetAsync(&h->B.st->err, 0, sizeof(int), s));
+  SPD_CUDA(h, cudaMemsetAsync(&h->B.st->err_where, 0, sizeof(int), s));
+  // a word of the control block that no kernel writes stands for a grid-barrier count nobody adds to
+  SPD_CUDA(h, launch_wait_selftest(h->B.st, reinterpret_cast<unsigned*>(&h->B.st->pad0), which,
+                                   (uint64_t)limit_ns, s));
+  int rc;
+  if ((rc = read_state(h))) return rc;
+  const int verdict = state_error(h);  // SPD_ETIMEOUT when the wait gave up, as it must
+  SPD_CUDA(h, cudaMemsetAsync(&h->B.st->err, 0, sizeof(int), s));
+  SPD_CUDA(h, cudaMemsetAsync(&h->B.st->err_where, 0, sizeof(int), s));
+  SPD_CUDA(h, cudaStreamSynchronize(s));
+  return verdict;
 }
 
 int spd_set_sampling(spd_handle* h, float temperature, int32_t top_k, int32_t first_pos, int32_t count,
@@ -1079,6 +1142,46 @@ int spd_attention(const float* q, const void* k_cache, const void* v_cache, int3
   if (e != cudaSuccess)
     return fail(nullptr, SPD_ECUDA, "attention launch (grid %d): %s", LC.attn_grid_decode,
                 cudaGetErrorString(e));
+  return SPD_OK;
+}
+
+size_t spd_prefill_attention_workspace_bytes(int32_t n_heads, int32_t n_kv_heads, int32_t head_dim,
+                                             int32_t max_seq) {
+  if (n_heads < 1 || n_kv_heads < 1 || n_heads % n_kv_heads || max_seq < 1 || (head_dim != 64 && head_dim != 128))
+    return 0;
+  return 256 + (size_t)n_heads * sizeof(int) +
+         pfattn_part_floats(n_kv_heads, n_heads / n_kv_heads, max_seq, num_sms()) * sizeof(float);
+}
+
+int spd_prefill_attention(const float* q, const void* k_cache, const void* v_cache, int32_t pos0, int32_t R,
+                          int32_t n_heads, int32_t n_kv_heads, int32_t head_dim, int32_t max_seq, float* out,
+                          void* workspace, size_t ws_bytes, void* stream) {
+  if (!q || !k_cache || !v_cache || !out || !workspace || n_kv_heads < 1 || n_heads < 1 || n_heads % n_kv_heads ||
+      !pfattn_supported(SPD_DTYPE_BF16, head_dim, R, n_heads / n_kv_heads) || pos0 < 1 ||
+      (long long)pos0 + R - 1 > max_seq)
+    return fail(nullptr, SPD_EINVAL, "spd_prefill_attention: bad arguments");
+  if (!aligned16(q) || !aligned16(out) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(workspace))
+    return fail(nullptr, SPD_EINVAL, "spd_prefill_attention: pointers must be 16-byte aligned");
+  if (ws_bytes < spd_prefill_attention_workspace_bytes(n_heads, n_kv_heads, head_dim, max_seq))
+    return fail(nullptr, SPD_EINVAL, "spd_prefill_attention: workspace too small");
+  cudaGetLastError();
+  CUtensorMap km, vm;
+  const long long rows = (long long)n_kv_heads * max_seq;
+  cudaError_t e = pfattn_encode_map(&km, k_cache, rows, head_dim);
+  if (e == cudaSuccess) e = pfattn_encode_map(&vm, v_cache, rows, head_dim);
+  if (e == cudaSuccess) e = pfattn_setup_attributes();
+  if (e != cudaSuccess) return fail(nullptr, SPD_ECUDA, "spd_prefill_attention: set-up: %s", cudaGetErrorString(e));
+  PfAttnArgs a;
+  memset(&a, 0, sizeof(a));
+  a.kmap = &km; a.vmap = &vm;
+  a.q = q; a.q_stride = n_heads * head_dim; a.out = out;
+  a.tick = reinterpret_cast<int*>(workspace);
+  a.part = reinterpret_cast<float*>(reinterpret_cast<unsigned char*>(workspace) + 256 + (size_t)n_heads * sizeof(int));
+  a.part = reinterpret_cast<float*>((reinterpret_cast<uintptr_t>(a.part) + 15) & ~(uintptr_t)15);
+  a.st = nullptr; a.kv_row0 = 0; a.max_seq = max_seq;
+  a.hq = n_heads; a.hkv = n_kv_heads; a.hd = head_dim; a.pos0 = pos0; a.nq = R; a.sms = num_sms();
+  e = launch_pfattn(a, reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return fail(nullptr, SPD_ECUDA, "spd_prefill_attention: launch: %s", cudaGetErrorString(e));
   return SPD_OK;
 }
 

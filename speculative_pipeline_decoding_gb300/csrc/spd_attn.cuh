@@ -466,8 +466,12 @@ __device__ void warp_item(const Dims& D, const Tile& T, const Item& it, const WT
   }
 }
 
-// Merge of (tile T, kv head kh) on the calling warp, after its last ticket: each query head over
-// its own chunks, in chunk order; resets the ticket.
+// Merge of (tile T, kv head kh) on the calling warp, after its last ticket; resets the ticket.
+// For each query head over its own nc chunks: lane j takes chunks j, j+32, ... (in that order),
+// weighting each partial by exp(m - M); the 32 lanes' sums are then added by a fixed butterfly that
+// leaves dim d of a 32-dim slice on lane d.  The arithmetic depends only on nc (the query's
+// position), so a token's result does not depend on its batch; every lane's loads are independent,
+// so a merge costs a few memory round trips, not one per chunk.
 template <int DPL>
 __device__ void warp_merge(const Dims& D, const Tile& T, int kh) {
   constexpr int CK = kWarpCK;
@@ -484,21 +488,44 @@ __device__ void warp_merge(const Dims& D, const Tile& T, int kh) {
     for (int cc = lane; cc < nc; cc += 32) M = fmaxf(M, __ldcg(base + cc * cstride + hd));
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-    // the sums run over the chunks in order; four chunks' loads are issued together
-    float Ls = 0.f, O[DPL];
-#pragma unroll
-    for (int e = 0; e < DPL; ++e) O[e] = 0.f;
-#pragma unroll 4
-    for (int cc = 0; cc < nc; ++cc) {
+    float Ls = 0.f;
+    for (int cc = lane; cc < nc; cc += 32) {
       const float* rc = base + cc * cstride;
-      const float w = expf(__ldcg(rc + hd) - M);
-      Ls = fmaf(__ldcg(rc + hd + 1), w, Ls);
-#pragma unroll
-      for (int e = 0; e < DPL; ++e) O[e] = fmaf(__ldcg(rc + lane * DPL + e), w, O[e]);
+      Ls = fmaf(__ldcg(rc + hd + 1), expf(__ldcg(rc + hd) - M), Ls);
     }
-    float* out = T.out + (size_t)(T.vid0 + r) * hqd + (kh * GQ + hg) * hd + lane * DPL;
 #pragma unroll
-    for (int e = 0; e < DPL; ++e) out[e] = O[e] / Ls;
+    for (int o = 16; o > 0; o >>= 1) Ls += __shfl_xor_sync(0xffffffffu, Ls, o);
+    float* out = T.out + (size_t)(T.vid0 + r) * hqd + (kh * GQ + hg) * hd;
+    for (int d0 = 0; d0 < hd; d0 += 32) {  // one 32-dim slice of the output
+      float acc[32];
+#pragma unroll
+      for (int e = 0; e < 32; ++e) acc[e] = 0.f;
+      for (int cc = lane; cc < nc; cc += 32) {
+        const float* rc = base + cc * cstride;
+        const float w = expf(__ldcg(rc + hd) - M);
+#pragma unroll
+        for (int e = 0; e < 32; e += 4) {
+          const float4 v = __ldcg(reinterpret_cast<const float4*>(rc + d0 + e));
+          acc[e] = fmaf(v.x, w, acc[e]);
+          acc[e + 1] = fmaf(v.y, w, acc[e + 1]);
+          acc[e + 2] = fmaf(v.z, w, acc[e + 2]);
+          acc[e + 3] = fmaf(v.w, w, acc[e + 3]);
+        }
+      }
+      // reduce-scatter: after the step of width h, lane l keeps the h dims of its half
+#pragma unroll
+      for (int h = 16; h > 0; h >>= 1) {
+        const bool upper = (lane & h) != 0;
+#pragma unroll
+        for (int e = 0; e < h; ++e) {
+          const float send = upper ? acc[e] : acc[e + h];
+          const float keep = upper ? acc[e + h] : acc[e];
+          acc[e] = keep + __shfl_xor_sync(0xffffffffu, send, h);
+        }
+      }
+      // lane l now holds dim d0 + bitreverse-free index: the kept half follows the lane bits
+      out[d0 + lane] = acc[0] / Ls;
+    }
   }
   __syncwarp();
   if (lane == 0) T.tick[T.tick_off + kh] = 0;

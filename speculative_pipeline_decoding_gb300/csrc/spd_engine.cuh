@@ -43,6 +43,7 @@
 //   TOP2    logits of the vocab head; per-CTA top-2 (+ optional full logits for debugging)
 #pragma once
 #include "spd_internal.cuh"
+#include "spd_tc.cuh"
 
 namespace spd {
 namespace eng {
@@ -71,6 +72,8 @@ struct GG {
   int rows, cols;              // output rows (gate/up: rows of each weight), input columns
   short nv, nw, epi, kind;     // vectors, weights per output row, epilogue, head kind
   short mma, tr;               // tensor-core path; tile height in output rows (64 / nw)
+  short tc;                    // tcgen05 path (mma groups of <= 16 vectors, bf16, 3-D maps): 128-row
+                               // tiles, stages of 128 rows x 2 chunks from the map at m[s] + 1
   const float* x; int xrow0, xring, xstride;
   float* y; int yrow0, yring, ystride;
   const float* normw;
@@ -85,14 +88,16 @@ struct GG {
 struct EngineCfg {
   int debug_logits;
   int has_mma;                 // bf16 weights (tensor-core path available)
+  int has_tc;                  // tcgen05 tiles available (maps in pairs, TMEM allocated, B ring)
   float eps;
   Dims D;
   Bufs B;
 };
 
 // split cost of one output row: its weight elements, weighted by the path's cost per byte
+constexpr int kCostTc = 2;  // a tcgen05 stage streams at the single-vector rate (to be measured)
 __device__ __forceinline__ long long rowcost(const GG& g) {
-  return (long long)g.cols * g.nw * (g.mma ? kCostMma : kCostSV);
+  return (long long)g.cols * g.nw * (g.tc ? kCostTc : (g.mma ? kCostMma : kCostSV));
 }
 
 __device__ __forceinline__ int anchor_index(const Dims& D, int layer_done) {
@@ -260,7 +265,10 @@ static __device__ int finish_groups(const EngineCfg& p, GG* gg, int ng, int cap)
     GG& o = gg[g];
     if (o.nv > 16 * kMaxMT) { set_err(p.B.st, ERR_BOUNDS, 91); return 0; }
     o.mma = o.nv > 1;
-    o.tr = (short)(kSlots / o.nw);
+    // tcgen05 tiles: <= 16 vectors (16 high + 16 low B rows), whole 128-column stages, heads of at
+    // most 128 rows (a 128-row tile holds whole heads, so RoPE pairs stay inside it)
+    o.tc = (short)(p.has_tc && o.mma && o.nv <= 16 && o.cols % 128 == 0 && p.D.hd <= 128);
+    o.tr = (short)(o.tc ? tc::kRows : kSlots / o.nw);
     o.cost0 = cost;
     cost += (long long)o.rows * rowcost(o);
   }
@@ -459,6 +467,7 @@ __device__ __forceinline__ void span_of(const GG* gg, int ng, int cta, int ncta,
 __device__ __forceinline__ int tile_rows(const GG& G, int r, int last) {
   int tr = min((int)G.tr, last - r);
   if (G.epi == EPI_QKV && r < G.seg2) tr = min(tr, G.seg2 - r);
+  if (G.tc && G.epi == EPI_QKV && r < G.seg1) tr = min(tr, G.seg1 - r);  // one tensor map per tile
   return tr;
 }
 
@@ -532,6 +541,24 @@ __device__ __forceinline__ void issue_stage(const TileSrc& S, int c0, Ring& R, D
   ++R.ctr;
 }
 
+// Producer warp: one stage of a tcgen05 tile -- 128 rows x 2 chunks (32 KB) in one 3-D copy from
+// the 128-row map `mp`, landing [chunk][row][128 B].
+__device__ __forceinline__ void issue_tc_stage(const CUtensorMap* mp, int y, int z, Ring& R, DevState* st,
+                                               uint64_t pol, int lane) {
+  const int s = R.ctr % kStages;
+  if (R.ctr >= (uint32_t)kStages && !mbar_wait_bounded(&R.empty[s], ((R.ctr / kStages) - 1) & 1)) {
+    if (lane == 0) set_err(st, ERR_TIMEOUT, 45);
+    R.failed = true;
+    return;
+  }
+  if (lane == 0) {
+    mbar_arrive_expect_tx(&R.full[s], (uint32_t)kStageBytes);
+    tma_box3(R.base + (size_t)s * kStageBytes, mp, y, z, &R.full[s], pol);
+  }
+  __syncwarp();
+  ++R.ctr;
+}
+
 // Producer warp (all 32 lanes): issue the tensor copies of every stage of the span, tile by tile,
 // column chunk by column chunk.
 template <typename WT>
@@ -542,6 +569,16 @@ __device__ void produce_span(const GG* gg, int gb, int rb, int ge, int re, int h
     const GG& G = gg[g];
     const int last = (g == ge) ? re : G.rows;
     const int tr = tile_rows(G, r, last);
+    if (G.tc) {  // tcgen05 tile: 128 physical rows, 2 chunks a stage; gate/up alternate the matrices
+      const int sg = r < G.seg1 ? 0 : (r < G.seg2 ? 1 : 2);
+      const int y = r - (sg == 0 ? 0 : (sg == 1 ? G.seg1 : G.seg2));
+      for (int c0 = 0; c0 < G.cols && !R.failed; c0 += tc::kStageCh * tc::kChunk)
+        for (int h = 0; h < G.nw && !R.failed; ++h)
+          issue_tc_stage(G.nw == 2 ? G.m[h] + 1 : G.m[sg] + 1, G.nw == 2 ? r : y, c0 / tc::kChunk, R, st, pol, lane);
+      r += tr;
+      if (r >= last) { ++g; r = 0; }
+      continue;
+    }
     const TileSrc S = tile_src(G, r, tr, hd, box3);
     const int cols = G.cols, step = S.wide ? 2 * CW : CW;
     for (int c0 = 0; c0 < cols && !R.failed; c0 += step) issue_stage<WT>(S, c0, R, st, pol, lane);
@@ -734,6 +771,131 @@ __device__ void mma_tile(const EngineCfg& p, const GG& G, int r, int tr, Ring& R
   named_bar(1, NCT);  // `red` is rewritten by the next tile
 }
 
+// State of the tcgen05 path of one CTA: the B operand ring (one 8 KB slot per ring stage), the TMEM
+// accumulator (64 columns: gate in 0..31, up in 32..63), the tile-completion mbarrier and its phase.
+struct TcCtx {
+  unsigned char* bring;   // kStages x tc::kBBytes, 1024-byte aligned
+  uint32_t tmem;          // TMEM address of column 0
+  uint64_t* done;         // arrives when every MMA of the tile has completed
+  uint32_t phase;
+};
+
+// tcgen05 tile: output rows r..r+tr-1 (physical rows; whole heads in the rotary region) of a group of
+// nv <= 16 vectors.  Per stage the consumers build B (high and low halves of the normalised
+// activations of the stage's 128 columns) once the stage's weights have landed -- which also means
+// the MMAs that last read that B slot are done -- then one thread issues the 8 MMAs and commits them
+// to the stage's empty barrier in place of warp 0's arrival, so the producer refills the slot only
+// after the tensor core has read it.  At the tile end warps 0-3 read their 32 TMEM lanes (rows) and
+// run the epilogue of every vector; RoPE partners (row + hd/2) are exchanged through `scratch`.
+template <typename WT>
+__device__ void tc_tile(const EngineCfg& p, const GG& G, int r, int tr, Ring& R, TcCtx& T, unsigned char* scratch,
+                        const float* rstd_s, Top2* loc) {
+  constexpr int NCT = kNCW * 32;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int hd = p.D.hd, nv = G.nv;
+  DevState* st = p.B.st;
+  const int nst = (G.cols / (tc::kStageCh * tc::kChunk)) * G.nw;
+  // B of a stage: thread t builds the 8 columns 8*(t%16).. of vector t/16, both halves (row v: high,
+  // row 16+v: low); the vector's row and its 1/rms are resolved once per tile
+  const int bv = tid >> 4, bpc = tid & 15;
+  const float* bx = bv < nv ? G.x + (size_t)((G.xrow0 + bv) % G.xring) * G.xstride : nullptr;
+  const float brs = (bv < nv && G.normw) ? rstd_s[bv] : 1.f;
+  const uint32_t boff_hi = (uint32_t)((bpc >> 3) * tc::kB * 128 + bv * 128 + (((bpc & 7) ^ (bv & 7)) << 4));
+  const uint32_t boff_lo = (uint32_t)((bpc >> 3) * tc::kB * 128 + (16 + bv) * 128 + (((bpc & 7) ^ ((16 + bv) & 7)) << 4));
+  auto build_b = [&](unsigned char* b, int c0) {
+    uint4 hi = make_uint4(0u, 0u, 0u, 0u), lo = hi;
+    if (bx) {
+      const int col = c0 + 8 * bpc;
+      float4 x0 = *reinterpret_cast<const float4*>(bx + col), x1 = *reinterpret_cast<const float4*>(bx + col + 4);
+      if (G.normw) {
+        const float4 n0 = *reinterpret_cast<const float4*>(G.normw + col);
+        const float4 n1 = *reinterpret_cast<const float4*>(G.normw + col + 4);
+        x0.x = x0.x * brs * n0.x; x0.y = x0.y * brs * n0.y; x0.z = x0.z * brs * n0.z; x0.w = x0.w * brs * n0.w;
+        x1.x = x1.x * brs * n1.x; x1.y = x1.y * brs * n1.y; x1.z = x1.z * brs * n1.z; x1.w = x1.w * brs * n1.w;
+      }
+      const float xv[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+      uint32_t h4[4], l4[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const __nv_bfloat16 a = __float2bfloat16_rn(xv[2 * e]), c = __float2bfloat16_rn(xv[2 * e + 1]);
+        const float fa = __bfloat162float(a), fc = __bfloat162float(c);
+        h4[e] = pack_bf16x2(fa, fc);
+        l4[e] = pack_bf16x2(xv[2 * e] - fa, xv[2 * e + 1] - fc);
+      }
+      hi = make_uint4(h4[0], h4[1], h4[2], h4[3]);
+      lo = make_uint4(l4[0], l4[1], l4[2], l4[3]);
+    }
+    *reinterpret_cast<uint4*>(b + boff_hi) = hi;
+    *reinterpret_cast<uint4*>(b + boff_lo) = lo;
+  };
+  for (int k = 0; k < nst; ++k) {
+    const int s = R.ctr % kStages;
+    if (!R.failed && !mbar_wait_bounded(&R.full[s], (R.ctr / kStages) & 1)) {
+      if (lane == 0) set_err(st, ERR_TIMEOUT, 61);
+      R.failed = true;
+    }
+    unsigned char* bs = T.bring + (size_t)s * tc::kBBytes;
+    const int c0 = (k / G.nw) * tc::kStageCh * tc::kChunk;
+    if (!R.failed) build_b(bs, c0);
+    tc::fence_async_smem();
+    named_bar(1, NCT);
+    if (tid == 0) {
+      if (!R.failed) {
+        tc::fence_after();
+        const int h = G.nw == 2 ? (k & 1) : 0;  // gate / up accumulator
+        tc::mma_stage(T.tmem + (uint32_t)(32 * h), R.base + (size_t)s * kStageBytes, bs, k < G.nw);
+        tc::commit(&R.empty[s]);              // warp 0's arrival, when the MMAs have read the stage
+      } else {
+        mbar_arrive(&R.empty[s]);
+      }
+    } else if (warp != 0 && lane == 0) {
+      mbar_arrive(&R.empty[s]);
+    }
+    ++R.ctr;
+  }
+  // tile end: every MMA done -> TMEM rows to registers -> epilogues.  The completion is committed
+  // whatever happened (it arrives once the MMAs issued so far are done, at once if there are none),
+  // so the barrier's phase stays in step with T.phase on the failure path too.
+  if (tid == 0) tc::commit(T.done);
+  bool ok = mbar_wait_bounded(T.done, T.phase);
+  T.phase ^= 1u;
+  if (!ok) { if (lane == 0) set_err(st, ERR_TIMEOUT, 62); R.failed = true; }
+  ok = ok && !R.failed;
+  tc::fence_after();
+  float* xch = reinterpret_cast<float*>(scratch);  // [128 rows][16 vectors]: RoPE partner values
+  const bool pairs = G.epi == EPI_QKV && r < G.seg2;
+  uint32_t d[32], u[32];
+  const bool wok = __all_sync(0xffffffffu, ok);  // tcgen05.ld is warp-collective
+  if (warp < 4 && wok) {
+    tc::load_rows(T.tmem, warp, d);
+    if (G.nw == 2) tc::load_rows(T.tmem + 32, warp, u);
+    if (pairs) {
+      const int row = 32 * warp + lane;
+#pragma unroll
+      for (int v = 0; v < 16; ++v) xch[row * 16 + v] = __uint_as_float(d[v]) + __uint_as_float(d[16 + v]);
+    }
+  }
+  named_bar(1, NCT);
+  if (wok && warp < 4) {
+    const int row = 32 * warp + lane;  // tile-local physical row
+    if (row < tr) {
+      for (int v = 0; v < nv; ++v) {
+        const float y0 = __uint_as_float(d[v]) + __uint_as_float(d[16 + v]);
+        if (G.nw == 2) {
+          epilogue<WT>(p, G, v, r + row, y0, __uint_as_float(u[v]) + __uint_as_float(u[16 + v]), false, loc);
+        } else if (pairs) {
+          const int i = (r + row) % hd;      // tiles start on a head boundary
+          if (i < hd / 2) epilogue<WT>(p, G, v, r + row, y0, xch[(row + hd / 2) * 16 + v], true, loc);
+        } else {
+          epilogue<WT>(p, G, v, r + row, y0, 0.f, false, loc);
+        }
+      }
+    }
+  }
+  tc::fence_before();
+  named_bar(1, NCT);  // TMEM and `scratch` are rewritten by the next tile
+}
+
 // Single-vector tile: output rows r..r+tr-1 of G, its column-chunk stages from the ring, then the
 // epilogue.  The input vector comes from `xs` (staged in shared memory, already normalised) or,
 // when null, from G.x through L1 (times rstd and the norm weight when the group has a norm).
@@ -869,7 +1031,7 @@ __device__ void sv_tile(const EngineCfg& p, const GG& G, int r, int tr, Ring& R,
 // head kind.
 template <typename WT>
 static __device__ void consume_span(const EngineCfg& p, const GG* gg, int gb, int rb, int ge, int re, Ring& R,
-                             unsigned char* scratch, float* rstd_s, float* wpart, Top2* loc) {
+                             unsigned char* scratch, float* rstd_s, float* wpart, Top2* loc, TcCtx* tcx) {
   constexpr int VEC = WTraits<WT>::kVec;
   constexpr int CW = 512 / sizeof(WT);
   constexpr int NCT = kNCW * 32;
@@ -938,6 +1100,8 @@ static __device__ void consume_span(const EngineCfg& p, const GG* gg, int gb, in
     }
     if (!G.mma) {
       sv_tile<WT>(p, G, r, tr, R, xs_on ? xs : nullptr, rstd, loc);
+    } else if (G.tc) {
+      tc_tile<WT>(p, G, r, tr, R, *tcx, scratch, rstd_s, loc);
     } else if (G.nv <= 16) {
       mma_tile<WT, 1>(p, G, r, tr, R, scratch, rstd_s, loc);
     } else {

@@ -70,7 +70,25 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_engine(const __grid_constant
   Top2 loc[2];
   top2_init(loc[0]);
   top2_init(loc[1]);
-  consume_span<WT>(p.cfg, gg, s_gb, s_rb, s_ge, s_re, R, scratch, rstd_s, wpart, loc);
+  __shared__ uint32_t s_tmem;
+  __shared__ __align__(8) uint64_t s_tc_done;
+  TcCtx tcx{scratch, 0u, &s_tc_done, 0u};
+  if (p.cfg.has_tc) {  // consumer warp 0 holds the TMEM accumulator columns for the launch
+    if (warp == 0) tc::alloc_cols(&s_tmem);
+    if (tid == 0) { mbar_init(&s_tc_done, 1); fence_mbar_init(); }
+    tc::fence_before();
+    named_bar(1, kNCW * 32);
+    tc::fence_after();
+    tcx.tmem = s_tmem;
+  }
+  consume_span<WT>(p.cfg, gg, s_gb, s_rb, s_ge, s_re, R, scratch, rstd_s, wpart, loc, &tcx);
+  if (p.cfg.has_tc) {  // every MMA this CTA issued has completed and every tcgen05.ld is done
+    if (tid == 0) tc::commit(&s_tc_done);
+    mbar_wait_bounded(&s_tc_done, tcx.phase);
+    tc::fence_before();
+    named_bar(1, kNCW * 32);
+    if (warp == 0) tc::free_cols(tcx.tmem);
+  }
   bool head = false;
   for (int i = 0; i < ng; ++i) head |= gg[i].epi == EPI_TOP2;
   if (head || (ng == 0 && p.nparts > 0 && p.part[0].op == OP_HEAD))
@@ -138,6 +156,7 @@ cudaError_t launch_gemv(const GemvPart* parts, int nparts, const Dims& D, const 
   p.resolve_after_wait = resolve_after_wait ? 1 : 0;
   p.cfg.debug_logits = cfg.debug_logits;
   p.cfg.has_mma = D.dtype == SPD_DTYPE_BF16;
+  p.cfg.has_tc = D.tc;
   p.cfg.eps = D.eps;
   p.cfg.D = D; p.cfg.B = B;
   return D.dtype == SPD_DTYPE_BF16 ? launch_engine<__nv_bfloat16>(p, pdl, s) : launch_engine<float>(p, pdl, s);
@@ -185,6 +204,29 @@ cudaError_t gemv_encode_map(CUtensorMap* out, const void* W, int rows, int cols,
     r = encode(out, ty, 2, const_cast<void*>(W), gdim, gstride, box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE,
                CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   }
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+cudaError_t gemv_encode_tc_map(CUtensorMap* out, const void* W, int rows, int cols) {
+  CUtensorMap probe;
+  cudaError_t e = gemv_encode_map(&probe, W, rows, cols, SPD_DTYPE_BF16, true);  // resolves the encoder
+  if (e != cudaSuccess) return e;
+  static PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
+  if (!encode) {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+    e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q);
+    if (e != cudaSuccess) return e;
+    if (q != cudaDriverEntryPointSuccess || !fn) return cudaErrorNotSupported;
+    encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  }
+  const cuuint64_t gdim[3] = {64, (cuuint64_t)rows, (cuuint64_t)(cols / 64)};
+  const cuuint64_t gstride[2] = {(cuuint64_t)cols * 2, 128};
+  const cuuint32_t box[3] = {64, (cuuint32_t)tc::kRows, (cuuint32_t)tc::kStageCh};
+  const cuuint32_t estride[3] = {1, 1, 1};
+  const CUresult r = encode(out, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(W), gdim, gstride, box, estride,
+                            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 

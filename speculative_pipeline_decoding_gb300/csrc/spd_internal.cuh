@@ -55,6 +55,7 @@ struct Dims {
   int L, d, hq, hkv, hd, ffn, V, n, S, Ls, m;
   int max_seq, dtype, qkv_rows, gq;
   int box3;         // weight tensor maps are 3-D (see box3_cols): two copies per GEMV stage
+  int tc;           // tcgen05 draft tiles: every stream map is followed by its 128-row map
   int top_k;        // sampled decoding: top-k (0: greedy decoding)
   float temp;       // sampled decoding: temperature T > 0
   int anchors[SPD_MAX_ANCHORS];
@@ -176,13 +177,17 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
       : "=r"(ok) : "r"(smem_u32(bar)), "r"(parity) : "memory");
   return ok != 0;
 }
-// Bounded wait: gives up after ~2 s of wall time and reports false.
-__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity) {
+// Limit of every bounded device wait: after this much wall time (%globaltimer) the wait gives up,
+// the kernel sets the control block's error word and leaves; the host reports SPD_ETIMEOUT.
+constexpr uint64_t kWaitLimitNs = 2000000000ull;
+
+// Bounded wait: gives up after `limit_ns` of wall time and reports false.
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity, uint64_t limit_ns = kWaitLimitNs) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
   for (uint32_t it = 0;; ++it) {
     if (mbar_try_wait(bar, parity)) return true;
-    if ((it & 255u) == 255u && globaltimer_ns() - t0 > 2000000000ull) return false;
+    if ((it & 255u) == 255u && globaltimer_ns() - t0 > limit_ns) return false;
   }
 }
 __device__ __forceinline__ uint64_t l2_evict_first_policy() {
@@ -355,6 +360,9 @@ cudaError_t gemv_setup_attributes();
 inline bool box3_cols(int cols, int dtype) { return cols % (dtype == SPD_DTYPE_BF16 ? 64 : 32) == 0; }
 // Encodes that tensor map (3-D when box3, else 2-D).  Host call; returns a CUDA error code.
 cudaError_t gemv_encode_map(CUtensorMap* out, const void* W, int rows, int cols, int dtype, bool box3);
+// The 128-row map of a bf16 matrix for tcgen05 tiles: 3-D (chunk, row, chunk index), box 128 rows x
+// 2 chunks (32 KB, one ring stage), 128-byte swizzle.
+cudaError_t gemv_encode_tc_map(CUtensorMap* out, const void* W, int rows, int cols);
 int gemv_head_grid(int dtype);
 int num_sms();
 cudaError_t attn_setup_attributes(size_t max_smem);
@@ -371,6 +379,30 @@ cudaError_t launch_rollback(const Dims& D, const Bufs& B, int keep_len, int rese
 cudaError_t launch_begin_generate(const Dims& D, const Bufs& B, int max_new, cudaStream_t s);
 cudaError_t launch_rope_tables(float* cosv, float* sinv, int max_seq, int hd, float theta,
                                cudaStream_t s);
+
+// Runs one of the step kernel's bounded waits on a condition nothing satisfies (which: 0 grid barrier
+// counter, 1 mbarrier phase, 2 shared progress counter), with limit `limit_ns`; the wait sets the
+// ERR_TIMEOUT bit of st->err when it gives up.
+cudaError_t launch_wait_selftest(DevState* st, unsigned* counter, int which, uint64_t limit_ns, cudaStream_t s);
+
+// Causal attention of one prefill block on the tensor cores (spd_pfattn.cu): nq <= 32 query rows at
+// positions pos0..pos0+nq-1, keys and values of the layer already in its bf16 cache.
+struct PfAttnArgs {
+  const CUtensorMap* kmap;  // host copies of the 2-D maps over the K / V caches (pfattn_encode_map)
+  const CUtensorMap* vmap;
+  const float* q; int q_stride;  // query rows (rotated q of head h at h*hd)
+  float* out;                    // attention rows [row][hq*hd]
+  float* part; int* tick;        // split partials (pfattn_part_floats) and tickets (>= hq ints, zeroed)
+  DevState* st;                  // error word, or null
+  int kv_row0;                   // map row of position 1 of kv head 0 of the layer
+  int max_seq, hq, hkv, hd, pos0, nq, sms;
+};
+bool pfattn_supported(int dtype, int hd, int nq, int gq);
+size_t pfattn_smem_bytes(int hd);
+size_t pfattn_part_floats(int hkv, int gq, int max_seq, int sms);
+cudaError_t pfattn_encode_map(CUtensorMap* out, const void* cache, long long rows, int hd);
+cudaError_t pfattn_setup_attributes();
+cudaError_t launch_pfattn(const PfAttnArgs& a, cudaStream_t s);
 
 // records `msg` as the text spd_last_error(NULL) returns; gives back `code`
 int spd_internal_fail(int code, const char* msg);

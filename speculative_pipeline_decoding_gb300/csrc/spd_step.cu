@@ -62,11 +62,12 @@ __device__ __forceinline__ void red_add_release(unsigned* p, unsigned v) {
 __device__ __forceinline__ void grid_arrive(unsigned* bar) { red_add_release(bar, 1u); }  // thread 0
 
 // Thread 0: bounded wait for the counter to reach `target`.  False if it gave up.
-__device__ __forceinline__ bool grid_wait(const unsigned* bar, unsigned target, DevState* st) {
+__device__ __forceinline__ bool grid_wait(const unsigned* bar, unsigned target, DevState* st,
+                                          uint64_t limit_ns = kWaitLimitNs) {
   if ((int)(ld_acquire(bar) - target) >= 0) return true;
   const uint64_t t0 = globaltimer_ns();
   for (uint32_t it = 0; (int)(ld_acquire(bar) - target) < 0; ++it) {
-    if ((it & 63u) == 63u && globaltimer_ns() - t0 > 2000000000ull) {
+    if ((it & 63u) == 63u && globaltimer_ns() - t0 > limit_ns) {
       set_err(st, ERR_TIMEOUT, 70);
       return false;
     }
@@ -87,12 +88,34 @@ __device__ __forceinline__ int ld_acquire_cta(const int* p) {
   return v;
 }
 // Bounded wait (lane 0 of a warp) for a shared progress counter to reach `v`.
-__device__ __forceinline__ bool wait_progress(const int* p, int v) {
+__device__ __forceinline__ bool wait_progress(const int* p, int v, uint64_t limit_ns = kWaitLimitNs) {
   if (ld_acquire_cta(p) >= v) return true;
   const uint64_t t0 = globaltimer_ns();
   for (uint32_t it = 0; ld_acquire_cta(p) < v; ++it)
-    if ((it & 63u) == 63u && globaltimer_ns() - t0 > 2000000000ull) return false;
+    if ((it & 63u) == 63u && globaltimer_ns() - t0 > limit_ns) return false;
   return true;
+}
+
+// Self-check of the bounded waits: one thread runs the chosen wait on a condition that nothing
+// satisfies (a grid-barrier count that no CTA adds to, an mbarrier nobody arrives on, a progress
+// counter nobody advances) with a short limit; each must give up and flag ERR_TIMEOUT.
+__global__ void wait_selftest_kernel(DevState* st, unsigned* counter, int which, uint64_t limit_ns) {
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ int progress;
+  if (threadIdx.x != 0) return;
+  bool ok = true;
+  if (which == 0) {
+    ok = grid_wait(counter, ld_acquire(counter) + 1u, st, limit_ns);  // sets the flag itself
+  } else if (which == 1) {
+    mbar_init(&bar, 1);
+    fence_mbar_init();
+    ok = mbar_wait_bounded(&bar, 0, limit_ns);
+    if (!ok) set_err(st, ERR_TIMEOUT, 71);
+  } else {
+    progress = 0;
+    ok = wait_progress(&progress, 1, limit_ns);
+    if (!ok) set_err(st, ERR_TIMEOUT, 72);
+  }
 }
 
 __device__ __forceinline__ void mbar_arrive_cnt(uint64_t* bar, uint32_t n) {
@@ -337,7 +360,7 @@ __global__ void __launch_bounds__(kStepThreads, 1) step_kernel(const __grid_cons
               const uint64_t t0 = globaltimer_ns();
               const unsigned target = base + (unsigned)ph * gridDim.x;
               for (uint32_t it = 0; (int)(ld_acquire(p.bar) - target) < 0; ++it)
-                if ((it & 63u) == 63u && globaltimer_ns() - t0 > 2000000000ull) {
+                if ((it & 63u) == 63u && globaltimer_ns() - t0 > kWaitLimitNs) {
                   set_err(st, ERR_TIMEOUT, 41);
                   ok = 0;
                   break;
@@ -391,6 +414,18 @@ __global__ void __launch_bounds__(kStepThreads, 1) step_kernel(const __grid_cons
   // arrivals before this launch (fewer than gridDim.x of this launch can have been added yet)
   const unsigned bar_base = tid == 0 ? (ld_acquire(p.bar) / gridDim.x) * gridDim.x : 0u;
   named_bar(4, kNCT + 32);  // phase 0 resolved
+  // tcgen05 tiles: consumer warp 0 holds the TMEM accumulator columns for the whole launch
+  __shared__ uint32_t s_tmem;
+  __shared__ __align__(8) uint64_t s_tc_done;
+  TcCtx tcx{uni, 0u, &s_tc_done, 0u};
+  if (cfg.has_tc) {
+    if (warp == 0) tc::alloc_cols(&s_tmem);
+    if (tid == 0) { mbar_init(&s_tc_done, 1); fence_mbar_init(); }
+    tc::fence_before();
+    named_bar(1, kNCT);
+    tc::fence_after();
+    tcx.tmem = s_tmem;
+  }
   for (int ph = 0; ph < p.nphases; ++ph) {
     const int b = ph & 1;
     const Phase& P = s_ph[b];
@@ -400,7 +435,7 @@ __global__ void __launch_bounds__(kStepThreads, 1) step_kernel(const __grid_cons
       top2_init(loc[0]);
       top2_init(loc[1]);
       consume_span<WT>(cfg, gg + b * kStepGroups, s_gb[b], s_rb[b], s_ge[b], s_re[b], R, uni, rstd_s, wpart,
-                       loc);
+                       loc, &tcx);
       if (P.nparts > 0 && P.part[0].op == OP_HEAD)
         write_head_partial(loc, hred, cfg.B.head_part + (size_t)blockIdx.x * 8);
     } else if (P.type == PH_ATTN) {
@@ -437,6 +472,13 @@ __global__ void __launch_bounds__(kStepThreads, 1) step_kernel(const __grid_cons
       t_prev = t;
     }
   }
+  if (cfg.has_tc) {  // every MMA this CTA issued has completed and every tcgen05.ld is done
+    if (tid == 0) tc::commit(&s_tc_done);
+    mbar_wait_bounded(&s_tc_done, tcx.phase);
+    tc::fence_before();
+    named_bar(1, kNCT);
+    if (warp == 0) tc::free_cols(tcx.tmem);
+  }
 }
 
 static_assert(sizeof(Phase) % 16 == 0, "phase descriptors are copied in 16-byte pieces");
@@ -466,6 +508,11 @@ size_t step_smem_bytes(const Dims& D) {
   return total + static_bytes <= 227 * 1024 ? total : 0;
 }
 
+cudaError_t launch_wait_selftest(DevState* st, unsigned* counter, int which, uint64_t limit_ns, cudaStream_t s) {
+  wait_selftest_kernel<<<1, 32, 0, s>>>(st, counter, which, limit_ns);
+  return cudaGetLastError();
+}
+
 cudaError_t step_setup_attributes(size_t smem) {
   cudaError_t e = cudaFuncSetAttribute(step_kernel<float>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
@@ -478,6 +525,7 @@ cudaError_t launch_step(const Dims& D, const Bufs& B, const LaunchCfg& lcfg, con
   memset(&p, 0, sizeof(p));
   p.cfg.debug_logits = lcfg.debug_logits;
   p.cfg.has_mma = D.dtype == SPD_DTYPE_BF16;
+  p.cfg.has_tc = D.tc;
   p.cfg.eps = D.eps;
   p.cfg.D = D;
   p.cfg.B = B;

@@ -130,3 +130,31 @@ def test_attention_rows_outside_the_cache_come_back_nan(spd):
         for h in range(hq):
             want = om.softmax_attend(qc[r, h], kc[h // (hq // hkv), :p], vc[h // (hq // hkv), :p])
             np.testing.assert_allclose(oc[r, h].numpy(), want, rtol=2e-5, atol=2e-5)
+
+
+@pytest.mark.parametrize("hq,hkv,hd,pos0,R,max_seq", [
+    (32, 8, 128, 1, 32, 300),        # first block: keys 1..32, one chunk, one split
+    (32, 8, 128, 1000, 32, 1100),    # a later block: causal chunk at the diagonal
+    (32, 8, 128, 8001, 32, 8200),    # long context: split over CTAs, merged in split order
+    (16, 16, 128, 470, 17, 600),     # MHA, ragged block
+    (8, 2, 64, 250, 32, 300),        # head size 64
+    (4, 4, 64, 1, 1, 8),             # one query at position 1
+])
+def test_prefill_attention_matches_oracle(spd, hq, hkv, hd, pos0, R, max_seq):
+    g = torch.Generator(device="cpu").manual_seed(pos0 + R)
+    k = (torch.randn(hkv, max_seq, hd, generator=g) * 0.5).to(torch.bfloat16).cuda()
+    v = torch.randn(hkv, max_seq, hd, generator=g).to(torch.bfloat16).cuda()
+    q = (torch.randn(R, hq, hd, generator=g) * 0.5).cuda()
+    out = torch.full((R, hq, hd), float("nan"), device="cuda")
+    ws = torch.zeros(spd.binding.prefill_attention_workspace_bytes(hq, hkv, hd, max_seq) // 4 + 64,
+                     dtype=torch.int32, device="cuda")
+    for rep in range(2):  # the workspace's tickets are left zeroed for the next call
+        spd.binding.prefill_attention(q, k, v, pos0, out, ws)
+        torch.cuda.synchronize()
+        kc, vc, qc, oc = (t.float().cpu().numpy() for t in (k, v, q, out))
+        gq = hq // hkv
+        for r in range(R):
+            p = pos0 + r
+            for h in range(hq):
+                want = om.softmax_attend(qc[r, h], kc[h // gq, :p], vc[h // gq, :p])
+                np.testing.assert_allclose(oc[r, h], want, rtol=1e-4, atol=1e-4, err_msg=f"rep {rep} row {r} head {h}")
