@@ -503,13 +503,12 @@ __device__ void warp_merge(const Dims& D, const Tile& T, int kh) {
       for (int cc = lane; cc < nc; cc += 32) {
         const float* rc = base + cc * cstride;
         const float w = expf(__ldcg(rc + hd) - M);
+        // records are hd + 2 floats long: 8-byte aligned, so the slice is read as float2
 #pragma unroll
-        for (int e = 0; e < 32; e += 4) {
-          const float4 v = __ldcg(reinterpret_cast<const float4*>(rc + d0 + e));
+        for (int e = 0; e < 32; e += 2) {
+          const float2 v = __ldcg(reinterpret_cast<const float2*>(rc + d0 + e));
           acc[e] = fmaf(v.x, w, acc[e]);
           acc[e + 1] = fmaf(v.y, w, acc[e + 1]);
-          acc[e + 2] = fmaf(v.z, w, acc[e + 2]);
-          acc[e + 3] = fmaf(v.w, w, acc[e + 3]);
         }
       }
       // reduce-scatter: after the step of width h, lane l keeps the h dims of its half

@@ -794,7 +794,6 @@ __device__ void tc_tile(const EngineCfg& p, const GG& G, int r, int tr, Ring& R,
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int hd = p.D.hd, nv = G.nv;
   DevState* st = p.B.st;
-  const int nst = (G.cols / (tc::kStageCh * tc::kChunk)) * G.nw;
   // B of a stage: thread t builds the 8 columns 8*(t%16).. of vector t/16, both halves (row v: high,
   // row 16+v: low); the vector's row and its 1/rms are resolved once per tile
   const int bv = tid >> 4, bpc = tid & 15;
@@ -802,18 +801,32 @@ __device__ void tc_tile(const EngineCfg& p, const GG& G, int r, int tr, Ring& R,
   const float brs = (bv < nv && G.normw) ? rstd_s[bv] : 1.f;
   const uint32_t boff_hi = (uint32_t)((bpc >> 3) * tc::kB * 128 + bv * 128 + (((bpc & 7) ^ (bv & 7)) << 4));
   const uint32_t boff_lo = (uint32_t)((bpc >> 3) * tc::kB * 128 + (16 + bv) * 128 + (((bpc & 7) ^ ((16 + bv) & 7)) << 4));
-  auto build_b = [&](unsigned char* b, int c0) {
+  // The stage's 8 activations and norm weights of this thread come from L2 (each stage touches new
+  // columns), so they are loaded one column block ahead into registers.  Two register sets take
+  // turns; the column-block loop is unrolled by two so that each set keeps a fixed name.
+  constexpr int CB = tc::kStageCh * tc::kChunk;  // columns per stage
+  const int ncb = G.cols / CB;
+  float4 xa[2], na[2], xb[2], nb[2];
+  auto fetch = [&](int cb, float4* xr, float4* nr) {
+    if (bx && cb < ncb) {
+      const int col = cb * CB + 8 * bpc;
+      xr[0] = *reinterpret_cast<const float4*>(bx + col);
+      xr[1] = *reinterpret_cast<const float4*>(bx + col + 4);
+      if (G.normw) {
+        nr[0] = *reinterpret_cast<const float4*>(G.normw + col);
+        nr[1] = *reinterpret_cast<const float4*>(G.normw + col + 4);
+      }
+    }
+  };
+  auto build_b = [&](unsigned char* b, const float4* x4, const float4* n4) {
     uint4 hi = make_uint4(0u, 0u, 0u, 0u), lo = hi;
     if (bx) {
-      const int col = c0 + 8 * bpc;
-      float4 x0 = *reinterpret_cast<const float4*>(bx + col), x1 = *reinterpret_cast<const float4*>(bx + col + 4);
+      float xv[8] = {x4[0].x, x4[0].y, x4[0].z, x4[0].w, x4[1].x, x4[1].y, x4[1].z, x4[1].w};
       if (G.normw) {
-        const float4 n0 = *reinterpret_cast<const float4*>(G.normw + col);
-        const float4 n1 = *reinterpret_cast<const float4*>(G.normw + col + 4);
-        x0.x = x0.x * brs * n0.x; x0.y = x0.y * brs * n0.y; x0.z = x0.z * brs * n0.z; x0.w = x0.w * brs * n0.w;
-        x1.x = x1.x * brs * n1.x; x1.y = x1.y * brs * n1.y; x1.z = x1.z * brs * n1.z; x1.w = x1.w * brs * n1.w;
+        const float nv8[8] = {n4[0].x, n4[0].y, n4[0].z, n4[0].w, n4[1].x, n4[1].y, n4[1].z, n4[1].w};
+#pragma unroll
+        for (int e = 0; e < 8; ++e) xv[e] = xv[e] * brs * nv8[e];
       }
-      const float xv[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
       uint32_t h4[4], l4[4];
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
@@ -828,30 +841,39 @@ __device__ void tc_tile(const EngineCfg& p, const GG& G, int r, int tr, Ring& R,
     *reinterpret_cast<uint4*>(b + boff_hi) = hi;
     *reinterpret_cast<uint4*>(b + boff_lo) = lo;
   };
-  for (int k = 0; k < nst; ++k) {
-    const int s = R.ctr % kStages;
-    if (!R.failed && !mbar_wait_bounded(&R.full[s], (R.ctr / kStages) & 1)) {
-      if (lane == 0) set_err(st, ERR_TIMEOUT, 61);
-      R.failed = true;
-    }
-    unsigned char* bs = T.bring + (size_t)s * tc::kBBytes;
-    const int c0 = (k / G.nw) * tc::kStageCh * tc::kChunk;
-    if (!R.failed) build_b(bs, c0);
-    tc::fence_async_smem();
-    named_bar(1, NCT);
-    if (tid == 0) {
-      if (!R.failed) {
-        tc::fence_after();
-        const int h = G.nw == 2 ? (k & 1) : 0;  // gate / up accumulator
-        tc::mma_stage(T.tmem + (uint32_t)(32 * h), R.base + (size_t)s * kStageBytes, bs, k < G.nw);
-        tc::commit(&R.empty[s]);              // warp 0's arrival, when the MMAs have read the stage
-      } else {
+  // the nw stages (gate, up) of column block cb from set (x, n); block cb+1 prefetched into (xp, np)
+  auto block = [&](int cb, const float4* x, const float4* n, float4* xp, float4* np) {
+    fetch(cb + 1, xp, np);
+    for (int h = 0; h < G.nw; ++h) {
+      const int k = cb * G.nw + h;
+      const int s = R.ctr % kStages;
+      if (!R.failed && !mbar_wait_bounded(&R.full[s], (R.ctr / kStages) & 1)) {
+        if (lane == 0) set_err(st, ERR_TIMEOUT, 61);
+        R.failed = true;
+      }
+      unsigned char* bs = T.bring + (size_t)s * tc::kBBytes;
+      if (!R.failed) build_b(bs, x, n);
+      tc::fence_async_smem();
+      named_bar(1, NCT);
+      if (tid == 0) {
+        if (!R.failed) {
+          tc::fence_after();
+          // gate / up accumulators in columns 0..31 / 32..63
+          tc::mma_stage(T.tmem + (uint32_t)(32 * h), R.base + (size_t)s * kStageBytes, bs, k < G.nw);
+          tc::commit(&R.empty[s]);  // warp 0's arrival, when the MMAs have read the stage
+        } else {
+          mbar_arrive(&R.empty[s]);
+        }
+      } else if (warp != 0 && lane == 0) {
         mbar_arrive(&R.empty[s]);
       }
-    } else if (warp != 0 && lane == 0) {
-      mbar_arrive(&R.empty[s]);
+      ++R.ctr;
     }
-    ++R.ctr;
+  };
+  fetch(0, xa, na);
+  for (int cb = 0; cb < ncb; cb += 2) {
+    block(cb, xa, na, xb, nb);
+    if (cb + 1 < ncb) block(cb + 1, xb, nb, xa, na);
   }
   // tile end: every MMA done -> TMEM rows to registers -> epilogues.  The completion is committed
   // whatever happened (it arrives once the MMAs issued so far are done, at once if there are none),
