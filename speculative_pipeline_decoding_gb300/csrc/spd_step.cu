@@ -16,6 +16,8 @@
 // one resets it and advances the generation, the others wait (bounded: 2 s of %globaltimer, then
 // the error flag is set and the CTA leaves; the producer's bounded waits then run out too).  The
 // cooperative launch guarantees that all CTAs are resident.
+#include <mutex>
+
 #include "spd_attn.cuh"
 #include "spd_ctrl.cuh"
 #include "spd_engine.cuh"
@@ -513,10 +515,22 @@ cudaError_t launch_wait_selftest(DevState* st, unsigned* counter, int which, uin
   return cudaGetLastError();
 }
 
+// The dynamic shared-memory limit is an attribute of the kernel on the current device, shared by every
+// handle of the process: it is only ever raised (a handle of a smaller model must not lower the limit
+// another live handle launches with), per device ordinal, under a mutex.
 cudaError_t step_setup_attributes(size_t smem) {
-  cudaError_t e = cudaFuncSetAttribute(step_kernel<float>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  static std::mutex mu;
+  static size_t current[64] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  return cudaFuncSetAttribute(step_kernel<__nv_bfloat16>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  std::lock_guard<std::mutex> lock(mu);
+  if (dev >= 0 && dev < 64 && smem <= current[dev]) return cudaSuccess;
+  e = cudaFuncSetAttribute(step_kernel<float>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(step_kernel<__nv_bfloat16>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e == cudaSuccess && dev >= 0 && dev < 64) current[dev] = smem;
+  return e;
 }
 
 cudaError_t launch_step(const Dims& D, const Bufs& B, const LaunchCfg& lcfg, const Phase* prog, int nphases,
