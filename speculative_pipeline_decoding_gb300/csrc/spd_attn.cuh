@@ -466,68 +466,53 @@ __device__ void warp_item(const Dims& D, const Tile& T, const Item& it, const WT
   }
 }
 
-// Merge of (tile T, kv head kh) on the calling warp, after its last ticket; resets the ticket.
-// For each query head over its own nc chunks: lane j takes chunks j, j+32, ... (in that order),
-// weighting each partial by exp(m - M); the 32 lanes' sums are then added by a fixed butterfly that
-// leaves dim d of a 32-dim slice on lane d.  The arithmetic depends only on nc (the query's
-// position), so a token's result does not depend on its batch; every lane's loads are independent,
-// so a merge costs a few memory round trips, not one per chunk.
+// Merge of query head qh of (tile T, kv head kh) on the calling warp, once every chunk partial of
+// the pair is written: O = sum_c exp(m_c - M) o_c / sum_c exp(m_c - M) l_c over the query's own nc
+// chunks, M = max_c m_c.  Lane l owns dims l, l + 32, ... and adds the chunks in chunk order, so the
+// arithmetic depends only on nc (the query's position) and a token's result does not depend on its
+// batch.  The loads of NB consecutive chunks are issued together (the m and l loads are broadcasts),
+// so a merge costs about nc / NB memory round trips.
 template <int DPL>
-__device__ void warp_merge(const Dims& D, const Tile& T, int kh) {
+__device__ void merge_qh(const Dims& D, const Tile& T, int kh, int qh) {
   constexpr int CK = kWarpCK;
+  constexpr int NB = 32 / DPL;  // chunks per batch of loads
   const int lane = threadIdx.x & 31;
   const int hd = D.hd, GQ = D.gq;
-  const int hqd = D.hq * hd;
   const int QH = T.nq * GQ;
-  for (int qh = 0; qh < QH; ++qh) {
-    const int r = qh / GQ, hg = qh % GQ;
-    const int nc = (T.pos0 + r + CK - 1) / CK;
-    const float* base = T.part + ((size_t)T.rec_off + (size_t)kh * T.nch * QH + qh) * (hd + 2);
-    const size_t cstride = (size_t)QH * (hd + 2);
-    float M = -INFINITY;
-    for (int cc = lane; cc < nc; cc += 32) M = fmaxf(M, __ldcg(base + cc * cstride + hd));
+  const int r = qh / GQ, hg = qh % GQ;
+  const int nc = (T.pos0 + r + CK - 1) / CK;
+  const float* base = T.part + ((size_t)T.rec_off + (size_t)kh * T.nch * QH + qh) * (hd + 2);
+  const size_t cstride = (size_t)QH * (hd + 2);
+  float M = -INFINITY;
+  for (int cc = lane; cc < nc; cc += 32) M = fmaxf(M, __ldcg(base + cc * cstride + hd));
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-    float Ls = 0.f;
-    for (int cc = lane; cc < nc; cc += 32) {
-      const float* rc = base + cc * cstride;
-      Ls = fmaf(__ldcg(rc + hd + 1), expf(__ldcg(rc + hd) - M), Ls);
+  for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+  float Ls = 0.f, O[DPL];
+#pragma unroll
+  for (int e = 0; e < DPL; ++e) O[e] = 0.f;
+  for (int c0 = 0; c0 < nc; c0 += NB) {
+    float mm[NB], ll[NB], oo[NB][DPL];
+#pragma unroll
+    for (int u = 0; u < NB; ++u) {
+      const float* rc = base + (size_t)min(c0 + u, nc - 1) * cstride;
+      mm[u] = __ldcg(rc + hd);
+      ll[u] = __ldcg(rc + hd + 1);
+#pragma unroll
+      for (int e = 0; e < DPL; ++e) oo[u][e] = __ldcg(rc + lane + 32 * e);
     }
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) Ls += __shfl_xor_sync(0xffffffffu, Ls, o);
-    float* out = T.out + (size_t)(T.vid0 + r) * hqd + (kh * GQ + hg) * hd;
-    for (int d0 = 0; d0 < hd; d0 += 32) {  // one 32-dim slice of the output
-      float acc[32];
+    for (int u = 0; u < NB; ++u) {
+      if (c0 + u < nc) {
+        const float w = expf(mm[u] - M);
+        Ls = fmaf(ll[u], w, Ls);
 #pragma unroll
-      for (int e = 0; e < 32; ++e) acc[e] = 0.f;
-      for (int cc = lane; cc < nc; cc += 32) {
-        const float* rc = base + cc * cstride;
-        const float w = expf(__ldcg(rc + hd) - M);
-        // records are hd + 2 floats long: 8-byte aligned, so the slice is read as float2
-#pragma unroll
-        for (int e = 0; e < 32; e += 2) {
-          const float2 v = __ldcg(reinterpret_cast<const float2*>(rc + d0 + e));
-          acc[e] = fmaf(v.x, w, acc[e]);
-          acc[e + 1] = fmaf(v.y, w, acc[e + 1]);
-        }
+        for (int e = 0; e < DPL; ++e) O[e] = fmaf(oo[u][e], w, O[e]);
       }
-      // reduce-scatter: after the step of width h, lane l keeps the h dims of its half
-#pragma unroll
-      for (int h = 16; h > 0; h >>= 1) {
-        const bool upper = (lane & h) != 0;
-#pragma unroll
-        for (int e = 0; e < h; ++e) {
-          const float send = upper ? acc[e] : acc[e + h];
-          const float keep = upper ? acc[e + h] : acc[e];
-          acc[e] = keep + __shfl_xor_sync(0xffffffffu, send, h);
-        }
-      }
-      // lane l now holds dim d0 + bitreverse-free index: the kept half follows the lane bits
-      out[d0 + lane] = acc[0] / Ls;
     }
   }
-  __syncwarp();
-  if (lane == 0) T.tick[T.tick_off + kh] = 0;
+  float* out = T.out + (size_t)(T.vid0 + r) * (D.hq * hd) + (kh * GQ + hg) * hd;
+#pragma unroll
+  for (int e = 0; e < DPL; ++e) out[lane + 32 * e] = O[e] / Ls;
 }
 
 }  // namespace att

@@ -95,7 +95,8 @@ struct EngineCfg {
 };
 
 // split cost of one output row: its weight elements, weighted by the path's cost per byte
-constexpr int kCostTc = 2;  // a tcgen05 stage streams at the single-vector rate (to be measured)
+constexpr int kCostTc = 4;  // a tcgen05 tile byte takes ~2x a single-vector byte streamed alongside it
+                            // (per-CTA phase times of the co-scheduled cycle, 9B-class model)
 __device__ __forceinline__ long long rowcost(const GG& g) {
   return (long long)g.cols * g.nw * (g.tc ? kCostTc : (g.mma ? kCostMma : kCostSV));
 }

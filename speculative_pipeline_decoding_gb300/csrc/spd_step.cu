@@ -156,14 +156,19 @@ __device__ __forceinline__ int attn_item_at(const AttnPlan& a, int q, int& pass)
   return blockIdx.x + k * gridDim.x;
 }
 
+constexpr int kMergeList = 64;  // (tile, kv head) pairs one CTA can hold for its end-of-phase merge
+
 // Consumer warps of an attention phase.  Warp w takes padded positions q = w / wpi + j * (8 / wpi)
 // of this CTA's item sequence (ring stage q / ips, slot q % ips); wpi warps share an item (each takes
 // every wpi-th query head) and the two warps of a stage release it with 4 arrivals each.  The next
 // item's first query is loaded while the current one is computed; tickets are batched per warp
-// (one lane per (tile, kv head) touched) and flushed at the end.
+// (one lane per (tile, kv head) touched) and flushed at the end.  A pair whose last ticket a warp
+// takes goes on the CTA's merge list (mlist, *mcount); the caller merges the list with all warps
+// once every warp is done (attn_merge_list).
 template <typename WT, int DPL>
 __device__ void attn_consume(const Dims& D, const att::Tile* tb, int nt, const AttnPlan& A, int nst, int ips,
-                             int item_bytes, Ring& R, float* qb, int* s_fail, DevState* st) {
+                             int item_bytes, Ring& R, float* qb, int* s_fail, DevState* st, int* mlist,
+                             int* mcount) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int wpi = 2 / ips;
   const int qh0 = warp % wpi;
@@ -184,7 +189,17 @@ __device__ void attn_consume(const Dims& D, const att::Tile* tb, int nt, const A
       const int b = __ffs(mask) - 1;
       mask &= mask - 1;
       const int T_ = __shfl_sync(0xffffffffu, pT, b), kh_ = __shfl_sync(0xffffffffu, pkh, b);
-      att::warp_merge<DPL>(D, tb[T_], kh_);
+      int slot = 0;
+      if (lane == 0) slot = atomicAdd(mcount, 1);
+      slot = __shfl_sync(0xffffffffu, slot, 0);
+      if (slot < kMergeList) {
+        if (lane == 0) mlist[slot] = (T_ << 16) | kh_;
+      } else {  // list full: merge here, one query head after the other
+        const att::Tile& T = tb[T_];
+        for (int qh = 0; qh < T.nq * D.gq; ++qh) att::merge_qh<DPL>(D, T, kh_, qh);
+        __syncwarp();
+        if (lane == 0) T.tick[T.tick_off + kh_] = 0;
+      }
     }
     npend = 0;
   };
@@ -234,6 +249,23 @@ __device__ void attn_consume(const Dims& D, const att::Tile* tb, int nt, const A
   if (npend > 0 && !*(volatile int*)s_fail) flush();
 }
 
+// All consumer warps, after every warp's attn_consume of the phase (named barrier 1 in between):
+// merge the CTA's listed pairs, one (pair, query head) per warp at a time, and reset their tickets.
+template <int DPL>
+__device__ void attn_merge_list(const Dims& D, const att::Tile* tb, const int* mlist, int n) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  n = min(n, kMergeList);
+  int u = warp;  // units (pair, query head) in list order; warp w takes units w, w + 8, ...
+  for (int i = 0; i < n; ++i) {
+    const att::Tile& T = tb[mlist[i] >> 16];
+    const int kh = mlist[i] & 0xFFFF;
+    const int QH = T.nq * D.gq;
+    for (; u < QH; u += kNCW) att::merge_qh<DPL>(D, T, kh, u);
+    u -= QH;  // the next pair's query heads continue the warp's turn
+    if (lane == 0 && warp == 0) T.tick[T.tick_off + kh] = 0;
+  }
+}
+
 template <typename WT>
 __global__ void __launch_bounds__(kStepThreads, 1) step_kernel(const __grid_constant__ StepParams p) {
   extern __shared__ __align__(1024) unsigned char smem_raw[];
@@ -253,6 +285,7 @@ __global__ void __launch_bounds__(kStepThreads, 1) step_kernel(const __grid_cons
   __shared__ int s_ng[2], s_gb[2], s_rb[2], s_ge[2], s_re[2];  // GEMV: groups, this CTA's share
   __shared__ int s_nt[2], s_nold[2], s_nnew[2];                // attention: tiles, item counts
   __shared__ int s_fail, s_abort, s_tok, s_slot;
+  __shared__ int s_mlist[kMergeList], s_mcount;  // attention pairs this CTA merges at the phase end
   __shared__ float rstd_s[16 * kMaxMT];
   __shared__ float wpart[kNCW];
   __shared__ Top2 hred[kNCW * 8][2];
@@ -279,6 +312,7 @@ __global__ void __launch_bounds__(kStepThreads, 1) step_kernel(const __grid_cons
     s_produced = -1;
     s_fail = 0;
     s_abort = 0;
+    s_mcount = 0;
   }
   __syncthreads();
   if (s_sv.done || s_sv.err) return;  // every CTA reads the same control block: a uniform decision
@@ -446,11 +480,17 @@ __global__ void __launch_bounds__(kStepThreads, 1) step_kernel(const __grid_cons
       const AttnPlan A = attn_plan(s_nold[b], s_nnew[b], ips);
       const int nst = nt > 0 ? A.stages(ips) : 0;
       float* qb = reinterpret_cast<float*>(uni) + (size_t)warp * D.hd;
-      if (D.hd == 64) attn_consume<WT, 2>(D, tb, nt, A, nst, ips, item_bytes, R, qb, &s_fail, st);
-      else attn_consume<WT, 4>(D, tb, nt, A, nst, ips, item_bytes, R, qb, &s_fail, st);
+      if (D.hd == 64) attn_consume<WT, 2>(D, tb, nt, A, nst, ips, item_bytes, R, qb, &s_fail, st, s_mlist, &s_mcount);
+      else attn_consume<WT, 4>(D, tb, nt, A, nst, ips, item_bytes, R, qb, &s_fail, st, s_mlist, &s_mcount);
       R.ctr += (uint32_t)nst;
       named_bar(1, kNCT);
       if (s_fail) R.failed = true;
+      if (!R.failed && s_mcount > 0) {
+        if (D.hd == 64) attn_merge_list<2>(D, tb, s_mlist, s_mcount);
+        else attn_merge_list<4>(D, tb, s_mlist, s_mcount);
+      }
+      named_bar(1, kNCT);  // every warp has read the count
+      if (tid == 0) s_mcount = 0;
     } else if (blockIdx.x == 0 && !R.failed) {  // control: the last phase
       Top2 (*red)[2] = reinterpret_cast<Top2(*)[2]>(uni);
       // the ring is idle in the control phase (every stage of the head phase was consumed): the
