@@ -89,6 +89,7 @@ struct EngineCfg {
   int debug_logits;
   int has_mma;                 // bf16 weights (tensor-core path available)
   int has_tc;                  // tcgen05 tiles available (maps in pairs, TMEM allocated, B ring)
+  int tc_nv_max;               // largest vector count of a tcgen05 tile (16 or 32: the B ring's size)
   float eps;
   Dims D;
   Bufs B;
@@ -268,7 +269,7 @@ static __device__ int finish_groups(const EngineCfg& p, GG* gg, int ng, int cap)
     o.mma = o.nv > 1;
     // tcgen05 tiles: <= 16 vectors (16 high + 16 low B rows), whole 128-column stages, heads of at
     // most 128 rows (a 128-row tile holds whole heads, so RoPE pairs stay inside it)
-    o.tc = (short)(p.has_tc && o.mma && o.nv <= 16 && o.cols % 128 == 0 && p.D.hd <= 128);
+    o.tc = (short)(p.has_tc && o.mma && o.nv <= p.tc_nv_max && o.cols % 128 == 0 && p.D.hd <= 128);
     o.tr = (short)(o.tc ? tc::kRows : kSlots / o.nw);
     o.cost0 = cost;
     cost += (long long)o.rows * rowcost(o);
@@ -775,75 +776,94 @@ __device__ void mma_tile(const EngineCfg& p, const GG& G, int r, int tr, Ring& R
 // State of the tcgen05 path of one CTA: the B operand ring (one 8 KB slot per ring stage), the TMEM
 // accumulator (64 columns: gate in 0..31, up in 32..63), the tile-completion mbarrier and its phase.
 struct TcCtx {
-  unsigned char* bring;   // kStages x tc::kBBytes, 1024-byte aligned
+  unsigned char* bring;   // kStages x the tile shape's B bytes, 1024-byte aligned
   uint32_t tmem;          // TMEM address of column 0
   uint64_t* done;         // arrives when every MMA of the tile has completed
   uint32_t phase;
 };
 
 // tcgen05 tile: output rows r..r+tr-1 (physical rows; whole heads in the rotary region) of a group of
-// nv <= 16 vectors.  Per stage the consumers build B (high and low halves of the normalised
-// activations of the stage's 128 columns) once the stage's weights have landed -- which also means
-// the MMAs that last read that B slot are done -- then one thread issues the 8 MMAs and commits them
-// to the stage's empty barrier in place of warp 0's arrival, so the producer refills the slot only
-// after the tensor core has read it.  At the tile end warps 0-3 read their 32 TMEM lanes (rows) and
-// run the epilogue of every vector; RoPE partners (row + hd/2) are exchanged through `scratch`.
-template <typename WT>
+// nv <= NVP vectors (NVP = 16 or 32).  Per stage the consumers build B (high and low halves of the
+// normalised activations of the stage's 128 columns: rows v and NVP+v) once the stage's weights
+// have landed -- which also means the MMAs that last read that B slot are done -- then one thread
+// issues the 8 MMAs and commits them to the stage's empty barrier in place of warp 0's arrival, so the
+// producer refills the slot only after the tensor core has read it.  At the tile end warps 0-3 read
+// their 32 TMEM lanes (rows) 16 vectors at a time and run the epilogue of every vector; RoPE partners
+// (row + hd/2) are exchanged through `scratch`.
+template <typename WT, int NVP>
 __device__ void tc_tile(const EngineCfg& p, const GG& G, int r, int tr, Ring& R, TcCtx& T, unsigned char* scratch,
                         const float* rstd_s, Top2* loc) {
   constexpr int NCT = kNCW * 32;
+  constexpr int kB = tc::Shape<NVP>::kB;
+  constexpr int kBBytes = tc::Shape<NVP>::kBBytes;
+  constexpr uint32_t kAcc = tc::Shape<NVP>::kAccCols;
+  constexpr int NPT = NVP / 16;  // (vector, 8-column piece) pairs per thread and stage
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int hd = p.D.hd, nv = G.nv;
   DevState* st = p.B.st;
-  // B of a stage: thread t builds the 8 columns 8*(t%16).. of vector t/16, both halves (row v: high,
-  // row 16+v: low); the vector's row and its 1/rms are resolved once per tile
-  const int bv = tid >> 4, bpc = tid & 15;
-  const float* bx = bv < nv ? G.x + (size_t)((G.xrow0 + bv) % G.xring) * G.xstride : nullptr;
-  const float brs = (bv < nv && G.normw) ? rstd_s[bv] : 1.f;
-  const uint32_t boff_hi = (uint32_t)((bpc >> 3) * tc::kB * 128 + bv * 128 + (((bpc & 7) ^ (bv & 7)) << 4));
-  const uint32_t boff_lo = (uint32_t)((bpc >> 3) * tc::kB * 128 + (16 + bv) * 128 + (((bpc & 7) ^ ((16 + bv) & 7)) << 4));
-  // The stage's 8 activations and norm weights of this thread come from L2 (each stage touches new
+  // B of a stage: thread t builds the 8 columns 8*(t%16).. of vectors t/16 + 16 i (i < NPT), both
+  // halves (row v: high, row NVP+v: low); the vectors' rows and 1/rms are resolved once per tile
+  const int bpc = tid & 15;
+  const float* bx[NPT];
+  float brs[NPT];
+  uint32_t boff_hi[NPT], boff_lo[NPT];
+#pragma unroll
+  for (int i = 0; i < NPT; ++i) {
+    const int bv = (tid >> 4) + 16 * i;
+    bx[i] = bv < nv ? G.x + (size_t)((G.xrow0 + bv) % G.xring) * G.xstride : nullptr;
+    brs[i] = (bv < nv && G.normw) ? rstd_s[bv] : 1.f;
+    boff_hi[i] = (uint32_t)((bpc >> 3) * kB * 128 + bv * 128 + (((bpc & 7) ^ (bv & 7)) << 4));
+    boff_lo[i] = (uint32_t)((bpc >> 3) * kB * 128 + (NVP + bv) * 128 + (((bpc & 7) ^ ((NVP + bv) & 7)) << 4));
+  }
+  // The stage's activations and norm weights of this thread come from L2 (each stage touches new
   // columns), so they are loaded one column block ahead into registers.  Two register sets take
   // turns; the column-block loop is unrolled by two so that each set keeps a fixed name.
   constexpr int CB = tc::kStageCh * tc::kChunk;  // columns per stage
   const int ncb = G.cols / CB;
-  float4 xa[2], na[2], xb[2], nb[2];
-  auto fetch = [&](int cb, float4* xr, float4* nr) {
-    if (bx && cb < ncb) {
+  float4 xa[NPT][2], xb[NPT][2], na[2], nb[2];
+  auto fetch = [&](int cb, float4 (*xr)[2], float4* nr) {
+    if (cb < ncb) {
       const int col = cb * CB + 8 * bpc;
-      xr[0] = *reinterpret_cast<const float4*>(bx + col);
-      xr[1] = *reinterpret_cast<const float4*>(bx + col + 4);
-      if (G.normw) {
+#pragma unroll
+      for (int i = 0; i < NPT; ++i)
+        if (bx[i]) {
+          xr[i][0] = *reinterpret_cast<const float4*>(bx[i] + col);
+          xr[i][1] = *reinterpret_cast<const float4*>(bx[i] + col + 4);
+        }
+      if (G.normw && bx[0]) {
         nr[0] = *reinterpret_cast<const float4*>(G.normw + col);
         nr[1] = *reinterpret_cast<const float4*>(G.normw + col + 4);
       }
     }
   };
-  auto build_b = [&](unsigned char* b, const float4* x4, const float4* n4) {
-    uint4 hi = make_uint4(0u, 0u, 0u, 0u), lo = hi;
-    if (bx) {
-      float xv[8] = {x4[0].x, x4[0].y, x4[0].z, x4[0].w, x4[1].x, x4[1].y, x4[1].z, x4[1].w};
-      if (G.normw) {
-        const float nv8[8] = {n4[0].x, n4[0].y, n4[0].z, n4[0].w, n4[1].x, n4[1].y, n4[1].z, n4[1].w};
+  auto build_b = [&](unsigned char* b, const float4 (*x4)[2], const float4* n4) {
 #pragma unroll
-        for (int e = 0; e < 8; ++e) xv[e] = xv[e] * brs * nv8[e];
-      }
-      uint32_t h4[4], l4[4];
+    for (int i = 0; i < NPT; ++i) {
+      uint4 hi = make_uint4(0u, 0u, 0u, 0u), lo = hi;
+      if (bx[i]) {
+        float xv[8] = {x4[i][0].x, x4[i][0].y, x4[i][0].z, x4[i][0].w, x4[i][1].x, x4[i][1].y, x4[i][1].z, x4[i][1].w};
+        if (G.normw) {
+          const float nv8[8] = {n4[0].x, n4[0].y, n4[0].z, n4[0].w, n4[1].x, n4[1].y, n4[1].z, n4[1].w};
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const __nv_bfloat16 a = __float2bfloat16_rn(xv[2 * e]), c = __float2bfloat16_rn(xv[2 * e + 1]);
-        const float fa = __bfloat162float(a), fc = __bfloat162float(c);
-        h4[e] = pack_bf16x2(fa, fc);
-        l4[e] = pack_bf16x2(xv[2 * e] - fa, xv[2 * e + 1] - fc);
+          for (int e = 0; e < 8; ++e) xv[e] = xv[e] * brs[i] * nv8[e];
+        }
+        uint32_t h4[4], l4[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const __nv_bfloat16 a = __float2bfloat16_rn(xv[2 * e]), c = __float2bfloat16_rn(xv[2 * e + 1]);
+          const float fa = __bfloat162float(a), fc = __bfloat162float(c);
+          h4[e] = pack_bf16x2(fa, fc);
+          l4[e] = pack_bf16x2(xv[2 * e] - fa, xv[2 * e + 1] - fc);
+        }
+        hi = make_uint4(h4[0], h4[1], h4[2], h4[3]);
+        lo = make_uint4(l4[0], l4[1], l4[2], l4[3]);
       }
-      hi = make_uint4(h4[0], h4[1], h4[2], h4[3]);
-      lo = make_uint4(l4[0], l4[1], l4[2], l4[3]);
+      *reinterpret_cast<uint4*>(b + boff_hi[i]) = hi;
+      *reinterpret_cast<uint4*>(b + boff_lo[i]) = lo;
     }
-    *reinterpret_cast<uint4*>(b + boff_hi) = hi;
-    *reinterpret_cast<uint4*>(b + boff_lo) = lo;
   };
   // the nw stages (gate, up) of column block cb from set (x, n); block cb+1 prefetched into (xp, np)
-  auto block = [&](int cb, const float4* x, const float4* n, float4* xp, float4* np) {
+  auto block = [&](int cb, const float4 (*x)[2], const float4* n, float4 (*xp)[2], float4* np) {
     fetch(cb + 1, xp, np);
     for (int h = 0; h < G.nw; ++h) {
       const int k = cb * G.nw + h;
@@ -852,15 +872,15 @@ __device__ void tc_tile(const EngineCfg& p, const GG& G, int r, int tr, Ring& R,
         if (lane == 0) set_err(st, ERR_TIMEOUT, 61);
         R.failed = true;
       }
-      unsigned char* bs = T.bring + (size_t)s * tc::kBBytes;
+      unsigned char* bs = T.bring + (size_t)s * kBBytes;
       if (!R.failed) build_b(bs, x, n);
       tc::fence_async_smem();
       named_bar(1, NCT);
       if (tid == 0) {
         if (!R.failed) {
           tc::fence_after();
-          // gate / up accumulators in columns 0..31 / 32..63
-          tc::mma_stage(T.tmem + (uint32_t)(32 * h), R.base + (size_t)s * kStageBytes, bs, k < G.nw);
+          // gate / up accumulators in columns [0, kAcc) / [kAcc, 2 kAcc)
+          tc::mma_stage<NVP>(T.tmem + kAcc * (uint32_t)h, R.base + (size_t)s * kStageBytes, bs, k < G.nw);
           tc::commit(&R.empty[s]);  // warp 0's arrival, when the MMAs have read the stage
         } else {
           mbar_arrive(&R.empty[s]);
@@ -885,32 +905,46 @@ __device__ void tc_tile(const EngineCfg& p, const GG& G, int r, int tr, Ring& R,
   if (!ok) { if (lane == 0) set_err(st, ERR_TIMEOUT, 62); R.failed = true; }
   ok = ok && !R.failed;
   tc::fence_after();
-  float* xch = reinterpret_cast<float*>(scratch);  // [128 rows][16 vectors]: RoPE partner values
+  float* xch = reinterpret_cast<float*>(scratch);  // [128 rows][NVP vectors]: RoPE partner values
   const bool pairs = G.epi == EPI_QKV && r < G.seg2;
-  uint32_t d[32], u[32];
   const bool wok = __all_sync(0xffffffffu, ok);  // tcgen05.ld is warp-collective
-  if (warp < 4 && wok) {
-    tc::load_rows(T.tmem, warp, d);
-    if (G.nw == 2) tc::load_rows(T.tmem + 32, warp, u);
-    if (pairs) {
-      const int row = 32 * warp + lane;
+  const int row = 32 * warp + lane;              // tile-local physical row (warps 0-3)
+  if (pairs) {
+    if (warp < 4 && wok) {
 #pragma unroll
-      for (int v = 0; v < 16; ++v) xch[row * 16 + v] = __uint_as_float(d[v]) + __uint_as_float(d[16 + v]);
+      for (int v0 = 0; v0 < NVP; v0 += 16) {
+        uint32_t dh[16], dl[16];
+        tc::load_rows16(T.tmem + v0, warp, dh);
+        tc::load_rows16(T.tmem + NVP + v0, warp, dl);
+#pragma unroll
+        for (int v = 0; v < 16; ++v) xch[row * NVP + v0 + v] = __uint_as_float(dh[v]) + __uint_as_float(dl[v]);
+      }
     }
-  }
-  named_bar(1, NCT);
-  if (wok && warp < 4) {
-    const int row = 32 * warp + lane;  // tile-local physical row
-    if (row < tr) {
-      for (int v = 0; v < nv; ++v) {
-        const float y0 = __uint_as_float(d[v]) + __uint_as_float(d[16 + v]);
-        if (G.nw == 2) {
-          epilogue<WT>(p, G, v, r + row, y0, __uint_as_float(u[v]) + __uint_as_float(u[16 + v]), false, loc);
-        } else if (pairs) {
-          const int i = (r + row) % hd;      // tiles start on a head boundary
-          if (i < hd / 2) epilogue<WT>(p, G, v, r + row, y0, xch[(row + hd / 2) * 16 + v], true, loc);
-        } else {
-          epilogue<WT>(p, G, v, r + row, y0, 0.f, false, loc);
+    named_bar(1, NCT);
+    if (wok && warp < 4 && row < tr) {
+      const int i = (r + row) % hd;  // tiles start on a head boundary
+      if (i < hd / 2)
+        for (int v = 0; v < nv; ++v)
+          epilogue<WT>(p, G, v, r + row, xch[row * NVP + v], xch[(row + hd / 2) * NVP + v], true, loc);
+    }
+  } else if (warp < 4 && wok) {
+#pragma unroll
+    for (int v0 = 0; v0 < NVP; v0 += 16) {
+      if (v0 >= nv) break;
+      uint32_t dh[16], dl[16], uh[16], ul[16];
+      tc::load_rows16(T.tmem + v0, warp, dh);
+      tc::load_rows16(T.tmem + NVP + v0, warp, dl);
+      if (G.nw == 2) {
+        tc::load_rows16(T.tmem + kAcc + v0, warp, uh);
+        tc::load_rows16(T.tmem + kAcc + NVP + v0, warp, ul);
+      }
+      if (row < tr) {
+        for (int v = 0; v < 16 && v0 + v < nv; ++v) {
+          const float y0 = __uint_as_float(dh[v]) + __uint_as_float(dl[v]);
+          if (G.nw == 2)
+            epilogue<WT>(p, G, v0 + v, r + row, y0, __uint_as_float(uh[v]) + __uint_as_float(ul[v]), false, loc);
+          else
+            epilogue<WT>(p, G, v0 + v, r + row, y0, 0.f, false, loc);
         }
       }
     }
@@ -1052,7 +1086,7 @@ __device__ void sv_tile(const EngineCfg& p, const GG& G, int r, int tr, Ring& R,
 // epilogues.  `scratch` (kMmaScratch bytes) holds the tensor-core path's activation fragments and
 // pair exchange, `rstd_s` one 1/rms per vector, `wpart` kNCW floats, `loc` the thread's top-2 per
 // head kind.
-template <typename WT>
+template <typename WT, int TCMAX>
 static __device__ void consume_span(const EngineCfg& p, const GG* gg, int gb, int rb, int ge, int re, Ring& R,
                              unsigned char* scratch, float* rstd_s, float* wpart, Top2* loc, TcCtx* tcx) {
   constexpr int VEC = WTraits<WT>::kVec;
@@ -1124,7 +1158,12 @@ static __device__ void consume_span(const EngineCfg& p, const GG* gg, int gb, in
     if (!G.mma) {
       sv_tile<WT>(p, G, r, tr, R, xs_on ? xs : nullptr, rstd, loc);
     } else if (G.tc) {
-      tc_tile<WT>(p, G, r, tr, R, *tcx, scratch, rstd_s, loc);
+      if constexpr (TCMAX > 16) {
+        if (G.nv > 16) tc_tile<WT, 32>(p, G, r, tr, R, *tcx, scratch, rstd_s, loc);
+        else tc_tile<WT, 16>(p, G, r, tr, R, *tcx, scratch, rstd_s, loc);
+      } else {
+        tc_tile<WT, 16>(p, G, r, tr, R, *tcx, scratch, rstd_s, loc);
+      }
     } else if (G.nv <= 16) {
       mma_tile<WT, 1>(p, G, r, tr, R, scratch, rstd_s, loc);
     } else {

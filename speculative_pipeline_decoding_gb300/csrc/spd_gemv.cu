@@ -14,7 +14,10 @@ namespace {
 
 using namespace eng;
 
-constexpr int kGemvSmem = 1024 + kStages * kStageBytes + kMmaScratch;
+// scratch: the tensor-core path's partial tiles, or the tcgen05 B ring of tiles of up to 32 vectors
+constexpr int kGemvScratch = kMmaScratch > kStages * tc::Shape<32>::kBBytes ? kMmaScratch
+                                                                            : kStages * tc::Shape<32>::kBBytes;
+constexpr int kGemvSmem = 1024 + kStages * kStageBytes + kGemvScratch;
 
 struct GemvParams {
   EngineCfg cfg;
@@ -74,20 +77,20 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_engine(const __grid_constant
   __shared__ __align__(8) uint64_t s_tc_done;
   TcCtx tcx{scratch, 0u, &s_tc_done, 0u};
   if (p.cfg.has_tc) {  // consumer warp 0 holds the TMEM accumulator columns for the launch
-    if (warp == 0) tc::alloc_cols(&s_tmem);
+    if (warp == 0) tc::alloc_cols(&s_tmem, tc::kColsGemv);
     if (tid == 0) { mbar_init(&s_tc_done, 1); fence_mbar_init(); }
     tc::fence_before();
     named_bar(1, kNCW * 32);
     tc::fence_after();
     tcx.tmem = s_tmem;
   }
-  consume_span<WT>(p.cfg, gg, s_gb, s_rb, s_ge, s_re, R, scratch, rstd_s, wpart, loc, &tcx);
+  consume_span<WT, 32>(p.cfg, gg, s_gb, s_rb, s_ge, s_re, R, scratch, rstd_s, wpart, loc, &tcx);
   if (p.cfg.has_tc) {  // every MMA this CTA issued has completed and every tcgen05.ld is done
     if (tid == 0) tc::commit(&s_tc_done);
     mbar_wait_bounded(&s_tc_done, tcx.phase);
     tc::fence_before();
     named_bar(1, kNCW * 32);
-    if (warp == 0) tc::free_cols(tcx.tmem);
+    if (warp == 0) tc::free_cols(tcx.tmem, tc::kColsGemv);
   }
   bool head = false;
   for (int i = 0; i < ng; ++i) head |= gg[i].epi == EPI_TOP2;
@@ -157,6 +160,7 @@ cudaError_t launch_gemv(const GemvPart* parts, int nparts, const Dims& D, const 
   p.cfg.debug_logits = cfg.debug_logits;
   p.cfg.has_mma = D.dtype == SPD_DTYPE_BF16;
   p.cfg.has_tc = D.tc;
+  p.cfg.tc_nv_max = 32;
   p.cfg.eps = D.eps;
   p.cfg.D = D; p.cfg.B = B;
   return D.dtype == SPD_DTYPE_BF16 ? launch_engine<__nv_bfloat16>(p, pdl, s) : launch_engine<float>(p, pdl, s);

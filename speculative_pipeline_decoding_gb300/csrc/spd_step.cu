@@ -455,7 +455,7 @@ __global__ void __launch_bounds__(kStepThreads, 1) step_kernel(const __grid_cons
   __shared__ __align__(8) uint64_t s_tc_done;
   TcCtx tcx{uni, 0u, &s_tc_done, 0u};
   if (cfg.has_tc) {
-    if (warp == 0) tc::alloc_cols(&s_tmem);
+    if (warp == 0) tc::alloc_cols(&s_tmem, tc::kColsStep);
     if (tid == 0) { mbar_init(&s_tc_done, 1); fence_mbar_init(); }
     tc::fence_before();
     named_bar(1, kNCT);
@@ -470,7 +470,7 @@ __global__ void __launch_bounds__(kStepThreads, 1) step_kernel(const __grid_cons
       Top2 loc[2];
       top2_init(loc[0]);
       top2_init(loc[1]);
-      consume_span<WT>(cfg, gg + b * kStepGroups, s_gb[b], s_rb[b], s_ge[b], s_re[b], R, uni, rstd_s, wpart,
+      consume_span<WT, 16>(cfg, gg + b * kStepGroups, s_gb[b], s_rb[b], s_ge[b], s_re[b], R, uni, rstd_s, wpart,
                        loc, &tcx);
       if (P.nparts > 0 && P.part[0].op == OP_HEAD)
         write_head_partial(loc, hred, cfg.B.head_part + (size_t)blockIdx.x * 8);
@@ -519,7 +519,7 @@ __global__ void __launch_bounds__(kStepThreads, 1) step_kernel(const __grid_cons
     mbar_wait_bounded(&s_tc_done, tcx.phase);
     tc::fence_before();
     named_bar(1, kNCT);
-    if (warp == 0) tc::free_cols(tcx.tmem);
+    if (warp == 0) tc::free_cols(tcx.tmem, tc::kColsStep);
   }
 }
 
@@ -580,6 +580,7 @@ cudaError_t launch_step(const Dims& D, const Bufs& B, const LaunchCfg& lcfg, con
   p.cfg.debug_logits = lcfg.debug_logits;
   p.cfg.has_mma = D.dtype == SPD_DTYPE_BF16;
   p.cfg.has_tc = D.tc;
+  p.cfg.tc_nv_max = 16;  // the union scratch holds the B ring of 16-vector tiles
   p.cfg.eps = D.eps;
   p.cfg.D = D;
   p.cfg.B = B;

@@ -19,11 +19,17 @@ namespace spd {
 namespace tc {
 
 constexpr int kRows = 128;     // M: weight rows of a tile
-constexpr int kB = 32;         // N: B rows (16 high + 16 low)
 constexpr int kChunk = 64;     // bf16 elements of a 128-byte chunk
 constexpr int kStageCh = 2;    // chunks per 32 KB stage
-constexpr int kBBytes = kStageCh * kB * 128;  // 8 KB of B per stage
-constexpr uint32_t kCols = 64; // TMEM columns allocated (gate 0..31, up 32..63)
+// A tile serves up to NVP vectors (16 or 32): B has 2*NVP rows (NVP high halves, NVP low halves),
+// the accumulator 2*NVP TMEM columns (gate / up tiles: two accumulators).
+template <int NVP> struct Shape {
+  static constexpr int kB = 2 * NVP;                          // N: B rows
+  static constexpr int kBBytes = kStageCh * kB * 128;         // B bytes per stage (8 or 16 KB)
+  static constexpr uint32_t kAccCols = 2 * NVP;               // TMEM columns of one accumulator
+};
+constexpr uint32_t kColsStep = 64;    // TMEM columns the step kernel allocates (16 vectors, gate + up)
+constexpr uint32_t kColsGemv = 128;   // ... the stand-alone engine (32 vectors, gate + up)
 
 __device__ __forceinline__ uint32_t su32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
 
@@ -40,14 +46,14 @@ __host__ __device__ constexpr uint32_t idesc_bf16(int m, int n) {
   return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(m >> 4) << 24);
 }
 
-__device__ __forceinline__ void alloc_cols(uint32_t* smem_dst) {  // whole warp
+__device__ __forceinline__ void alloc_cols(uint32_t* smem_dst, uint32_t ncols) {  // whole warp
   asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(su32(smem_dst)),
-               "r"(kCols)
+               "r"(ncols)
                : "memory");
   asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
 }
-__device__ __forceinline__ void free_cols(uint32_t taddr) {  // whole warp
-  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(kCols) : "memory");
+__device__ __forceinline__ void free_cols(uint32_t taddr, uint32_t ncols) {  // whole warp
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
 }
 __device__ __forceinline__ void fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
@@ -66,10 +72,12 @@ __device__ __forceinline__ void commit(uint64_t* bar) {
                : "memory");
 }
 
-// One stage: A (kStageCh chunks x 128 rows) at `a`, B (kStageCh chunks x 32 rows) at `b`, both
+// One stage: A (kStageCh chunks x 128 rows) at `a`, B (kStageCh chunks x 2*NVP rows) at `b`, both
 // 1024-byte aligned; 4 MMAs of K = 16 per chunk, advancing 32 bytes inside the swizzle atom.
+template <int NVP>
 __device__ __forceinline__ void mma_stage(uint32_t d_tmem, const unsigned char* a, const unsigned char* b,
                                           bool first) {
+  constexpr int kB = Shape<NVP>::kB;
   constexpr uint32_t id = idesc_bf16(kRows, kB);
 #pragma unroll
   for (int ch = 0; ch < kStageCh; ++ch)
@@ -77,6 +85,17 @@ __device__ __forceinline__ void mma_stage(uint32_t d_tmem, const unsigned char* 
     for (int ks = 0; ks < kChunk / 16; ++ks)
       mma(d_tmem, sdesc(su32(a) + ch * kRows * 128 + ks * 32), sdesc(su32(b) + ch * kB * 128 + ks * 32), id,
           !(first && ch == 0 && ks == 0));
+}
+
+// The warp's 32 TMEM lanes (rows 32*(warp%4) .. +31), 16 columns, into v[0..15] (fp32 bits).
+__device__ __forceinline__ void load_rows16(uint32_t tmem, int warp, uint32_t* v) {
+  const uint32_t ta = tmem + ((uint32_t)(32 * (warp & 3)) << 16);
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+      : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7]),
+        "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]), "=r"(v[15])
+      : "r"(ta));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
 
 // The warp's 32 TMEM lanes (rows 32*(warp%4) .. +31), 32 columns, into v[0..31] (fp32 bits).
