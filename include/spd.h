@@ -264,9 +264,13 @@ int spd_set_options(spd_handle* h, int32_t flags);
  *   SPD_DUMP_SEQ     int32[max_seq+2]      token at each position (index = position)
  *   SPD_DUMP_TRACE   int32[2][max_seq]     per verification: position, accepted
  *   SPD_DUMP_KVLEN   int32[L]              per-layer KV length bookkeeping
+ *   SPD_DUMP_PREFILL_H fp32[32][d]         residual after all L layers of the last prefill block's
+ *                                          rows (row i = position P - cnt + 1 + i, cnt = the block's
+ *                                          row count, 1..32); later rows are stale
  * SPD_EINVAL if `bytes` differs from the layout's size (query it with spd_dump_size). */
 enum { SPD_DUMP_STATE = 0, SPD_DUMP_RESID = 1, SPD_DUMP_ANCHORS = 2, SPD_DUMP_PDM_Z = 3,
-       SPD_DUMP_LOGITS = 4, SPD_DUMP_SEQ = 5, SPD_DUMP_TRACE = 6, SPD_DUMP_KVLEN = 7 };
+       SPD_DUMP_LOGITS = 4, SPD_DUMP_SEQ = 5, SPD_DUMP_TRACE = 6, SPD_DUMP_KVLEN = 7,
+       SPD_DUMP_PREFILL_H = 8 };
 size_t spd_dump_size(const spd_handle* h, int32_t what);
 int spd_debug_dump(spd_handle* h, int32_t what, void* host_dst, size_t bytes);
 

@@ -26,7 +26,7 @@ DTYPE_F32, DTYPE_BF16 = 0, 1
 OPT_GRAPHS, OPT_COSCHED, OPT_TARGET_ONLY, OPT_DEBUG_LOGITS, OPT_PDL, OPT_STEP = 1, 2, 4, 8, 16, 32
 OPT_POST_STEP = 64  # draft module after the target step, on its output state
 OPT_DEFAULT = OPT_GRAPHS | OPT_COSCHED | OPT_PDL | OPT_STEP
-DUMP_STATE, DUMP_RESID, DUMP_ANCHORS, DUMP_PDM_Z, DUMP_LOGITS, DUMP_SEQ, DUMP_TRACE, DUMP_KVLEN = range(8)
+DUMP_STATE, DUMP_RESID, DUMP_ANCHORS, DUMP_PDM_Z, DUMP_LOGITS, DUMP_SEQ, DUMP_TRACE, DUMP_KVLEN, DUMP_PREFILL_H = range(9)
 _OPS = ["qkv", "rope_append", "attention", "o_proj", "gate_up", "down", "anchor_fc", "head",
         "control"]
 KIND_NAMES = _OPS + ["draft_" + k for k in _OPS]
@@ -357,6 +357,8 @@ class Engine:
             return buf.reshape(2, c.vocab)
         if what == DUMP_TRACE:
             return buf.reshape(2, c.max_seq)
+        if what == DUMP_PREFILL_H:
+            return buf.reshape(-1, c.d_model)
         return buf
 
     def state(self) -> Dict[str, int]:

@@ -993,6 +993,7 @@ size_t spd_dump_size(const spd_handle* h, int32_t what) {
     case SPD_DUMP_SEQ: return sizeof(int32_t) * (D.max_seq + 2);
     case SPD_DUMP_TRACE: return sizeof(int32_t) * 2 * D.max_seq;
     case SPD_DUMP_KVLEN: return sizeof(int32_t) * D.L;
+    case SPD_DUMP_PREFILL_H: return sizeof(float) * kPrefillBlock * D.d;
     default: return 0;
   }
 }
@@ -1010,6 +1011,7 @@ int spd_debug_dump(spd_handle* h, int32_t what, void* dst, size_t bytes) {
     case SPD_DUMP_LOGITS: src = h->B.logits; break;
     case SPD_DUMP_SEQ: src = h->B.seq; break;
     case SPD_DUMP_TRACE: src = h->B.trace; break;
+    case SPD_DUMP_PREFILL_H: src = h->act_pf.resid; break;
     default: src = h->B.kvlen; break;
   }
   SPD_CUDA(h, cudaStreamSynchronize(h->s_main));

@@ -395,6 +395,43 @@ def test_full_width_per_cycle_parity_short_prompt(spd, name):
 
 
 # ------------------------------------------------------------------------------------------------
+# prefill on the tensor cores: a prompt of 2100 tokens (65 full blocks and a ragged block of 20 rows;
+# the causal attention splits its 17 key chunks over CTAs) -- the hidden states after all layers of
+# the last block and the tokens after it, against the oracle
+# ------------------------------------------------------------------------------------------------
+LONG_PROMPT_BF16 = si.Workload(
+    "small_bf16_gqa_long_prompt",
+    si.ModelConfig(n_layers=8, d_model=512, n_heads=8, n_kv_heads=2, head_dim=64, d_ffn=1024,
+                   vocab=2048, dtype="bf16"),
+    n_stages=4, pdm_layers=2, anchors=(0, 2, 4, 6, 7), prompt_len=2100, gen_len=8, alphas=(0.7,))
+
+HD128_LONG_PROMPT = si.Workload(
+    "gqa_hd128_long_prompt",
+    si.ModelConfig(n_layers=4, d_model=1024, n_heads=16, n_kv_heads=4, head_dim=128, d_ffn=2048,
+                   vocab=4096, dtype="bf16"),
+    n_stages=2, pdm_layers=2, anchors=(0, 2, 4), prompt_len=2049, gen_len=8, alphas=(0.7,))
+
+
+@pytest.mark.parametrize("w", [LONG_PROMPT_BF16, HD128_LONG_PROMPT], ids=lambda w: w.name)
+def test_long_prompt_prefill_hidden_states_match_oracle(spd, w):
+    from speculative_pipeline_decoding_gb300.binding import DUMP_PREFILL_H
+    S = Setup(spd, w)
+    try:
+        P = S.P
+        cnt = P - 32 * ((P - 1) // 32)  # rows of the last prefill block
+        got = S.eng.dump(DUMP_PREFILL_H)[:cnt]
+        target, _ = S.models
+        H, _ = target.prefill(S.prompt, target.new_cache(P + 1))
+        err = rel(got, H[P - cnt:])
+        assert err < 2e-2, err
+        flagged, _ = teacher_forced_check(S.models, S.prompt, S.ar)
+        assert flagged <= 1
+    finally:
+        S.eng.close()
+    print(w.name, "prefill hidden-state relative error", err)
+
+
+# ------------------------------------------------------------------------------------------------
 # execution options: the persistent step kernel vs per-operator launches, draft module co-scheduled
 # vs serialised, graphs vs eager launches -- every combination computes the same streams
 # ------------------------------------------------------------------------------------------------
@@ -438,16 +475,15 @@ def test_execution_options_give_identical_streams(request, setup, name):
 # model, the first GPU tokens against the oracle (teacher-forced)
 # ------------------------------------------------------------------------------------------------
 FULL_SIZE = ["gqa4b_bf16_n8", "gqa9b_bf16_n4", "gqa9b_bf16_n8", "gqa9b_bf16_n16", "gqa4b_bf16_n8_ctx32k"]
-# the 32K-token prefill spends ~7 minutes in causal attention on the CUDA-core prefill path: run it
-# with SPD_SLOW_TESTS=1
-SLOW = {"gqa4b_bf16_n8_ctx32k"}
+# every full-size configuration runs by default (the 32K-token prefill takes about half a minute)
+SLOW = set()
 
 
 @pytest.mark.parametrize("name", FULL_SIZE)
 def test_full_size_spd_equals_ar_and_trace(spd, name):
     import os
     if name in SLOW and os.environ.get("SPD_SLOW_TESTS") != "1":
-        pytest.skip("32K-token prefill takes ~7 min; set SPD_SLOW_TESTS=1")
+        pytest.skip("set SPD_SLOW_TESTS=1")
     w = si.WORKLOADS[name]
     params = si.generate_weights(w, device="cuda")
     prompt = si.prompt_tokens(w).tolist()
