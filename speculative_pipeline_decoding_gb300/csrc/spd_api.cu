@@ -701,6 +701,13 @@ int spd_create(const spd_config* cfg, const spd_weights* w, void* cuda_stream, s
   FP = F;
   ALLOC(FP.resid, float, (size_t)PB * d);
   FP.anch = F.anch;  // anchor source of the prefix rows for the draft FC
+  // split-K partials and tickets of the tcgen05 groups (one launch or one step-kernel phase at a time)
+  if (D.tc) {
+    B.tc_part_cap = 8 << 20;
+    B.tc_tick_cap = 4096;
+    ALLOC(B.tc_part, float, (size_t)B.tc_part_cap);
+    ALLOC(B.tc_tick, int, (size_t)B.tc_tick_cap);
+  }
   // prefill attention on the tensor cores: maps over the whole caches (row = layer, kv head, position)
   if (pfattn_supported(c.dtype, hd, PB, gq)) {
     const int sms = num_sms();

@@ -74,6 +74,9 @@ struct GG {
   short mma, tr;               // tensor-core path; tile height in output rows (64 / nw)
   short tc;                    // tcgen05 path (mma groups of <= 16 vectors, bf16, 3-D maps): 128-row
                                // tiles, stages of 128 rows x 2 chunks from the map at m[s] + 1
+  short ks;                    // tcgen05 tiles split over ks column segments (split-K; 1: whole rows)
+  int vrows;                   // rows in share space: rows, or ntiles * ks * 128 when split
+  int tbase, pbase;            // split groups: first ticket of the group's tiles, first partial float
   const float* x; int xrow0, xring, xstride;
   float* y; int yrow0, yring, ystride;
   const float* normw;
@@ -99,8 +102,14 @@ struct EngineCfg {
 constexpr int kCostTc = 4;  // a tcgen05 tile byte takes ~2x a single-vector byte streamed alongside it
                             // (per-CTA phase times of the co-scheduled cycle, 9B-class model)
 __device__ __forceinline__ long long rowcost(const GG& g) {
-  return (long long)g.cols * g.nw * (g.tc ? kCostTc : (g.mma ? kCostMma : kCostSV));
+  return (long long)(g.cols / g.ks) * g.nw * (g.tc ? kCostTc : (g.mma ? kCostMma : kCostSV));
 }
+
+// Split-K of tcgen05 groups: a group of whole 128-row tiles whose tiles are too few to fill the grid
+// is cut into ks column segments of >= kMinSegBlocks 128-column blocks.  A unit (tile, segment)
+// writes its fp32 partial tile to scratch; the last unit of a tile to finish (atomic ticket) adds the
+// partials in segment order and runs the epilogue.  ks depends only on the group's shape and the grid.
+constexpr int kMinSegBlocks = 4;
 
 __device__ __forceinline__ int anchor_index(const Dims& D, int layer_done) {
   for (int i = 0; i < D.m; ++i)
@@ -110,7 +119,7 @@ __device__ __forceinline__ int anchor_index(const Dims& D, int layer_done) {
 
 __device__ __forceinline__ void gg_clear(GG& o) {
   o.seg1 = o.seg2 = kBig;
-  o.nw = 1; o.epi = EPI_STORE; o.kind = 0; o.mma = 0; o.nv = 1;
+  o.nw = 1; o.epi = EPI_STORE; o.kind = 0; o.mma = 0; o.nv = 1; o.ks = 1; o.tc = 0;
   o.normw = nullptr; o.anch = nullptr; o.astride = 0;
   o.kc = o.vc = nullptr; o.pos0 = 0; o.kvlen = nullptr;
   o.xrow0 = o.yrow0 = 0; o.xring = o.yring = kBig;
@@ -263,16 +272,35 @@ static __device__ int finish_groups(const EngineCfg& p, GG* gg, int ng, int cap)
   }
   ng = out;
   long long cost = 0;
+  int tickets = 0, parts = 0;
   for (int g = 0; g < ng; ++g) {
     GG& o = gg[g];
     if (o.nv > 16 * kMaxMT) { set_err(p.B.st, ERR_BOUNDS, 91); return 0; }
     o.mma = o.nv > 1;
-    // tcgen05 tiles: <= 16 vectors (16 high + 16 low B rows), whole 128-column stages, heads of at
-    // most 128 rows (a 128-row tile holds whole heads, so RoPE pairs stay inside it)
+    // tcgen05 tiles: <= 16 (32) vectors, whole 128-column stages, heads of at most 128 rows (a
+    // 128-row tile holds whole heads, so RoPE pairs stay inside it)
     o.tc = (short)(p.has_tc && o.mma && o.nv <= p.tc_nv_max && o.cols % 128 == 0 && p.D.hd <= 128);
     o.tr = (short)(o.tc ? tc::kRows : kSlots / o.nw);
+    o.ks = 1;
+    o.vrows = o.rows;
+    if (o.tc && p.B.tc_part && o.rows % tc::kRows == 0 &&
+        (o.epi != EPI_QKV || (o.seg1 % tc::kRows == 0 && o.seg2 % tc::kRows == 0))) {
+      const int ntile = o.rows / tc::kRows, ncb = o.cols / (tc::kStageCh * tc::kChunk);
+      int ks = (2 * (int)gridDim.x + ntile - 1) / ntile;  // about two units per CTA from this group alone
+      ks = min(ks, ncb / kMinSegBlocks);
+      const int nvp = o.nv <= 16 ? 16 : 32;
+      const int need = ntile * ks * o.nw * tc::kRows * nvp;
+      if (ks > 1 && tickets + ntile <= p.B.tc_tick_cap && parts + need <= p.B.tc_part_cap) {
+        o.ks = (short)ks;
+        o.vrows = ntile * ks * tc::kRows;
+        o.tbase = tickets;
+        o.pbase = parts;
+        tickets += ntile;
+        parts += need;
+      }
+    }
     o.cost0 = cost;
-    cost += (long long)o.rows * rowcost(o);
+    cost += (long long)o.vrows * rowcost(o);
   }
   return ng;
 }
@@ -302,7 +330,7 @@ static __device__ int resolve_explicit(const EngineCfg& p, const GemvExplicit& g
 // whose tiles hold complete (i, i+hd/2) pairs).  Monotone in X, so neighbouring shares meet exactly.
 static __device__ void locate(const GG* gg, int ng, long long X, int& g, int& r) {
   g = 0;
-  while (g < ng && X >= gg[g].cost0 + (long long)gg[g].rows * rowcost(gg[g])) ++g;
+  while (g < ng && X >= gg[g].cost0 + (long long)gg[g].vrows * rowcost(gg[g])) ++g;
   if (g >= ng) { g = ng; r = 0; return; }
   const long long rc = rowcost(gg[g]);
   const long long exact = (X - gg[g].cost0) / rc;
@@ -310,8 +338,8 @@ static __device__ void locate(const GG* gg, int ng, long long X, int& g, int& r)
   // same however many of its rows are used); 32-row boxes elsewhere
   const int gran = ((gg[g].epi == EPI_QKV && exact < gg[g].seg2) || gg[g].mma) ? (int)gg[g].tr : kBoxRows;
   r = (int)(((X - gg[g].cost0) + rc * gran / 2) / (rc * gran)) * gran;
-  if (gg[g].epi == EPI_QKV && r > gg[g].seg2 && exact < gg[g].seg2) r = gg[g].seg2;
-  if (r >= gg[g].rows) { ++g; r = 0; }
+  if (gg[g].ks == 1 && gg[g].epi == EPI_QKV && r > gg[g].seg2 && exact < gg[g].seg2) r = gg[g].seg2;
+  if (r >= gg[g].vrows) { ++g; r = 0; }
 }
 
 __device__ __forceinline__ float warp_sum(float v) {
@@ -459,7 +487,7 @@ __device__ __forceinline__ void span_of(const GG* gg, int ng, int cta, int ncta,
                                         int& re) {
   gb = ge = ng; rb = re = 0;
   if (!ng) return;
-  const long long total = gg[ng - 1].cost0 + (long long)gg[ng - 1].rows * rowcost(gg[ng - 1]);
+  const long long total = gg[ng - 1].cost0 + (long long)gg[ng - 1].vrows * rowcost(gg[ng - 1]);
   locate(gg, ng, total * cta / ncta, gb, rb);
   locate(gg, ng, total * (cta + 1) / ncta, ge, re);
 }
@@ -468,9 +496,24 @@ __device__ __forceinline__ void span_of(const GG* gg, int ng, int cta, int ncta,
 // tile height, clipped to the share and, in a QKV group, to the end of the rotary rows.
 __device__ __forceinline__ int tile_rows(const GG& G, int r, int last) {
   int tr = min((int)G.tr, last - r);
+  if (G.ks > 1) return tr;  // split groups: whole 128-row tiles in share space
   if (G.epi == EPI_QKV && r < G.seg2) tr = min(tr, G.seg2 - r);
   if (G.tc && G.epi == EPI_QKV && r < G.seg1) tr = min(tr, G.seg1 - r);  // one tensor map per tile
   return tr;
+}
+
+// A tcgen05 tile at share-space row r: its first physical row rr and its 128-column blocks
+// [cb0, cb1) (split groups: unit r / 128 = tile * ks + segment).
+__device__ __forceinline__ void tc_unit(const GG& G, int r, int& rr, int& cb0, int& cb1) {
+  const int ncb = G.cols / (tc::kStageCh * tc::kChunk);
+  if (G.ks > 1) {
+    const int u = r / tc::kRows, seg = u % G.ks;
+    rr = (u / G.ks) * tc::kRows;
+    cb0 = seg * ncb / G.ks;
+    cb1 = (seg + 1) * ncb / G.ks;
+  } else {
+    rr = r; cb0 = 0; cb1 = ncb;
+  }
 }
 
 // Producer warp: one stage = the 64 weight slots of tile row `r` (tr output rows) at column c0.
@@ -569,14 +612,16 @@ __device__ void produce_span(const GG* gg, int gb, int rb, int ge, int re, int h
   constexpr int CW = 512 / sizeof(WT);     // columns per stage
   for (int g = gb, r = rb; (g < ge || (g == ge && r < re)) && !R.failed;) {
     const GG& G = gg[g];
-    const int last = (g == ge) ? re : G.rows;
+    const int last = (g == ge) ? re : G.vrows;
     const int tr = tile_rows(G, r, last);
     if (G.tc) {  // tcgen05 tile: 128 physical rows, 2 chunks a stage; gate/up alternate the matrices
-      const int sg = r < G.seg1 ? 0 : (r < G.seg2 ? 1 : 2);
-      const int y = r - (sg == 0 ? 0 : (sg == 1 ? G.seg1 : G.seg2));
-      for (int c0 = 0; c0 < G.cols && !R.failed; c0 += tc::kStageCh * tc::kChunk)
+      int rr, cb0, cb1;
+      tc_unit(G, r, rr, cb0, cb1);
+      const int sg = rr < G.seg1 ? 0 : (rr < G.seg2 ? 1 : 2);
+      const int y = rr - (sg == 0 ? 0 : (sg == 1 ? G.seg1 : G.seg2));
+      for (int cb = cb0; cb < cb1 && !R.failed; ++cb)
         for (int h = 0; h < G.nw && !R.failed; ++h)
-          issue_tc_stage(G.nw == 2 ? G.m[h] + 1 : G.m[sg] + 1, G.nw == 2 ? r : y, c0 / tc::kChunk, R, st, pol, lane);
+          issue_tc_stage(G.nw == 2 ? G.m[h] + 1 : G.m[sg] + 1, G.nw == 2 ? rr : y, cb * tc::kStageCh, R, st, pol, lane);
       r += tr;
       if (r >= last) { ++g; r = 0; }
       continue;
@@ -780,6 +825,8 @@ struct TcCtx {
   uint32_t tmem;          // TMEM address of column 0
   uint64_t* done;         // arrives when every MMA of the tile has completed
   uint32_t phase;
+  uint64_t* bfull;        // [kStages]: the 8 consumer warps have written the slot's B (8 arrivals)
+  uint32_t bphase;        // bit s: parity of bfull[s]'s next completion (kept by the issuing thread)
 };
 
 // tcgen05 tile: output rows r..r+tr-1 (physical rows; whole heads in the rotary region) of a group of
@@ -792,7 +839,7 @@ struct TcCtx {
 // (row + hd/2) are exchanged through `scratch`.
 template <typename WT, int NVP>
 __device__ void tc_tile(const EngineCfg& p, const GG& G, int r, int tr, Ring& R, TcCtx& T, unsigned char* scratch,
-                        const float* rstd_s, Top2* loc) {
+                        const float* rstd_s, Top2* loc, int cb0, int cb1, int unit) {
   constexpr int NCT = kNCW * 32;
   constexpr int kB = tc::Shape<NVP>::kB;
   constexpr int kBBytes = tc::Shape<NVP>::kBBytes;
@@ -819,7 +866,7 @@ __device__ void tc_tile(const EngineCfg& p, const GG& G, int r, int tr, Ring& R,
   // columns), so they are loaded one column block ahead into registers.  Two register sets take
   // turns; the column-block loop is unrolled by two so that each set keeps a fixed name.
   constexpr int CB = tc::kStageCh * tc::kChunk;  // columns per stage
-  const int ncb = G.cols / CB;
+  const int ncb = cb1;                            // blocks [cb0, cb1) of this tile (unit)
   float4 xa[NPT][2], xb[NPT][2], na[2], nb[2];
   auto fetch = [&](int cb, float4 (*xr)[2], float4* nr) {
     if (cb < ncb) {
@@ -866,7 +913,6 @@ __device__ void tc_tile(const EngineCfg& p, const GG& G, int r, int tr, Ring& R,
   auto block = [&](int cb, const float4 (*x)[2], const float4* n, float4 (*xp)[2], float4* np) {
     fetch(cb + 1, xp, np);
     for (int h = 0; h < G.nw; ++h) {
-      const int k = cb * G.nw + h;
       const int s = R.ctr % kStages;
       if (!R.failed && !mbar_wait_bounded(&R.full[s], (R.ctr / kStages) & 1)) {
         if (lane == 0) set_err(st, ERR_TIMEOUT, 61);
@@ -875,14 +921,20 @@ __device__ void tc_tile(const EngineCfg& p, const GG& G, int r, int tr, Ring& R,
       unsigned char* bs = T.bring + (size_t)s * kBBytes;
       if (!R.failed) build_b(bs, x, n);
       tc::fence_async_smem();
-      named_bar(1, NCT);
+      __syncwarp();
+      // no CTA-wide barrier: each warp reports its part of B and moves on to the next stage; the
+      // issuing thread waits for the eight reports of this slot
+      if (lane == 0) mbar_arrive(&T.bfull[s]);
       if (tid == 0) {
-        if (!R.failed) {
+        const bool bok = !R.failed && mbar_wait_bounded(&T.bfull[s], (T.bphase >> s) & 1u);
+        T.bphase ^= 1u << s;
+        if (bok) {
           tc::fence_after();
           // gate / up accumulators in columns [0, kAcc) / [kAcc, 2 kAcc)
-          tc::mma_stage<NVP>(T.tmem + kAcc * (uint32_t)h, R.base + (size_t)s * kStageBytes, bs, k < G.nw);
+          tc::mma_stage<NVP>(T.tmem + kAcc * (uint32_t)h, R.base + (size_t)s * kStageBytes, bs, cb == cb0);
           tc::commit(&R.empty[s]);  // warp 0's arrival, when the MMAs have read the stage
         } else {
+          if (!R.failed) { set_err(st, ERR_TIMEOUT, 63); R.failed = true; }
           mbar_arrive(&R.empty[s]);
         }
       } else if (warp != 0 && lane == 0) {
@@ -891,8 +943,8 @@ __device__ void tc_tile(const EngineCfg& p, const GG& G, int r, int tr, Ring& R,
       ++R.ctr;
     }
   };
-  fetch(0, xa, na);
-  for (int cb = 0; cb < ncb; cb += 2) {
+  fetch(cb0, xa, na);
+  for (int cb = cb0; cb < ncb; cb += 2) {
     block(cb, xa, na, xb, nb);
     if (cb + 1 < ncb) block(cb + 1, xb, nb, xa, na);
   }
@@ -905,10 +957,64 @@ __device__ void tc_tile(const EngineCfg& p, const GG& G, int r, int tr, Ring& R,
   if (!ok) { if (lane == 0) set_err(st, ERR_TIMEOUT, 62); R.failed = true; }
   ok = ok && !R.failed;
   tc::fence_after();
-  float* xch = reinterpret_cast<float*>(scratch);  // [128 rows][NVP vectors]: RoPE partner values
   const bool pairs = G.epi == EPI_QKV && r < G.seg2;
   const bool wok = __all_sync(0xffffffffu, ok);  // tcgen05.ld is warp-collective
   const int row = 32 * warp + lane;              // tile-local physical row (warps 0-3)
+  if (G.ks > 1) {
+    // split-K unit: partial tile [acc][vector][128 rows] to scratch; the last unit of the tile adds
+    // the ks partials in segment order and runs the epilogue
+    __shared__ int s_last_unit;
+    const int usz = G.nw * NVP * tc::kRows;
+    float* pu = p.B.tc_part + G.pbase + (size_t)unit * usz;
+    if (warp < 4 && wok) {
+      for (int acc = 0; acc < G.nw; ++acc)
+#pragma unroll
+        for (int v0 = 0; v0 < NVP; v0 += 16) {
+          if (v0 >= nv) break;
+          uint32_t dh[16], dl[16];
+          tc::load_rows16(T.tmem + kAcc * (uint32_t)acc + v0, warp, dh);
+          tc::load_rows16(T.tmem + kAcc * (uint32_t)acc + NVP + v0, warp, dl);
+#pragma unroll
+          for (int v = 0; v < 16; ++v)
+            __stcg(pu + (size_t)(acc * NVP + v0 + v) * tc::kRows + row, __uint_as_float(dh[v]) + __uint_as_float(dl[v]));
+        }
+    }
+    __threadfence();
+    tc::fence_before();
+    named_bar(1, NCT);
+    if (tid == 0) {
+      int* tk = p.B.tc_tick + G.tbase + unit / G.ks;
+      const int old = atomicAdd(tk, 1);
+      s_last_unit = old == G.ks - 1;
+      if (s_last_unit) *tk = 0;  // left at zero for the next phase
+    }
+    named_bar(1, NCT);
+    if (s_last_unit && wok) {
+      __threadfence();
+      const float* pt = p.B.tc_part + G.pbase + (size_t)(unit / G.ks) * G.ks * usz;
+      auto sum = [&](int acc, int v, int rw) {
+        float a = 0.f;
+        for (int sg = 0; sg < G.ks; ++sg) a += __ldcg(pt + (size_t)sg * usz + (size_t)(acc * NVP + v) * tc::kRows + rw);
+        return a;
+      };
+      for (int idx = tid; idx < tc::kRows * nv; idx += NCT) {
+        const int rw = idx % tc::kRows, v = idx / tc::kRows;
+        if (rw >= tr) continue;
+        if (pairs) {
+          const int i = (r + rw) % hd;  // tiles start on a head boundary
+          if (i < hd / 2) epilogue<WT>(p, G, v, r + rw, sum(0, v, rw), sum(0, v, rw + hd / 2), true, loc);
+        } else if (G.nw == 2) {
+          epilogue<WT>(p, G, v, r + rw, sum(0, v, rw), sum(1, v, rw), false, loc);
+        } else {
+          epilogue<WT>(p, G, v, r + rw, sum(0, v, rw), 0.f, false, loc);
+        }
+      }
+    }
+    tc::fence_before();
+    named_bar(1, NCT);  // TMEM is rewritten by the next tile
+    return;
+  }
+  float* xch = reinterpret_cast<float*>(scratch);  // [128 rows][NVP vectors]: RoPE partner values
   if (pairs) {
     if (warp < 4 && wok) {
 #pragma unroll
@@ -1102,7 +1208,7 @@ static __device__ void consume_span(const EngineCfg& p, const GG* gg, int gb, in
   int last_g = -1;
   for (int g = gb, r = rb; g < ge || (g == ge && r < re);) {
     const GG& G = gg[g];
-    const int last = (g == ge) ? re : G.rows;
+    const int last = (g == ge) ? re : G.vrows;
     const int tr = tile_rows(G, r, last);
     if (g != last_g) {  // group entry: 1/rms of the input vector(s)
       named_bar(1, NCT);
@@ -1158,11 +1264,15 @@ static __device__ void consume_span(const EngineCfg& p, const GG* gg, int gb, in
     if (!G.mma) {
       sv_tile<WT>(p, G, r, tr, R, xs_on ? xs : nullptr, rstd, loc);
     } else if (G.tc) {
+      int rr, cb0, cb1;
+      tc_unit(G, r, rr, cb0, cb1);
+      const int trr = G.ks > 1 ? tc::kRows : tr;
+      const int unit = r / tc::kRows;
       if constexpr (TCMAX > 16) {
-        if (G.nv > 16) tc_tile<WT, 32>(p, G, r, tr, R, *tcx, scratch, rstd_s, loc);
-        else tc_tile<WT, 16>(p, G, r, tr, R, *tcx, scratch, rstd_s, loc);
+        if (G.nv > 16) tc_tile<WT, 32>(p, G, rr, trr, R, *tcx, scratch, rstd_s, loc, cb0, cb1, unit);
+        else tc_tile<WT, 16>(p, G, rr, trr, R, *tcx, scratch, rstd_s, loc, cb0, cb1, unit);
       } else {
-        tc_tile<WT, 16>(p, G, r, tr, R, *tcx, scratch, rstd_s, loc);
+        tc_tile<WT, 16>(p, G, rr, trr, R, *tcx, scratch, rstd_s, loc, cb0, cb1, unit);
       }
     } else if (G.nv <= 16) {
       mma_tile<WT, 1>(p, G, r, tr, R, scratch, rstd_s, loc);

@@ -75,10 +75,15 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_engine(const __grid_constant
   top2_init(loc[1]);
   __shared__ uint32_t s_tmem;
   __shared__ __align__(8) uint64_t s_tc_done;
-  TcCtx tcx{scratch, 0u, &s_tc_done, 0u};
+  __shared__ __align__(8) uint64_t s_tc_bfull[kStages];
+  TcCtx tcx{scratch, 0u, &s_tc_done, 0u, s_tc_bfull, 0u};
   if (p.cfg.has_tc) {  // consumer warp 0 holds the TMEM accumulator columns for the launch
     if (warp == 0) tc::alloc_cols(&s_tmem, tc::kColsGemv);
-    if (tid == 0) { mbar_init(&s_tc_done, 1); fence_mbar_init(); }
+    if (tid == 0) {
+      mbar_init(&s_tc_done, 1);
+      for (int i = 0; i < kStages; ++i) mbar_init(&s_tc_bfull[i], kNCW);
+      fence_mbar_init();
+    }
     tc::fence_before();
     named_bar(1, kNCW * 32);
     tc::fence_after();

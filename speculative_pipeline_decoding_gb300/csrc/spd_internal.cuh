@@ -92,6 +92,9 @@ struct Bufs {
   const CUtensorMap* tm_fc[SPD_MAX_ANCHORS];
   const CUtensorMap* tm_lm;
   const CUtensorMap* tm_pdm;
+  float* tc_part;    // split-K partial tiles of the tcgen05 groups of one launch or phase (or null)
+  int* tc_tick;      // their tickets (left at zero)
+  int tc_part_cap, tc_tick_cap;  // floats / tickets available
 };
 
 // How the rows of one launch are formed from the control block.

@@ -453,10 +453,15 @@ __global__ void __launch_bounds__(kStepThreads, 1) step_kernel(const __grid_cons
   // tcgen05 tiles: consumer warp 0 holds the TMEM accumulator columns for the whole launch
   __shared__ uint32_t s_tmem;
   __shared__ __align__(8) uint64_t s_tc_done;
-  TcCtx tcx{uni, 0u, &s_tc_done, 0u};
+  __shared__ __align__(8) uint64_t s_tc_bfull[kStages];
+  TcCtx tcx{uni, 0u, &s_tc_done, 0u, s_tc_bfull, 0u};
   if (cfg.has_tc) {
     if (warp == 0) tc::alloc_cols(&s_tmem, tc::kColsStep);
-    if (tid == 0) { mbar_init(&s_tc_done, 1); fence_mbar_init(); }
+    if (tid == 0) {
+      mbar_init(&s_tc_done, 1);
+      for (int i = 0; i < kStages; ++i) mbar_init(&s_tc_bfull[i], kNCW);
+      fence_mbar_init();
+    }
     tc::fence_before();
     named_bar(1, kNCT);
     tc::fence_after();
