@@ -108,7 +108,7 @@ __device__ __forceinline__ long long rowcost(const GG& g) {
 // Split-K of tcgen05 groups: a group of whole 128-row tiles whose tiles are too few to fill the grid
 // is cut into ks column segments of >= kMinSegBlocks 128-column blocks.  A unit (tile, segment)
 // writes its fp32 partial tile to scratch; the last unit of a tile to finish (atomic ticket) adds the
-// partials in segment order and runs the epilogue.  ks depends only on the group's shape and the grid.
+// partials in segment order and runs the epilogue.  ks depends on the group's shape and the launch's (phase's) total work.
 constexpr int kMinSegBlocks = 4;
 
 __device__ __forceinline__ int anchor_index(const Dims& D, int layer_done) {
@@ -283,10 +283,20 @@ static __device__ int finish_groups(const EngineCfg& p, GG* gg, int ng, int cap)
     o.tr = (short)(o.tc ? tc::kRows : kSlots / o.nw);
     o.ks = 1;
     o.vrows = o.rows;
-    if (o.tc && p.B.tc_part && o.rows % tc::kRows == 0 &&
+    cost += (long long)o.rows * rowcost(o);
+  }
+  // a CTA's share of the launch (or phase); a tcgen05 tile costing more than one share is split so
+  // that each of its units costs about half a share (the tiles of a phase that carries other work
+  // usually fit, and stay whole)
+  const long long share = cost / gridDim.x + 1;
+  cost = 0;
+  for (int g = 0; g < ng; ++g) {
+    GG& o = gg[g];
+    const long long tile_cost = (long long)tc::kRows * rowcost(o);
+    if (o.tc && p.B.tc_part && tile_cost > share && o.rows % tc::kRows == 0 &&
         (o.epi != EPI_QKV || (o.seg1 % tc::kRows == 0 && o.seg2 % tc::kRows == 0))) {
       const int ntile = o.rows / tc::kRows, ncb = o.cols / (tc::kStageCh * tc::kChunk);
-      int ks = (2 * (int)gridDim.x + ntile - 1) / ntile;  // about two units per CTA from this group alone
+      int ks = (int)((2 * tile_cost + share - 1) / share);
       ks = min(ks, ncb / kMinSegBlocks);
       const int nvp = o.nv <= 16 ? 16 : 32;
       const int need = ntile * ks * o.nw * tc::kRows * nvp;
@@ -960,9 +970,48 @@ __device__ void tc_tile(const EngineCfg& p, const GG& G, int r, int tr, Ring& R,
   const bool pairs = G.epi == EPI_QKV && r < G.seg2;
   const bool wok = __all_sync(0xffffffffu, ok);  // tcgen05.ld is warp-collective
   const int row = 32 * warp + lane;              // tile-local physical row (warps 0-3)
+  // The tile's results go to shared memory, ya[row][v] (hi + lo of accumulator 0) and yb[row][v]
+  // (accumulator 1: the up projection), then all 256 threads run the epilogues, items (row, v) with
+  // consecutive rows on consecutive threads; each thread first loads every epilogue input of its
+  // items (residual values, rotary cos / sin) and then computes, so the loads overlap.
+  float* ya = reinterpret_cast<float*>(scratch);
+  float* yb = ya + tc::kRows * NVP;
+  constexpr int MAXK = tc::kRows * NVP / NCT;  // items per thread
+  auto run_epilogues = [&]() {
+    const int nitem = tc::kRows * nv;
+    float pre[MAXK][2];
+#pragma unroll
+    for (int k = 0; k < MAXK; ++k) {
+      const int idx = tid + k * NCT, rw = idx % tc::kRows, v = idx / tc::kRows;
+      pre[k][0] = pre[k][1] = 0.f;
+      if (idx < nitem && rw < tr) {
+        if (G.epi == EPI_RESID) {
+          pre[k][0] = __ldcg(G.y + (size_t)((G.yrow0 + v) % G.yring) * G.ystride + r + rw);
+        } else if (pairs && (r + rw) % hd < hd / 2) {
+          const size_t at = (size_t)(G.pos0 + v - 1) * (hd / 2) + (r + rw) % hd;
+          pre[k][0] = __ldg(p.B.rope_cos + at);
+          pre[k][1] = __ldg(p.B.rope_sin + at);
+        }
+      }
+    }
+#pragma unroll
+    for (int k = 0; k < MAXK; ++k) {
+      const int idx = tid + k * NCT, rw = idx % tc::kRows, v = idx / tc::kRows;
+      if (idx >= nitem || rw >= tr) continue;
+      const float y0 = ya[rw * NVP + v];
+      if (pairs) {
+        if ((r + rw) % hd < hd / 2)  // tiles start on a head boundary
+          epilogue<WT>(p, G, v, r + rw, y0, ya[(rw + hd / 2) * NVP + v], true, loc, pre[k]);
+      } else if (G.nw == 2) {
+        epilogue<WT>(p, G, v, r + rw, y0, yb[rw * NVP + v], false, loc);
+      } else {
+        epilogue<WT>(p, G, v, r + rw, y0, 0.f, false, loc, G.epi == EPI_RESID ? pre[k] : nullptr);
+      }
+    }
+  };
   if (G.ks > 1) {
     // split-K unit: partial tile [acc][vector][128 rows] to scratch; the last unit of the tile adds
-    // the ks partials in segment order and runs the epilogue
+    // the ks partials in segment order into ya / yb and runs the epilogues
     __shared__ int s_last_unit;
     const int usz = G.nw * NVP * tc::kRows;
     float* pu = p.B.tc_part + G.pbase + (size_t)unit * usz;
@@ -992,69 +1041,56 @@ __device__ void tc_tile(const EngineCfg& p, const GG& G, int r, int tr, Ring& R,
     if (s_last_unit && wok) {
       __threadfence();
       const float* pt = p.B.tc_part + G.pbase + (size_t)(unit / G.ks) * G.ks * usz;
-      auto sum = [&](int acc, int v, int rw) {
-        float a = 0.f;
-        for (int sg = 0; sg < G.ks; ++sg) a += __ldcg(pt + (size_t)sg * usz + (size_t)(acc * NVP + v) * tc::kRows + rw);
-        return a;
-      };
-      for (int idx = tid; idx < tc::kRows * nv; idx += NCT) {
-        const int rw = idx % tc::kRows, v = idx / tc::kRows;
-        if (rw >= tr) continue;
-        if (pairs) {
-          const int i = (r + rw) % hd;  // tiles start on a head boundary
-          if (i < hd / 2) epilogue<WT>(p, G, v, r + rw, sum(0, v, rw), sum(0, v, rw + hd / 2), true, loc);
-        } else if (G.nw == 2) {
-          epilogue<WT>(p, G, v, r + rw, sum(0, v, rw), sum(1, v, rw), false, loc);
-        } else {
-          epilogue<WT>(p, G, v, r + rw, sum(0, v, rw), 0.f, false, loc);
+      // element e = (acc * NVP + v) * 128 + row of the tile, summed over the segments in order; four
+      // elements per thread at a time with all their loads issued together
+      const int nel = G.nw * NVP * tc::kRows;
+      for (int e0 = tid; e0 < nel; e0 += 4 * NCT) {
+        float acc4[4] = {0.f, 0.f, 0.f, 0.f};
+        for (int sg = 0; sg < G.ks; ++sg) {
+          float vv[4];
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const int e = e0 + q * NCT;
+            vv[q] = e < nel ? __ldcg(pt + (size_t)sg * usz + e) : 0.f;
+          }
+#pragma unroll
+          for (int q = 0; q < 4; ++q) acc4[q] += vv[q];
         }
-      }
-    }
-    tc::fence_before();
-    named_bar(1, NCT);  // TMEM is rewritten by the next tile
-    return;
-  }
-  float* xch = reinterpret_cast<float*>(scratch);  // [128 rows][NVP vectors]: RoPE partner values
-  if (pairs) {
-    if (warp < 4 && wok) {
 #pragma unroll
-      for (int v0 = 0; v0 < NVP; v0 += 16) {
-        uint32_t dh[16], dl[16];
-        tc::load_rows16(T.tmem + v0, warp, dh);
-        tc::load_rows16(T.tmem + NVP + v0, warp, dl);
-#pragma unroll
-        for (int v = 0; v < 16; ++v) xch[row * NVP + v0 + v] = __uint_as_float(dh[v]) + __uint_as_float(dl[v]);
+        for (int q = 0; q < 4; ++q) {
+          const int e = e0 + q * NCT;
+          if (e < nel) {
+            const int rw = e % tc::kRows, av = e / tc::kRows, acc = av / NVP, v = av % NVP;
+            (acc ? yb : ya)[rw * NVP + v] = acc4[q];
+          }
+        }
       }
     }
     named_bar(1, NCT);
-    if (wok && warp < 4 && row < tr) {
-      const int i = (r + row) % hd;  // tiles start on a head boundary
-      if (i < hd / 2)
-        for (int v = 0; v < nv; ++v)
-          epilogue<WT>(p, G, v, r + row, xch[row * NVP + v], xch[(row + hd / 2) * NVP + v], true, loc);
-    }
-  } else if (warp < 4 && wok) {
+    if (s_last_unit && wok) run_epilogues();
+    tc::fence_before();
+    named_bar(1, NCT);  // TMEM and the shared buffers are rewritten by the next tile
+    return;
+  }
+  if (warp < 4 && wok) {
 #pragma unroll
     for (int v0 = 0; v0 < NVP; v0 += 16) {
       if (v0 >= nv) break;
-      uint32_t dh[16], dl[16], uh[16], ul[16];
+      uint32_t dh[16], dl[16];
       tc::load_rows16(T.tmem + v0, warp, dh);
       tc::load_rows16(T.tmem + NVP + v0, warp, dl);
+#pragma unroll
+      for (int v = 0; v < 16; ++v) ya[row * NVP + v0 + v] = __uint_as_float(dh[v]) + __uint_as_float(dl[v]);
       if (G.nw == 2) {
-        tc::load_rows16(T.tmem + kAcc + v0, warp, uh);
-        tc::load_rows16(T.tmem + kAcc + NVP + v0, warp, ul);
-      }
-      if (row < tr) {
-        for (int v = 0; v < 16 && v0 + v < nv; ++v) {
-          const float y0 = __uint_as_float(dh[v]) + __uint_as_float(dl[v]);
-          if (G.nw == 2)
-            epilogue<WT>(p, G, v0 + v, r + row, y0, __uint_as_float(uh[v]) + __uint_as_float(ul[v]), false, loc);
-          else
-            epilogue<WT>(p, G, v0 + v, r + row, y0, 0.f, false, loc);
-        }
+        tc::load_rows16(T.tmem + kAcc + v0, warp, dh);
+        tc::load_rows16(T.tmem + kAcc + NVP + v0, warp, dl);
+#pragma unroll
+        for (int v = 0; v < 16; ++v) yb[row * NVP + v0 + v] = __uint_as_float(dh[v]) + __uint_as_float(dl[v]);
       }
     }
   }
+  named_bar(1, NCT);
+  if (wok) run_epilogues();
   tc::fence_before();
   named_bar(1, NCT);  // TMEM and `scratch` are rewritten by the next tile
 }
