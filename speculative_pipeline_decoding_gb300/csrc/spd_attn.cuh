@@ -387,13 +387,20 @@ __device__ __forceinline__ void load_q(const Dims& D, const Tile& T, int kh, int
   }
 }
 
-// Query heads qh0, qh0 + qstep, ... of item `it` on the calling warp; q0 holds query head qh0
-// (loaded ahead by the caller).  ks / vs: the chunk's K and V rows in shared memory; qb: hd floats
-// of per-warp scratch.  Writes one partial (o, m, l) per query head; no ticket.
+constexpr int kHeadsPerPass = 4;  // query heads a warp item computes together
+
+// Query heads qh0, qh0 + qstep, ... of item `it` on the calling warp, up to four at a time: each K
+// row chunk and each V row slice is read once from shared memory for all the heads of a pass, and
+// the heads' dot products, softmax reductions and output sums are independent chains that overlap.
+// q0[h] holds the lane's slice of query head qh0 + h*qstep (loaded ahead by the caller, first pass).
+// ks / vs: the chunk's K and V rows in shared memory; qb: 4*hd floats of per-warp scratch.  Writes
+// one partial (o, m, l) per query head; no ticket.  Each head's arithmetic is the same whatever
+// heads share its pass.
 template <typename WT, int DPL>
 __device__ void warp_item(const Dims& D, const Tile& T, const Item& it, const WT* ks, const WT* vs, float* qb,
-                          int qh0, int qstep, const float* q0) {
+                          int qh0, int qstep, const float (*q0)[DPL]) {
   constexpr int CK = kWarpCK;
+  constexpr int HP = kHeadsPerPass;
   constexpr int VEC = WTraits<WT>::kVec;  // elements per 16-byte chunk of a K row
   const int lane = threadIdx.x & 31;
   const int hd = D.hd;
@@ -402,67 +409,102 @@ __device__ void warp_item(const Dims& D, const Tile& T, const Item& it, const WT
   const int QH = T.nq * D.gq;
   const int kh = it.kh, c = it.c, nk = it.nk;
   const int key0 = c * CK;
-  float qc[DPL];
+  for (int g0 = qh0; g0 < QH; g0 += HP * qstep) {
+    // this pass's query vectors -> shared memory (the lane's slice of each)
 #pragma unroll
-  for (int e = 0; e < DPL; ++e) qc[e] = q0[e];
-  for (int qh = qh0; qh < QH; qh += qstep) {
-    const int pos_q = T.pos0 + qh / D.gq;
-    const bool more = qh + qstep < QH;
-    float qn[DPL];
-    if (more) load_q<DPL>(D, T, kh, qh + qstep, qn);  // next query head in flight
+    for (int h = 0; h < HP; ++h) {
+      const int qh = g0 + h * qstep;
+      if (qh < QH) {
+        float qv[DPL];
+        if (g0 == qh0) {
 #pragma unroll
-    for (int e = 0; e < DPL; ++e) qb[lane * DPL + e] = qc[e];
+          for (int e = 0; e < DPL; ++e) qv[e] = q0[h][e];
+        } else {
+          load_q<DPL>(D, T, kh, qh, qv);
+        }
+#pragma unroll
+        for (int e = 0; e < DPL; ++e) qb[h * hd + lane * DPL + e] = qv[e];
+      }
+    }
     __syncwarp();
-    // score of key `lane`: four partial sums (element e % 4), added at the end
-    float d4[4] = {0.f, 0.f, 0.f, 0.f};
+    // score of key `lane` for every head of the pass: four partial sums each (element e % 4)
+    float d4[HP][4];
+#pragma unroll
+    for (int h = 0; h < HP; ++h) d4[h][0] = d4[h][1] = d4[h][2] = d4[h][3] = 0.f;
     if (lane < nk) {
       const WT* kr = ks + (size_t)lane * hd;
-#pragma unroll 4
+#pragma unroll 2
       for (int j = 0; j < nchk; ++j) {
         const int jj = (j + lane) % nchk;
         float kf[VEC];
         WTraits<WT>::unpack(*reinterpret_cast<const uint4*>(kr + jj * VEC), kf);
-        const float* qv = qb + jj * VEC;
 #pragma unroll
-        for (int e = 0; e < VEC; e += 4) {
-          const float4 q4 = *reinterpret_cast<const float4*>(qv + e);
-          d4[0] = fmaf(kf[e], q4.x, d4[0]);
-          d4[1] = fmaf(kf[e + 1], q4.y, d4[1]);
-          d4[2] = fmaf(kf[e + 2], q4.z, d4[2]);
-          d4[3] = fmaf(kf[e + 3], q4.w, d4[3]);
+        for (int h = 0; h < HP; ++h) {
+          if (g0 + h * qstep < QH) {
+            const float* qv = qb + h * hd + jj * VEC;
+#pragma unroll
+            for (int e = 0; e < VEC; e += 4) {
+              const float4 q4 = *reinterpret_cast<const float4*>(qv + e);
+              d4[h][0] = fmaf(kf[e], q4.x, d4[h][0]);
+              d4[h][1] = fmaf(kf[e + 1], q4.y, d4[h][1]);
+              d4[h][2] = fmaf(kf[e + 2], q4.z, d4[h][2]);
+              d4[h][3] = fmaf(kf[e + 3], q4.w, d4[h][3]);
+            }
+          }
         }
       }
     }
-    const float dot = (d4[0] + d4[1]) + (d4[2] + d4[3]);
-    const float sk = (lane < nk && key0 + lane < pos_q) ? dot * scale : -INFINITY;
-    float m = sk;
+    float pk[HP], mh[HP], lh[HP];
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-    const float pk = (m == -INFINITY) ? 0.f : expf(sk - m);
-    float l = pk;
+    for (int h = 0; h < HP; ++h) {
+      const int qh = g0 + h * qstep;
+      const int pos_q = T.pos0 + (qh < QH ? qh : 0) / D.gq;
+      const float dot = (d4[h][0] + d4[h][1]) + (d4[h][2] + d4[h][3]);
+      const float sk = (qh < QH && lane < nk && key0 + lane < pos_q) ? dot * scale : -INFINITY;
+      mh[h] = sk;
+      pk[h] = sk;
+    }
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) l += __shfl_xor_sync(0xffffffffu, l, o);
-    // unnormalised chunk output, dims lane*DPL ..
-    float acc[DPL];
+    for (int o = 16; o > 0; o >>= 1)
 #pragma unroll
-    for (int e = 0; e < DPL; ++e) acc[e] = 0.f;
-#pragma unroll 8
+      for (int h = 0; h < HP; ++h) mh[h] = fmaxf(mh[h], __shfl_xor_sync(0xffffffffu, mh[h], o));
+#pragma unroll
+    for (int h = 0; h < HP; ++h) {
+      pk[h] = (mh[h] == -INFINITY) ? 0.f : expf(pk[h] - mh[h]);
+      lh[h] = pk[h];
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1)
+#pragma unroll
+      for (int h = 0; h < HP; ++h) lh[h] += __shfl_xor_sync(0xffffffffu, lh[h], o);
+    // unnormalised chunk outputs, dims lane*DPL ..; each V slice is loaded once for all heads
+    float acc[HP][DPL];
+#pragma unroll
+    for (int h = 0; h < HP; ++h)
+#pragma unroll
+      for (int e = 0; e < DPL; ++e) acc[h][e] = 0.f;
+#pragma unroll 4
     for (int k = 0; k < nk; ++k) {
-      const float pj = __shfl_sync(0xffffffffu, pk, k);
       float vf[DPL];
       load_row<WT, DPL>(vs + (size_t)k * hd + lane * DPL, vf);
 #pragma unroll
-      for (int e = 0; e < DPL; ++e) acc[e] = fmaf(pj, vf[e], acc[e]);
-    }
-    float* rec = T.part + ((size_t)T.rec_off + ((size_t)kh * T.nch + c) * QH + qh) * (hd + 2);
+      for (int h = 0; h < HP; ++h) {
+        const float pj = __shfl_sync(0xffffffffu, pk[h], k);
 #pragma unroll
-    for (int e = 0; e < DPL; ++e) rec[lane * DPL + e] = acc[e];
-    if (lane == 0) { rec[hd] = m; rec[hd + 1] = l; }
-    __syncwarp();  // qb is rewritten by the next query head
-    if (more) {
-#pragma unroll
-      for (int e = 0; e < DPL; ++e) qc[e] = qn[e];
+        for (int e = 0; e < DPL; ++e) acc[h][e] = fmaf(pj, vf[e], acc[h][e]);
+      }
     }
+#pragma unroll
+    for (int h = 0; h < HP; ++h) {
+      const int qh = g0 + h * qstep;
+      if (qh < QH) {
+        float* rec = T.part + ((size_t)T.rec_off + ((size_t)kh * T.nch + c) * QH + qh) * (hd + 2);
+#pragma unroll
+        for (int e = 0; e < DPL; ++e) rec[lane * DPL + e] = acc[h][e];
+        if (lane == 0) { rec[hd] = mh[h]; rec[hd + 1] = lh[h]; }
+      }
+    }
+    __syncwarp();  // qb is rewritten by the next pass
   }
 }
 

@@ -205,22 +205,28 @@ __device__ void attn_consume(const Dims& D, const att::Tile* tb, int nt, const A
   };
   att::Item it{0, 0, 0, 0};
   int g = -1;
-  float qv[DPL];
-  auto fetch = [&](int qpos) {  // identity of the item at qpos and its first query head
+  constexpr int HP = att::kHeadsPerPass;
+  float qv[HP][DPL];
+  auto fetch = [&](int qpos) {  // identity of the item at qpos and its first pass of query heads
     int pass = 0;
     g = qpos < qend ? attn_item_at(A, qpos, pass) : -1;
     if (g >= 0) {
       it = att::item_of_pass(tb, nt, pass, g, att::kWarpCK);
-      if (qh0 < tb[it.T].nq * D.gq) att::load_q<DPL>(D, tb[it.T], it.kh, qh0, qv);
+      const int QH = tb[it.T].nq * D.gq;
+#pragma unroll
+      for (int h = 0; h < HP; ++h)
+        if (qh0 + h * wpi < QH) att::load_q<DPL>(D, tb[it.T], it.kh, qh0 + h * wpi, qv[h]);
     }
   };
   fetch(warp / wpi);
   for (int q = warp / wpi; q < qend; q += qstride) {
     const att::Item cur = it;
     const int gcur = g;
-    float qc[DPL];
+    float qc[HP][DPL];
 #pragma unroll
-    for (int e = 0; e < DPL; ++e) qc[e] = qv[e];
+    for (int h = 0; h < HP; ++h)
+#pragma unroll
+      for (int e = 0; e < DPL; ++e) qc[h][e] = qv[h][e];
     fetch(q + qstride);
     const uint32_t ctr = R.ctr + (uint32_t)(q / ips);
     const int s = ctr % kStages;
@@ -484,7 +490,7 @@ __global__ void __launch_bounds__(kStepThreads, 1) step_kernel(const __grid_cons
       const int nt = s_nt[b];
       const AttnPlan A = attn_plan(s_nold[b], s_nnew[b], ips);
       const int nst = nt > 0 ? A.stages(ips) : 0;
-      float* qb = reinterpret_cast<float*>(uni) + (size_t)warp * D.hd;
+      float* qb = reinterpret_cast<float*>(uni) + (size_t)warp * att::kHeadsPerPass * D.hd;
       if (D.hd == 64) attn_consume<WT, 2>(D, tb, nt, A, nst, ips, item_bytes, R, qb, &s_fail, st, s_mlist, &s_mcount);
       else attn_consume<WT, 4>(D, tb, nt, A, nst, ips, item_bytes, R, qb, &s_fail, st, s_mlist, &s_mcount);
       R.ctr += (uint32_t)nst;
@@ -537,7 +543,7 @@ static_assert(sizeof(DevState) % 16 == 0 && sizeof(LayerW) % 16 == 0, "16-byte s
 // (control).
 static size_t step_union_bytes(const Dims& D) {
   size_t uni = (size_t)kMmaScratch;
-  const size_t q = (size_t)kNCW * D.hd * sizeof(float);
+  const size_t q = (size_t)kNCW * att::kHeadsPerPass * D.hd * sizeof(float);
   if (uni < q) uni = q;
   if (uni < (size_t)kNCW * 32 * 2 * sizeof(Top2)) uni = (size_t)kNCW * 32 * 2 * sizeof(Top2);
   return (uni + 127) & ~(size_t)127;

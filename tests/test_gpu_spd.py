@@ -667,6 +667,46 @@ def test_sampled_spd_and_ar_match_oracle(request, setup, thr, opts):
     print(setup, opts, "sampled SPD first mismatch", j, "AR", ja, "accepts", sum(accepted), "/", len(accepted))
 
 
+# temperatures other than 1 (both sides divide each logit by T in fp32 before the weights) and a
+# top-k that is not the pages' 50: a sharper and a flatter distribution
+@pytest.mark.parametrize("T,k,seed", [(0.6, 8, 77), (1.7, 64, 31)])
+@pytest.mark.parametrize("setup,thr", [("tiny_setup", 1e-4), ("small_setup", 1e-3)])
+def test_sampled_other_temperatures_match_oracle(request, setup, thr, T, k, seed):
+    S = request.getfixturevalue(setup)
+    target, pdm = S.models
+    first, arr, u = _uniforms(S, seed)
+    S.eng.set_sampling(T, k, first, arr)
+    try:
+        S.eng.rollback(S.P, S.first)
+        toks, stats = S.eng.generate(S.G)
+        toks = toks.tolist()
+        trace = S.eng.dump(DUMP_TRACE)[:, : S.eng.state()["exits"]]
+        S.eng.rollback(S.P, S.first)
+        ar, _ = S.eng.generate_ar(S.G)
+        ar = ar.tolist()
+    finally:
+        S.eng.set_sampling(0.0)
+    smp = {"T": T, "k": k, "u_draft": u["draft"], "u_accept": u["accept"], "u_resample": u["resample"]}
+    run = ospd.SPDRun(target, pdm, S.w.n_stages, S.w.pdm_layers, S.w.anchors, S.prompt,
+                      S.P + S.G + S.w.n_stages + 2, sampling=smp)
+    ref = run.generate(S.G)
+    j = _first_mismatch(toks, ref)
+    if j is not None:
+        q = S.P + 1 + j
+        assert min([m for p, m in run.margins if p <= q] + [1.0]) < thr, (j, toks[j:j + 3], ref[j:j + 3])
+    upto = S.G if j is None else j
+    assert [bool(x) for x in trace[1][:upto - 1]] == [ok for _, ok in run.trace][:upto - 1]
+    assert stats["cycles"] == ospd.expected_cycles(S.w.n_stages, [bool(x) for x in trace[1]])
+    ora = osm.sampled_ar(target, S.prompt, S.G, T, k, u["ar"])
+    ja = _first_mismatch(ar, ora["tokens"])
+    if ja is not None:
+        assert min(ora["margins"][:ja] + [1.0]) < thr, (ja, ar[ja:ja + 3], ora["tokens"][ja:ja + 3])
+    # the output is a draw, not the greedy stream: at T = 1.7 over 64 tokens it leaves argmax early
+    if T > 1.0:
+        assert ar != S.ar[: len(ar)]
+    print(setup, T, k, "sampled SPD first mismatch", j, "AR", ja, "accepts", int(trace[1].sum()), "/", trace.shape[1])
+
+
 # ------------------------------------------------------------------------------------------------
 # degenerate shapes: a one-stage pipeline (n = 1: the exiting token verifies the draft of the same
 # cycle, SPD degenerates to AR with a draft per step) on a one-token prompt
