@@ -835,18 +835,18 @@ struct TcCtx {
   uint32_t tmem;          // TMEM address of column 0
   uint64_t* done;         // arrives when every MMA of the tile has completed
   uint32_t phase;
-  uint64_t* bfull;        // [kStages]: the 8 consumer warps have written the slot's B (8 arrivals)
+  uint64_t* bfull;        // [kStages]: the 7 builder warps have written the slot's B (7 arrivals)
   uint32_t bphase;        // bit s: parity of bfull[s]'s next completion (kept by the issuing thread)
 };
 
 // tcgen05 tile: output rows r..r+tr-1 (physical rows; whole heads in the rotary region) of a group of
-// nv <= NVP vectors (NVP = 16 or 32).  Per stage the consumers build B (high and low halves of the
-// normalised activations of the stage's 128 columns: rows v and NVP+v) once the stage's weights
-// have landed -- which also means the MMAs that last read that B slot are done -- then one thread
-// issues the 8 MMAs and commits them to the stage's empty barrier in place of warp 0's arrival, so the
-// producer refills the slot only after the tensor core has read it.  At the tile end warps 0-3 read
-// their 32 TMEM lanes (rows) 16 vectors at a time and run the epilogue of every vector; RoPE partners
-// (row + hd/2) are exchanged through `scratch`.
+// nv <= NVP vectors (NVP = 16 or 32).  Thread 0 only issues: per stage it waits for the weights and
+// for B, issues the 8 MMAs and commits them to the stage's empty barrier in place of warp 0's
+// arrival, so the producer refills the slot only after the tensor core has read it.  Warps 1-7 build
+// B (high and low halves of the normalised activations of the stage's 128 columns: rows v and NVP+v)
+// as soon as its slot is free.  At the tile end warps 0-3 read their 32 TMEM lanes (rows) 16 vectors
+// at a time and all 256 threads run the epilogues; RoPE partners (row + hd/2) are exchanged through
+// `scratch`.
 template <typename WT, int NVP>
 __device__ void tc_tile(const EngineCfg& p, const GG& G, int r, int tr, Ring& R, TcCtx& T, unsigned char* scratch,
                         const float* rstd_s, Top2* loc, int cb0, int cb1, int unit) {
@@ -854,35 +854,41 @@ __device__ void tc_tile(const EngineCfg& p, const GG& G, int r, int tr, Ring& R,
   constexpr int kB = tc::Shape<NVP>::kB;
   constexpr int kBBytes = tc::Shape<NVP>::kBBytes;
   constexpr uint32_t kAcc = tc::Shape<NVP>::kAccCols;
-  constexpr int NPT = NVP / 16;  // (vector, 8-column piece) pairs per thread and stage
+  constexpr int kBuilders = NCT - 32;                          // warps 1-7
+  constexpr int NI = (NVP * 16 + kBuilders - 1) / kBuilders;   // B items per builder thread (2 or 3)
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int hd = p.D.hd, nv = G.nv;
   DevState* st = p.B.st;
-  // B of a stage: thread t builds the 8 columns 8*(t%16).. of vectors t/16 + 16 i (i < NPT), both
-  // halves (row v: high, row NVP+v: low); the vectors' rows and 1/rms are resolved once per tile
-  const int bpc = tid & 15;
-  const float* bx[NPT];
-  float brs[NPT];
-  uint32_t boff_hi[NPT], boff_lo[NPT];
+  // B of a stage is NVP x 16 items (vector, 8-column piece), both halves of each; builder b = tid - 32
+  // builds items b + kBuilders i (i < NI), which share the piece (kBuilders is a multiple of 16): the
+  // 8 columns 8*(b%16).. of vectors (b + kBuilders i)/16.  Rows and 1/rms are resolved once per tile.
+  const int bb = tid - 32;
+  const int bpc = bb & 15;
+  const float* bx[NI];
+  float brs[NI];
+  uint32_t boff_hi[NI], boff_lo[NI];
 #pragma unroll
-  for (int i = 0; i < NPT; ++i) {
-    const int bv = (tid >> 4) + 16 * i;
-    bx[i] = bv < nv ? G.x + (size_t)((G.xrow0 + bv) % G.xring) * G.xstride : nullptr;
-    brs[i] = (bv < nv && G.normw) ? rstd_s[bv] : 1.f;
-    boff_hi[i] = (uint32_t)((bpc >> 3) * kB * 128 + bv * 128 + (((bpc & 7) ^ (bv & 7)) << 4));
-    boff_lo[i] = (uint32_t)((bpc >> 3) * kB * 128 + (NVP + bv) * 128 + (((bpc & 7) ^ ((NVP + bv) & 7)) << 4));
+  for (int i = 0; i < NI; ++i) {
+    const int item = bb + kBuilders * i;
+    const int bv = item >> 4;
+    const bool use = warp != 0 && item < NVP * 16;
+    bx[i] = (use && bv < nv) ? G.x + (size_t)((G.xrow0 + bv) % G.xring) * G.xstride : nullptr;
+    brs[i] = (use && bv < nv && G.normw) ? rstd_s[bv] : 1.f;
+    boff_hi[i] = use ? (uint32_t)((bpc >> 3) * kB * 128 + bv * 128 + (((bpc & 7) ^ (bv & 7)) << 4)) : 0xffffffffu;
+    boff_lo[i] = use ? (uint32_t)((bpc >> 3) * kB * 128 + (NVP + bv) * 128 + (((bpc & 7) ^ ((NVP + bv) & 7)) << 4))
+                     : 0xffffffffu;
   }
   // The stage's activations and norm weights of this thread come from L2 (each stage touches new
   // columns), so they are loaded one column block ahead into registers.  Two register sets take
   // turns; the column-block loop is unrolled by two so that each set keeps a fixed name.
   constexpr int CB = tc::kStageCh * tc::kChunk;  // columns per stage
   const int ncb = cb1;                            // blocks [cb0, cb1) of this tile (unit)
-  float4 xa[NPT][2], xb[NPT][2], na[2], nb[2];
+  float4 xa[NI][2], xb[NI][2], na[2], nb[2];
   auto fetch = [&](int cb, float4 (*xr)[2], float4* nr) {
     if (cb < ncb) {
       const int col = cb * CB + 8 * bpc;
 #pragma unroll
-      for (int i = 0; i < NPT; ++i)
+      for (int i = 0; i < NI; ++i)
         if (bx[i]) {
           xr[i][0] = *reinterpret_cast<const float4*>(bx[i] + col);
           xr[i][1] = *reinterpret_cast<const float4*>(bx[i] + col + 4);
@@ -895,7 +901,8 @@ __device__ void tc_tile(const EngineCfg& p, const GG& G, int r, int tr, Ring& R,
   };
   auto build_b = [&](unsigned char* b, const float4 (*x4)[2], const float4* n4) {
 #pragma unroll
-    for (int i = 0; i < NPT; ++i) {
+    for (int i = 0; i < NI; ++i) {
+      if (boff_hi[i] == 0xffffffffu) continue;  // no item (vectors >= nv still get zero rows)
       uint4 hi = make_uint4(0u, 0u, 0u, 0u), lo = hi;
       if (bx[i]) {
         float xv[8] = {x4[i][0].x, x4[i][0].y, x4[i][0].z, x4[i][0].w, x4[i][1].x, x4[i][1].y, x4[i][1].z, x4[i][1].w};
@@ -919,45 +926,64 @@ __device__ void tc_tile(const EngineCfg& p, const GG& G, int r, int tr, Ring& R,
       *reinterpret_cast<uint4*>(b + boff_lo[i]) = lo;
     }
   };
-  // the nw stages (gate, up) of column block cb from set (x, n); block cb+1 prefetched into (xp, np)
+  // Builders (warps 1-7): the nw stages (gate, up) of column block cb from set (x, n); block cb+1
+  // prefetched into (xp, np).  B of a stage does not depend on its weights, so it is built as soon as
+  // its slot is free -- when ring slot s was last released (its empty barrier completed for the stage
+  // kStages back, which for a tensor-core stage means its MMAs are done).  A builder warp releases the
+  // ring slot with its B report: the slot completes only with thread 0's commit, which follows the
+  // MMAs.  The builders run up to kStages stages ahead of the tensor core.
   auto block = [&](int cb, const float4 (*x)[2], const float4* n, float4 (*xp)[2], float4* np) {
     fetch(cb + 1, xp, np);
     for (int h = 0; h < G.nw; ++h) {
       const int s = R.ctr % kStages;
-      if (!R.failed && !mbar_wait_bounded(&R.full[s], (R.ctr / kStages) & 1)) {
-        if (lane == 0) set_err(st, ERR_TIMEOUT, 61);
+      if (R.ctr >= (uint32_t)kStages && !R.failed &&
+          !mbar_wait_bounded(&R.empty[s], ((R.ctr / kStages) - 1) & 1)) {
+        if (lane == 0) set_err(st, ERR_TIMEOUT, 64);
         R.failed = true;
       }
-      unsigned char* bs = T.bring + (size_t)s * kBBytes;
-      if (!R.failed) build_b(bs, x, n);
+      if (!R.failed) build_b(T.bring + (size_t)s * kBBytes, x, n);
       tc::fence_async_smem();
       __syncwarp();
-      // no CTA-wide barrier: each warp reports its part of B and moves on to the next stage; the
-      // issuing thread waits for the eight reports of this slot
-      if (lane == 0) mbar_arrive(&T.bfull[s]);
-      if (tid == 0) {
-        const bool bok = !R.failed && mbar_wait_bounded(&T.bfull[s], (T.bphase >> s) & 1u);
-        T.bphase ^= 1u << s;
-        if (bok) {
-          tc::fence_after();
-          // gate / up accumulators in columns [0, kAcc) / [kAcc, 2 kAcc)
-          tc::mma_stage<NVP>(T.tmem + kAcc * (uint32_t)h, R.base + (size_t)s * kStageBytes, bs, cb == cb0);
-          tc::commit(&R.empty[s]);  // warp 0's arrival, when the MMAs have read the stage
-        } else {
-          if (!R.failed) { set_err(st, ERR_TIMEOUT, 63); R.failed = true; }
-          mbar_arrive(&R.empty[s]);
-        }
-      } else if (warp != 0 && lane == 0) {
+      if (lane == 0) {
+        mbar_arrive(&T.bfull[s]);
         mbar_arrive(&R.empty[s]);
       }
       ++R.ctr;
     }
   };
-  fetch(cb0, xa, na);
-  for (int cb = cb0; cb < ncb; cb += 2) {
-    block(cb, xa, na, xb, nb);
-    if (cb + 1 < ncb) block(cb + 1, xb, nb, xa, na);
+  const int nstages = (ncb - cb0) * G.nw;
+  if (warp != 0) {
+    fetch(cb0, xa, na);
+    for (int cb = cb0; cb < ncb; cb += 2) {
+      block(cb, xa, na, xb, nb);
+      if (cb + 1 < ncb) block(cb + 1, xb, nb, xa, na);
+    }
+  } else if (tid == 0) {
+    // the issuer: per stage the weights and B of the slot, then the MMAs (gate / up accumulators in
+    // columns [0, kAcc) / [kAcc, 2 kAcc)); after a failed wait it still releases every slot
+    for (int k = 0; k < nstages; ++k) {
+      const int s = R.ctr % kStages, h = k % G.nw, cb = cb0 + k / G.nw;
+      if (!R.failed && !mbar_wait_bounded(&R.full[s], (R.ctr / kStages) & 1)) {
+        set_err(st, ERR_TIMEOUT, 61);
+        R.failed = true;
+      }
+      const bool bok = !R.failed && mbar_wait_bounded(&T.bfull[s], (T.bphase >> s) & 1u);
+      T.bphase ^= 1u << s;
+      if (bok) {
+        tc::fence_after();
+        tc::mma_stage<NVP>(T.tmem + kAcc * (uint32_t)h, R.base + (size_t)s * kStageBytes,
+                           T.bring + (size_t)s * kBBytes, cb == cb0);
+        tc::commit(&R.empty[s]);  // warp 0's arrival, when the MMAs have read the stage
+      } else {
+        if (!R.failed) { set_err(st, ERR_TIMEOUT, 63); R.failed = true; }
+        mbar_arrive(&R.empty[s]);
+      }
+      ++R.ctr;
+    }
+  } else {
+    R.ctr += (uint32_t)nstages;  // lanes 1-31 of warp 0 wait at the tile end
   }
+  __syncwarp();
   // tile end: every MMA done -> TMEM rows to registers -> epilogues.  The completion is committed
   // whatever happened (it arrives once the MMAs issued so far are done, at once if there are none),
   // so the barrier's phase stays in step with T.phase on the failure path too.

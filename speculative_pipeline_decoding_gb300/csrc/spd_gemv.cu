@@ -81,7 +81,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_engine(const __grid_constant
     if (warp == 0) tc::alloc_cols(&s_tmem, tc::kColsGemv);
     if (tid == 0) {
       mbar_init(&s_tc_done, 1);
-      for (int i = 0; i < kStages; ++i) mbar_init(&s_tc_bfull[i], kNCW);
+      for (int i = 0; i < kStages; ++i) mbar_init(&s_tc_bfull[i], kNCW - 1);  // the builder warps
       fence_mbar_init();
     }
     tc::fence_before();

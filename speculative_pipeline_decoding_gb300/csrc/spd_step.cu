@@ -465,7 +465,7 @@ __global__ void __launch_bounds__(kStepThreads, 1) step_kernel(const __grid_cons
     if (warp == 0) tc::alloc_cols(&s_tmem, tc::kColsStep);
     if (tid == 0) {
       mbar_init(&s_tc_done, 1);
-      for (int i = 0; i < kStages; ++i) mbar_init(&s_tc_bfull[i], kNCW);
+      for (int i = 0; i < kStages; ++i) mbar_init(&s_tc_bfull[i], kNCW - 1);  // the builder warps
       fence_mbar_init();
     }
     tc::fence_before();
