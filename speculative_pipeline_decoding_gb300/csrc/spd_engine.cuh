@@ -57,7 +57,7 @@ constexpr int kSlots = 64;                     // weight rows per stage (2 boxes
 constexpr int kStageBytes = kSlots * 512;      // 4 boxes wide
 constexpr int kStages = 4;
 constexpr int kMaxMT = 2;                      // tensor-core path: up to 2 m-tiles of 16 vectors
-constexpr int kCostSV = 2, kCostMma = 3;       // split cost of a weight byte: a tensor-core stage of
+constexpr int kCostSV = 4, kCostMma = 6;       // split cost of a weight byte: an mma.sync stage of
                                                // the draft rows takes ~1.5x a single-vector stage
                                                // streamed alongside it (measured per CTA)
 // tensor-core path scratch: the warps' partial tiles of one m-tile
@@ -99,8 +99,9 @@ struct EngineCfg {
 };
 
 // split cost of one output row: its weight elements, weighted by the path's cost per byte
-constexpr int kCostTc = 4;  // a tcgen05 tile byte takes ~2x a single-vector byte streamed alongside it
-                            // (per-CTA phase times of the co-scheduled cycle, 9B-class model)
+constexpr int kCostTc = 6;  // a tcgen05 tile byte is weighted 1.5x a single-vector byte streamed
+                            // alongside it: the best of 1.0, 1.25, 1.5 and 2 in the co-scheduled
+                            // cycle of the 9B-class model (tok/s 180, 192, 199, 188)
 __device__ __forceinline__ long long rowcost(const GG& g) {
   return (long long)(g.cols / g.ks) * g.nw * (g.tc ? kCostTc : (g.mma ? kCostMma : kCostSV));
 }
