@@ -604,10 +604,11 @@ def main_spd(args):
 
 
 def main_profile(args):
-    """Prefill, G plain AR steps (the reference stream for the draft overrides), then K SPD cycles,
-    all launched one by one without graphs.  Under a profiler the launch sequence is fixed: set-up
-    and prefill kernels, G step-kernel launches (AR), then exactly one step-kernel launch per cycle,
-    so `-k regex:step_kernel -s <G + warm-up cycles>` selects steady-state cycles."""
+    """Prefill, G - 1 plain AR steps (the reference stream for the draft overrides; the first token
+    comes from the prefill), then K SPD cycles, all launched one by one without graphs.  Under a
+    profiler the launch sequence is fixed: set-up and prefill kernels, G - 1 step-kernel launches
+    (AR), then exactly one step-kernel launch per cycle, so `-k regex:step_kernel -s <G - 1 + c>`
+    selects cycle c (c >= n: a full pipeline)."""
     import torch
     import spd_inputs as si
     import speculative_pipeline_decoding_gb300 as spd
@@ -624,7 +625,7 @@ def main_profile(args):
     eng = spd.Engine(spd.Config.from_workload(w), params)
     eng.set_options(B.OPT_DEFAULT & ~B.OPT_GRAPHS)
     first = eng.prefill(prompt)
-    ar, _ = eng.generate_ar(G)  # G step-kernel launches, one per token: the reference stream
+    ar, _ = eng.generate_ar(G)  # G - 1 step-kernel launches, one per token: the reference stream
     eng.rollback(P, first)
     eng.set_acceptance(alpha, w.coin_seed, ar)
     t0 = time.time()
