@@ -9,7 +9,8 @@ no flush is needed between steps.  Prints ONE JSON line on rank 0.
 
 Default workload: the 9B-class model (L 32, d 4096, 32 q / 8 kv heads x 128, ffn 12288, vocab
 151936, bf16) at n = 8, Ls = 4, prompt 2048, 512 tokens, alpha 0.9 (its other acceptance rate, 0.5,
-and the 1.5B-class and 4B-class workloads are reported under extra keys).
+and the 1.5B-class, the 4B-class and the 4B-class 32K-context workloads are reported under extra
+keys).
 
   python bench.py [--gpus N --steps K --warmup W --workload NAME --alpha A]
   python bench.py --impl reference      # the CPU oracle timed on the host cores
@@ -30,7 +31,7 @@ sys.path.insert(0, ROOT)
 
 METRIC = "committed tokens/s (1 seq, greedy SPD n=8) and cycle HBM GB/s vs peak"
 DEFAULT_WORKLOAD = "gqa9b_bf16_n8"
-EXTRA_WORKLOADS = ("dense1.5b_bf16_n8", "gqa4b_bf16_n8")
+EXTRA_WORKLOADS = ("dense1.5b_bf16_n8", "gqa4b_bf16_n8", "gqa4b_bf16_n8_ctx32k")
 SPEC_HBM_GBS = 8000.0
 TRAFFIC_FILE = os.path.join("profiles", "step_kernel_traffic.json")
 
